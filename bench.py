@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""Benchmark of the Llama-3-style decoder block on GB300.
+
+Default workload: one Llama-3 8B-shaped decode block step at batch 32 with 1000
+cached positions (pos = 1000, keys 0..1000 read), bf16, seeded synthetic
+weights N(0, 0.02), x and cache N(0, 1).  A "step" is one full pass of the
+block (RMSNorm, QKV + RoPE + KV append, attention, O + residual, RMSNorm,
+gate/up + SwiGLU, down + residual) for every sequence of the batch; it rewrites
+cache row 1000, so steps are idempotent.  The weights (436 MB) are larger than
+L2 (126 MB), so every step streams them from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl ours|reference]
+
+Prints one JSON line.  `--impl reference` times the CPU oracle (the plain
+NumPy definition of the block) on a bounded sample of the same workload on the
+host cores.  Under torchrun each rank runs an independent replica (the path
+needs no exchange between GPUs): value = tokens of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "decode block tok/s & HBM-roofline frac; prefill block TFLOP/s vs bf16 peak"
+POS = 1000
+MAX_SEQ = 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def decode_step_bytes(dims, B, pos):
+    from_bytes = 2
+    d, f = dims.d_model, dims.d_ff
+    q, kv = dims.n_heads * dims.head_dim, dims.n_kv_heads * dims.head_dim
+    weights = d * (q + 2 * kv) + q * d + 3 * d * f + 2 * d
+    kv_read = 2 * B * dims.n_kv_heads * (pos + 1) * dims.head_dim
+    kv_write = 2 * B * kv
+    act = 2 * B * d
+    return from_bytes * (weights + kv_read + kv_write + act)
+
+
+def gateup_launch_bytes(dims, B):
+    """Algorithmic bytes of one gate/up projection launch: both weight matrices once,
+    the normalised input read, the SwiGLU output written."""
+    return 2 * (2 * dims.d_ff * dims.d_model + B * dims.d_model + B * dims.d_ff)
+
+
+def prefill_flops(dims, B, T):
+    d, f = dims.d_model, dims.d_ff
+    q, kv = dims.n_heads * dims.head_dim, dims.n_kv_heads * dims.head_dim
+    macs = d * (q + 2 * kv) + q * d + 3 * d * f
+    pairs = T * (T + 1) // 2
+    return B * (2 * macs * T + 4 * dims.n_heads * dims.head_dim * pairs)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags) if fl == "Active"})
+        top = max(r[0] for r in rows)
+        loaded = [r[0] for r in rows if r[0] >= 0.5 * top] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- traffic from the committed ncu summary
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_decoder_block_gb300", "csrc")
+    for f in ("gemm_tc.cuh", "gemm_weight_stream.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key: str):
+    """dram read+write bytes per launch recorded in profiles/ for this kernel, or None
+    when there is none or the kernel source changed since it was captured."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    digest = kernel_source_digest()
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(pdir, f)).read()
+        m = re.search(rf"traffic\[{re.escape(kernel_key)}\]\s*=\s*([0-9.eE+]+)\s+bytes per launch,\s*source\s+([0-9a-f]+)",
+                      text)
+        if m and m.group(2) == digest:
+            return float(m.group(1))
+    return None
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, device):
+    import dense_decoder_block_gb300 as ddb
+    ddb.lib()
+    dims = workloads.LLAMA3_8B
+    B = args.batch
+    wts = workloads.make_weights(dims, weight_std=0.02)
+    inp = workloads.make_block_inputs(dims, B, 1, cache_len=POS, max_seq=MAX_SEQ, weights=wts)
+    w = {k: v.to(device) for k, v in inp.weights.items()}
+    g = {k: v.to(device) for k, v in inp.gains.items()}
+    blk = ddb.LlamaBlock(dims, w, g, MAX_SEQ)
+    kc, vc = inp.k_cache.to(device), inp.v_cache.to(device)
+    kv = ddb.KVCache(kc, vc)
+    x = inp.x.to(device)
+    y = torch.empty_like(x)
+    ws = blk.workspace(B, 1)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        blk.decode(x, kv, POS, y, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    assert blk.poll_error() == 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+
+    # --- timed region: K steps, device-side events on the launching stream
+    gpu_index = device.index if device.index is not None else 0
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if visible:
+        try:
+            gpu_index = int(visible.split(",")[gpu_index])
+        except (ValueError, IndexError):
+            pass
+    with ClockSampler(gpu_index) as clk:
+        time.sleep(0.3)
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        barrier()
+        ms = t0.elapsed_time(t1)
+    clocks = clk.summary()
+    ms_step = ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        ms_step = ms / args.steps
+    tokens = B * world * args.steps
+    value = tokens / (ms / 1e3)
+
+    # --- per-stage durations (second pass, events between the block's kernels)
+    stage_ms = stage_profile(blk, x, kv, y, ws, stream, args.steps)
+
+    # --- end to end through the public API with host buffers
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    xh.copy_(inp.x)
+    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    for _ in range(args.warmup):
+        x.copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens / (e2e_ms / 1e3)
+    assert blk.poll_error() == 0
+
+    hbm, bf16_peak, _, peak_kind = peaks()
+    step_bytes = decode_step_bytes(dims, B, POS)
+    gu_bytes = gateup_launch_bytes(dims, B)
+    gu_ms = stage_ms.get("gate_up")
+    roof = None
+    if gu_ms:
+        ach = gu_bytes / (gu_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "gate/up projection + SwiGLU (weight-streaming tcgen05)",
+                "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                "traffic": committed_traffic("gate_up_decode_b%d" % B),
+                "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_us": round(gu_ms * 1e3, 2)}
+    step_ach = step_bytes / (ms_step / 1e3) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) x and KV cache)",
+        "config": {"workload": f"Llama-3 8B-shaped decode block, batch {B}, 1000 cached positions (pos 1000)",
+                   "batch": B, "pos": POS, "keys_read": POS + 1, "d_model": dims.d_model,
+                   "heads": f"{dims.n_heads}q/{dims.n_kv_heads}kv", "head_dim": dims.head_dim, "d_ff": dims.d_ff,
+                   "l2": "inputs larger than L2: 436 MB of weights streamed per step (L2 126 MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "step_hbm": {"algorithmic_bytes": step_bytes, "achieved_gbs": round(step_ach, 1),
+                     "frac": round(step_ach / hbm, 4), "peak_gbs": hbm, "peak_kind": peak_kind},
+        "roofline": roof,
+        "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tok/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": y.numel() * y.element_size()},
+        "gpu_launches": args.steps * blk_launches_per_decode(),
+    }
+    if args.extra and rank == 0:
+        out["extra"] = extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind)
+    return out
+
+
+def blk_launches_per_decode():
+    # rmsnorm, qkv, attention chunks, attention combine, o, rmsnorm, gate/up, down
+    return 8
+
+
+STAGES = ("rmsnorm_1", "qkv", "attention", "o_proj", "rmsnorm_2", "gate_up", "down")
+
+
+def stage_profile(blk, x, kv, y, ws, stream, steps):
+    """Average device time of each stage of the decode step, from CUDA events the
+    library records between its kernels on the launching stream."""
+    import dense_decoder_block_gb300 as ddb
+    n = len(STAGES) + 1
+    sums = [0.0] * len(STAGES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(steps)]
+    for s in range(steps):
+        ddb.llama_block_set_stage_events(blk.h, evs[s])
+        blk.decode(x, kv, POS, y, ws)
+    ddb.llama_block_set_stage_events(blk.h, None)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        for i in range(len(STAGES)):
+            sums[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+    return {name: sums[i] / steps for i, name in enumerate(STAGES)}
+
+
+def time_region(fn, steps, warmup, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind):
+    """Other batch sizes of the decode workload and the prefill workload (T = 512,
+    2048, 8192), each timed on its own."""
+    res = {}
+    w = {k: v.to(device) for k, v in wts[0].items()}
+    g = {k: v.to(device) for k, v in wts[1].items()}
+    stream = torch.cuda.current_stream(device)
+    for B in (1, 8):
+        inp = workloads.make_block_inputs(dims, B, 1, cache_len=POS, max_seq=MAX_SEQ, weights=wts)
+        blk = ddb.LlamaBlock(dims, w, g, MAX_SEQ)
+        kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+        x = inp.x.to(device)
+        y = torch.empty_like(x)
+        ws = blk.workspace(B, 1)
+        ms = time_region(lambda: blk.decode(x, kv, POS, y, ws), 50, 5, stream)
+        by = decode_step_bytes(dims, B, POS)
+        res[f"decode_b{B}"] = {"tok_s": round(B / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
+                               "hbm_frac": round(by / (ms / 1e3) / 1e9 / hbm, 4)}
+    for T in (512, 2048, 8192):
+        inp = workloads.make_block_inputs(dims, 1, T, max_seq=T, weights=wts, poison_tail=False)
+        blk = ddb.LlamaBlock(dims, w, g, T)
+        kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+        x = inp.x.to(device)
+        y = torch.empty_like(x)
+        ws = blk.workspace(1, T)
+        steps = 10 if T < 8192 else 3
+        ms = time_region(lambda: blk.prefill(x, kv, y, ws), steps, 2, stream)
+        fl = prefill_flops(dims, 1, T)
+        tf = fl / (ms / 1e3) / 1e12
+        res[f"prefill_t{T}"] = {"tok_s": round(T / (ms / 1e3), 1), "ms": round(ms, 3), "tflops": round(tf, 1),
+                                "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind}
+    return res
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_decode_sample(dims, wts32, seqs: int):
+    """Time the oracle (fp32 arrays, bf16 rounding points emulated) on `seqs`
+    sequences of the decode workload; returns (seconds, tokens)."""
+    from oracle import block as ob
+    from oracle.bf16 import round_bf16
+    inp = workloads.make_block_inputs(dims, seqs, 1, cache_len=POS, max_seq=MAX_SEQ,
+                                      weights=wts32["torch"], poison_tail=False)
+    x = inp.x.float().numpy()
+    kc = inp.k_cache.float().numpy()
+    vc = inp.v_cache.float().numpy()
+    t0 = time.perf_counter()
+    ob.block_forward(x, wts32["w"], wts32["g"], dims, kc, vc, POS, round_bf16)
+    return time.perf_counter() - t0, seqs
+
+
+def oracle_weights32(dims):
+    wts = workloads.make_weights(dims, weight_std=0.02)
+    return {"torch": wts, "w": {k: v.float().numpy() for k, v in wts[0].items()},
+            "g": {k: v.float().numpy() for k, v in wts[1].items()}}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count()
+
+
+def cpu_baseline_line(dims, seqs=2, reps=3):
+    w32 = oracle_weights32(dims)
+    oracle_decode_sample(dims, w32, 1)   # warm caches / BLAS threads
+    tot_s, tot_tok = 0.0, 0
+    for _ in range(reps):
+        s, t = oracle_decode_sample(dims, w32, seqs)
+        tot_s += s
+        tot_tok += t
+    return {"value": round(tot_tok / tot_s, 3), "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{reps} x {seqs} sequences of the batch-32 decode step (fp32 NumPy oracle, "
+                      f"bf16 rounding emulated), {tot_s:.1f} s total"}
+
+
+def run_reference(args):
+    dims = workloads.LLAMA3_8B
+    w32 = oracle_weights32(dims)
+    for _ in range(args.warmup):
+        oracle_decode_sample(dims, w32, 1)
+    t_total, tok = 0.0, 0
+    for _ in range(args.steps):
+        s, t = oracle_decode_sample(dims, w32, 1)
+        t_total += s
+        tok += t
+    value = tok / t_total
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) x and KV cache)",
+        "config": {"workload": f"Llama-3 8B-shaped decode block, batch {args.batch}, 1000 cached positions "
+                               f"(pos 1000); each reference step is one sequence of that batch",
+                   "batch": args.batch, "pos": POS},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{args.steps} steps x 1 sequence of the decode step, fp32 NumPy oracle"},
+        "e2e": {"value": round(value, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-extra", dest="extra", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    out = run_ours(args, rank, world, device)
+    if rank == 0 and args.cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline_line(workloads.LLAMA3_8B)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

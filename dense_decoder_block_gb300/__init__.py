@@ -1,0 +1,198 @@
+"""GB300 (sm_103a) Llama-3-style decoder block: Python binding of libllama_block.so.
+
+The functions here keep the C ABI's names and only marshal arguments (torch
+tensors -> device pointers, the current CUDA stream -> cudaStream_t); every
+step of the block runs in the library's CUDA kernels.  There is no fallback:
+importing works without the library, but every call raises if it is missing.
+
+    blk = LlamaBlock(dims, weights)            # weights: dict of CUDA tensors
+    ws = blk.workspace(batch, tokens)
+    blk.prefill(x, kv, y, ws)                  # x, y [B, T, d]
+    blk.decode(x, kv, pos, y, ws)              # x, y [B, 1, d]
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Dict, Optional
+
+import torch
+
+from . import _native
+from ._native import (LLAMA_BF16, LLAMA_F32, LLAMA_OK, LLAMA_ERR_INVALID_ARG, LLAMA_ERR_UNSUPPORTED_DIMS,
+                      LLAMA_ERR_POS_RANGE, LLAMA_ERR_WORKSPACE, LLAMA_ERR_CUDA, LLAMA_ERR_DEVICE_TIMEOUT,
+                      llama_block_dims, llama_block_weights, llama_kv_cache)
+
+__all__ = [
+    "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_destroy",
+    "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_decode", "llama_block_decode_devpos",
+    "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_embed", "llama_lmhead_workspace_bytes",
+    "llama_lmhead_argmax", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
+]
+
+
+class LlamaError(RuntimeError):
+    def __init__(self, code: int, msg: str = ""):
+        self.code = code
+        super().__init__(f"{_native.ERROR_NAMES.get(code, code)}: {msg}")
+
+
+def lib():
+    return _native.load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the block library must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the block library must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return LLAMA_BF16
+    if dt == torch.float32:
+        return LLAMA_F32
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+# ----------------------------------------------------------------------------- same-named wrappers
+
+def llama_block_create(dims: llama_block_dims, weights: llama_block_weights) -> C.c_void_p:
+    h = C.c_void_p()
+    rc = lib().llama_block_create(C.byref(dims), C.byref(weights), C.byref(h))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_block_create")
+    return h
+
+
+def llama_block_destroy(h) -> None:
+    lib().llama_block_destroy(h)
+
+
+def llama_block_workspace_bytes(h, batch: int, tokens: int) -> int:
+    return int(lib().llama_block_workspace_bytes(h, batch, tokens))
+
+
+def llama_block_last_error(h) -> str:
+    r = lib().llama_block_last_error(h)
+    return r.decode() if r else ""
+
+
+def _check(h, rc, what):
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, f"{what}: {llama_block_last_error(h)}")
+
+
+def llama_block_prefill(h, x, batch, tokens, kv: llama_kv_cache, y, ws, ws_bytes, stream=None) -> None:
+    _check(h, lib().llama_block_prefill(h, _ptr(x), batch, tokens, C.byref(kv), _ptr(y), _ptr(ws), ws_bytes,
+                                        _stream(stream)), "llama_block_prefill")
+
+
+def llama_block_decode(h, x, batch, kv: llama_kv_cache, pos, y, ws, ws_bytes, stream=None) -> None:
+    _check(h, lib().llama_block_decode(h, _ptr(x), batch, C.byref(kv), int(pos), _ptr(y), _ptr(ws), ws_bytes,
+                                       _stream(stream)), "llama_block_decode")
+
+
+def llama_block_decode_devpos(h, x, batch, kv: llama_kv_cache, pos_dev, y, ws, ws_bytes, stream=None) -> None:
+    _check(h, lib().llama_block_decode_devpos(h, _ptr(x), batch, C.byref(kv), _ptr(pos_dev), _ptr(y), _ptr(ws),
+                                              ws_bytes, _stream(stream)), "llama_block_decode_devpos")
+
+
+def llama_block_set_stage_events(h, events) -> None:
+    """events: None, or a list of LLAMA_BLOCK_STAGES + 1 torch.cuda.Event (enable_timing=True)."""
+    if events is None:
+        rc = lib().llama_block_set_stage_events(h, None, 0)
+    else:
+        arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
+        rc = lib().llama_block_set_stage_events(h, arr, len(events))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_block_set_stage_events")
+
+
+def llama_block_poll_error(h, stream=None) -> int:
+    return int(lib().llama_block_poll_error(h, _stream(stream)))
+
+
+def llama_rmsnorm(x, g, y, rows, d, eps, stream=None) -> None:
+    rc = lib().llama_rmsnorm(_ptr(x), _ptr(g), _ptr(y), rows, d, C.c_float(eps), _dtype_code(x.dtype),
+                             _stream(stream))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_rmsnorm")
+
+
+def llama_embed(ids, n_tokens, w_embed, vocab, d_model, x, err_dev=None, stream=None) -> None:
+    rc = lib().llama_embed(_ptr(ids), n_tokens, _ptr(w_embed), vocab, d_model, _ptr(x), _ptr(err_dev),
+                           _stream(stream))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_embed")
+
+
+def llama_lmhead_workspace_bytes(batch, d_model, vocab) -> int:
+    return int(lib().llama_lmhead_workspace_bytes(batch, d_model, vocab))
+
+
+def llama_lmhead_argmax(h, batch, h_stride, g_final, w_out, vocab, d_model, eps, ids, logits, ws, ws_bytes,
+                        stream=None) -> None:
+    rc = lib().llama_lmhead_argmax(_ptr(h), batch, h_stride, _ptr(g_final), _ptr(w_out), vocab, d_model,
+                                   C.c_float(eps), _ptr(ids), _ptr(logits), _ptr(ws), ws_bytes, _stream(stream))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_lmhead_argmax")
+
+
+# ----------------------------------------------------------------------------- convenience
+
+class KVCache:
+    """K and V buffers [batch, n_kv_heads, max_seq, head_dim] (caller-owned torch tensors)."""
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor):
+        assert k.shape == v.shape and k.dim() == 4
+        self.k, self.v = k, v
+        self.c = llama_kv_cache(C.c_void_p(k.data_ptr()), C.c_void_p(v.data_ptr()), k.shape[0], k.shape[2])
+
+
+class LlamaBlock:
+    """Owns a handle; borrows the weight tensors (kept referenced here)."""
+
+    def __init__(self, dims, weights: Dict[str, torch.Tensor], gains: Dict[str, torch.Tensor], max_seq: int):
+        dt = weights["wq"].dtype
+        self.dims = dims
+        self._keep = dict(weights, **gains)
+        self.c_dims = llama_block_dims(dims.d_model, dims.n_heads, dims.n_kv_heads, dims.head_dim, dims.d_ff,
+                                       max_seq, dims.eps, dims.rope_theta, _dtype_code(dt))
+        names = ("g_attn", "wq", "wk", "wv", "wo", "g_ffn", "w_gate", "w_up", "w_down")
+        self.c_w = llama_block_weights(*[_ptr(self._keep[n]) for n in names])
+        self.h = llama_block_create(self.c_dims, self.c_w)
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h is not None and _native._lib is not None:
+            llama_block_destroy(h)
+            self.h = None
+
+    def workspace_bytes(self, batch: int, tokens: int) -> int:
+        return llama_block_workspace_bytes(self.h, batch, tokens)
+
+    def workspace(self, batch: int, tokens: int, device=None) -> torch.Tensor:
+        n = self.workspace_bytes(batch, tokens)
+        return torch.empty(n, dtype=torch.uint8, device=device or self._keep["wq"].device)
+
+    def prefill(self, x, kv: KVCache, y, ws, stream=None):
+        B, T = x.shape[0], x.shape[1]
+        llama_block_prefill(self.h, x, B, T, kv.c, y, ws, ws.numel(), stream)
+
+    def decode(self, x, kv: KVCache, pos: int, y, ws, stream=None):
+        llama_block_decode(self.h, x, x.shape[0], kv.c, pos, y, ws, ws.numel(), stream)
+
+    def decode_devpos(self, x, kv: KVCache, pos_dev, y, ws, stream=None):
+        llama_block_decode_devpos(self.h, x, x.shape[0], kv.c, pos_dev, y, ws, ws.numel(), stream)
+
+    def poll_error(self, stream=None) -> int:
+        return llama_block_poll_error(self.h, stream)

@@ -1,0 +1,47 @@
+// Shared device/host definitions of the block library (not part of the public ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/llama_block.h"
+
+namespace llama {
+
+using bf16 = __nv_bfloat16;
+
+// Keys per attention chunk: the unit of the softmax partial (m, l, o) that both
+// the prefill and the decode attention kernels produce and fold in ascending order.
+constexpr int kAttnChunk = 128;
+// K-segment length (elements) of every bf16 projection: each output is the
+// ascending fp32 sum of per-segment tensor-core accumulations of this length,
+// in prefill and decode alike.
+constexpr int kSegK = 1024;
+constexpr int kRopeMaxPairs = 64;   // head_dim <= 128
+
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+__device__ __forceinline__ float ld_bf16(const bf16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// RMSNorm row scale 1/sqrt(ss/d + eps), correctly rounded steps.
+__device__ __forceinline__ float rms_scale(float sumsq, int d, float eps) {
+    float ms = __fdiv_rn(sumsq, (float)d);
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// Adjacent-pair rotation of one element: this thread holds `self` at an even
+// (first) or odd (second) index of the pair, `other` is its partner.
+//   first:  a' = a cos - b sin      second: b' = a sin + b cos
+__device__ __forceinline__ float rope_rotate_elem(float self, float other, float c, float s, bool second) {
+    return second ? __fmaf_rn(other, s, __fmul_rn(self, c)) : __fmaf_rn(self, c, __fmul_rn(-other, s));
+}
+
+// SiLU(z) = z / (1 + e^-z)
+__device__ __forceinline__ float silu_f(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, expf(-z))); }
+
+}  // namespace llama

@@ -1,0 +1,116 @@
+// Host side of the tcgen05 projection kernel: TMA descriptors, schedule choice, launch.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm_tc.cuh"
+
+namespace llama {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    std::string* why) {
+    auto fn = encode_fn();
+    if (!fn) {
+        if (why) *why = "cuTensorMapEncodeTiled unavailable from the driver";
+        return false;
+    }
+    if (((uintptr_t)base & 15) != 0 || (cols * 2) % 16 != 0) {
+        if (why) *why = "TMA needs a 16-byte aligned base and rows that are a multiple of 16 bytes";
+        return false;
+    }
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled failed (code " + std::to_string((int)r) + ")";
+        return false;
+    }
+    return true;
+}
+
+int pick_gemm_path(const GemmProblem& p, int path) {
+    if (path == PATH_AUTO) return p.M <= 32 ? PATH_WEIGHT_STREAM : PATH_TOKEN_TILED;
+    return path;
+}
+
+static int n_segments(const GemmProblem& p) { return (p.K + kSegK - 1) / kSegK; }
+
+size_t gemm_partial_bytes(const GemmProblem& p, int path) {
+    if (pick_gemm_path(p, path) != PATH_WEIGHT_STREAM) return 0;
+    const int segs = n_segments(p);
+    if (segs <= 1) return 0;
+    return (size_t)segs * p.M * (p.dual ? 2 : 1) * p.F * sizeof(float);
+}
+
+int gemm_counter_slots(const GemmProblem& p) { return p.F / kTileF; }
+
+// Instantiated in gemm_token_tiled.cu / gemm_weight_stream.cu
+cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
+                               const CUtensorMap& a1, const CUtensorMap& a2, const bf16* x, cudaStream_t s);
+cudaError_t launch_weight_stream(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
+                                 const CUtensorMap& a1, const CUtensorMap& a2, const bf16* x, cudaStream_t s);
+
+cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, unsigned* counters,
+                        cudaStream_t s) {
+    if (p.M <= 0) return cudaSuccess;
+    if (p.F % kTileF != 0 || p.K % kBlockK != 0) return cudaErrorInvalidValue;
+    GemmKArgs ka{};
+    ka.M = p.M;
+    ka.F = p.F;
+    ka.K = p.K;
+    ka.seg_kb = kSegK / kBlockK;
+    ka.n_segs = n_segments(p);
+    ka.e = e;
+    ka.partial = partial;
+    ka.counters = counters;
+    const CUtensorMap& a0 = *p.a_maps[0];
+    const CUtensorMap& a1 = p.a_maps[1] ? *p.a_maps[1] : a0;
+    const CUtensorMap& a2 = p.a_maps[2] ? *p.a_maps[2] : a0;
+    if (e.kind == EPI_QKV) {
+        ka.q_tiles = e.n_heads;
+        ka.k_tiles = e.n_kv_heads;
+    }
+    const int chosen = pick_gemm_path(p, path);
+    if (chosen == PATH_WEIGHT_STREAM) {
+        if (p.M > 32) return cudaErrorInvalidValue;
+        if (ka.n_segs > 1 && (!partial || !counters)) return cudaErrorInvalidValue;
+        return launch_weight_stream(p, ka, a0, a1, a2, p.x, s);
+    }
+    return launch_token_tiled(p, ka, a0, a1, a2, p.x, s);
+}
+
+cudaError_t launch_gemm_single_segment(const GemmProblem& p, const GemmEpi& e, cudaStream_t s) {
+    if (p.M <= 0) return cudaSuccess;
+    if (p.F % kTileF != 0 || p.K % kBlockK != 0 || p.M > 32 || p.dual) return cudaErrorInvalidValue;
+    GemmKArgs ka{};
+    ka.M = p.M;
+    ka.F = p.F;
+    ka.K = p.K;
+    ka.seg_kb = p.K / kBlockK;
+    ka.n_segs = 1;
+    ka.e = e;
+    const CUtensorMap& a0 = *p.a_maps[0];
+    return launch_weight_stream(p, ka, a0, a0, a0, p.x, s);
+}
+
+}  // namespace llama

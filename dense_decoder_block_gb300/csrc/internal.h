@@ -1,0 +1,101 @@
+// Host-side interfaces between the library's translation units (not public ABI).
+#pragma once
+#include <string>
+
+#include "common.cuh"
+
+namespace llama {
+
+enum EpiKind : int {
+    EPI_QKV = 0,     // RoPE on q/k tiles, q -> workspace, k/v -> cache rows
+    EPI_RESID = 1,   // y = bf16(resid + bf16(acc))
+    EPI_SWIGLU = 2,  // y = bf16(bf16(silu(bf16(gate))) * bf16(up)), two accumulators
+    EPI_PLAIN = 3,   // y = bf16(acc)
+    EPI_LOGITS = 4,  // y_f32 = acc
+};
+
+// Everything the GEMM epilogue needs.  Device pointers.
+struct GemmEpi {
+    int kind = EPI_PLAIN;
+    bf16* out = nullptr;          // [M, F] (QKV: q [M, n_heads*128])
+    const bf16* resid = nullptr;  // [M, F]
+    float* out_f32 = nullptr;     // [M, F]
+    // QKV / RoPE / cache append
+    bf16* kc = nullptr;
+    bf16* vc = nullptr;
+    int n_heads = 0, n_kv_heads = 0, kv_seq = 0;   // cache row stride = kv_seq * 128
+    int tokens_per_seq = 1;                         // token n -> (n / T, n % T)
+    int start_pos = 0;                              // position of token t = base + t
+    const int* pos_dev = nullptr;                   // if set, base = *pos_dev
+    int max_pos = 0;                                // positions must be < max_pos
+    const float* cos_tab = nullptr;                 // [max_pos, 64]
+    const float* sin_tab = nullptr;
+    int* err = nullptr;
+};
+
+// One projection: Y[M, F] = X[M, K] . W^T with W given as up to three row
+// blocks (wq / wk / wv) or as the gate/up pair (dual).
+struct GemmProblem {
+    int M = 0, F = 0, K = 0;
+    const CUtensorMap* a_maps[3] = {nullptr, nullptr, nullptr};   // host copies, [rows, K] bf16
+    int n_maps = 1;
+    bool dual = false;           // a_maps[0] = gate, a_maps[1] = up, F = d_ff
+    const bf16* x = nullptr;     // [M, K] bf16, row stride K
+};
+
+enum GemmPath : int { PATH_AUTO = 0, PATH_TOKEN_TILED = 1, PATH_WEIGHT_STREAM = 2 };
+
+// Scratch for the weight-streaming path: fp32 partials and per-tile counters.
+size_t gemm_partial_bytes(const GemmProblem& p, int path);
+int gemm_counter_slots(const GemmProblem& p);
+int pick_gemm_path(const GemmProblem& p, int path);
+
+cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, unsigned* counters,
+                        cudaStream_t s);
+
+// Whole-K dot products per CTA (no segment split), weight-streaming, M <= 32.
+// For outputs that have no token-tiled counterpart (the LM head logits).
+cudaError_t launch_gemm_single_segment(const GemmProblem& p, const GemmEpi& e, cudaStream_t s);
+
+// 2-D bf16 TMA descriptor, 128-byte swizzle, box = [box_rows, 64].
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    std::string* why);
+
+// ---------------------------------------------------------------- other kernels
+cudaError_t launch_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype,
+                           unsigned* zero_words, int n_zero, cudaStream_t s);
+
+// Attention (SIMT).  q, o [M, Hq*dh]; caches [Bc, Hkv, kv_seq, dh].
+struct AttnArgs {
+    const void* q = nullptr;
+    void* o = nullptr;
+    const void* kc = nullptr;
+    const void* vc = nullptr;
+    int batch = 0, tokens = 0;          // M = batch * tokens
+    int n_heads = 0, n_kv_heads = 0, head_dim = 0, kv_seq = 0;
+    int start_pos = 0;
+    const int* pos_dev = nullptr;
+    int max_pos = 0;
+    int dtype = LLAMA_BF16;
+    float* partial = nullptr;           // decode: [B, Hkv, n_chunks, n_rep, head_dim + 2]
+    int n_chunks = 0;                   // decode: chunk slots per (b, kv head)
+    int* err = nullptr;
+};
+size_t attn_decode_partial_bytes(int batch, int n_kv_heads, int n_chunks, int n_rep, int head_dim);
+cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
+
+// fp32 SIMT block pieces
+cudaError_t launch_linear_f32(const float* x, const float* w, const float* w2, const float* resid, float* y, int M,
+                              int F, int K, int mode, cudaStream_t s);   // mode 0 plain, 1 resid, 2 swiglu
+cudaError_t launch_rope_append_f32(const float* qkv_q, const float* qkv_k, const float* qkv_v, float* q_out,
+                                   float* kc, float* vc, int M, int T, int n_heads, int n_kv_heads, int head_dim,
+                                   int kv_seq, int start_pos, const int* pos_dev, int max_pos,
+                                   const float* cos_tab, const float* sin_tab, int* err, cudaStream_t s);
+
+// stack head
+cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, int d, void* x, int32_t* err,
+                         cudaStream_t s);
+cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, cudaStream_t s);
+
+}  // namespace llama

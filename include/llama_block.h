@@ -1,0 +1,186 @@
+/*
+ * llama_block.h — C ABI of the GB300 (sm_103a) Llama-3-style decoder block library.
+ *
+ * One pre-norm decoder block, forward pass only, in causal prefill and in
+ * KV-cached decode:
+ *
+ *     h = x + Attn(RMSNorm_1(x))          y = h + SwiGLU_FFN(RMSNorm_2(h))
+ *
+ * as defined by "Llama 3.1 70B" (ainfra.dev LLM architecture diagram:
+ * Transformer layer, RMSNorm, Grouped-Query Attention, Residual add, SwiGLU
+ * MLP), "How Llama 3.1 Generates the Next Token" (The transformer blocks,
+ * What's RMSNorm?, What's the SWIGLU block?, RoPE) and "Llama 3 8B · Prepare
+ * Q, K, V" (decode mode: Q/K/V projections, RoPE, K and V cached at KV-head
+ * size).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers to tensors are DEVICE pointers owned by the caller; the
+ *     library never frees them.  Weights are borrowed by the handle and must
+ *     outlive it.  Nothing is copied.
+ *   - Matrices are row-major [out, in] (torch.nn.Linear's storage: y = x W^T).
+ *   - Activations are row-major [B, T, d_model].  The KV cache is two
+ *     buffers K, V of shape [batch, n_kv_heads, max_seq, head_dim].
+ *   - Element type is bf16 (LLAMA_BF16) or fp32 (LLAMA_F32) throughout one
+ *     handle; token ids are int32.
+ *   - Device pointers must be 16-byte aligned; every row length in bytes must
+ *     be a multiple of 16.
+ *   - Work is enqueued on the caller's stream (a cudaStream_t passed as
+ *     void*; NULL = legacy default stream).  No host synchronisation, no
+ *     device allocation and no device-wide barrier happens inside
+ *     prefill/decode, so they may be captured into a CUDA graph.
+ *   - Every function returns LLAMA_OK (0) or a negative LLAMA_ERR_* code;
+ *     nothing throws across the ABI.  llama_block_last_error() returns a
+ *     message for the last failure on that handle.
+ */
+#ifndef LLAMA_BLOCK_H_
+#define LLAMA_BLOCK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LLAMA_OK 0
+#define LLAMA_ERR_INVALID_ARG (-1)      /* null / misaligned pointer, bad size */
+#define LLAMA_ERR_UNSUPPORTED_DIMS (-2) /* dims outside what the kernels implement */
+#define LLAMA_ERR_POS_RANGE (-3)        /* position outside [0, max_seq) */
+#define LLAMA_ERR_WORKSPACE (-4)        /* workspace missing or too small */
+#define LLAMA_ERR_CUDA (-5)             /* a CUDA runtime call failed */
+#define LLAMA_ERR_DEVICE_TIMEOUT (-6)   /* a bounded device-side wait expired */
+
+typedef enum { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
+
+/* Block shape.  n_heads query heads share n_kv_heads K/V heads in groups of
+ * n_heads / n_kv_heads ("Llama 3.1 70B", Grouped-Query Attention).  eps sits
+ * inside the square root of RMSNorm; rope_theta is the RoPE base (omega_i =
+ * theta^(-2i/head_dim), "How Llama 3.1 Generates the Next Token", Why use
+ * different rotation speeds?).  max_seq bounds positions and sizes the
+ * cos/sin table built at create.
+ * bf16 handles need head_dim == 128 and d_model, d_ff multiples of 128;
+ * fp32 handles accept head_dim in {32, 64, 128} and d_model, d_ff multiples
+ * of 4. */
+typedef struct {
+    int32_t d_model, n_heads, n_kv_heads, head_dim, d_ff, max_seq;
+    float eps, rope_theta;
+    int32_t dtype; /* llama_dtype */
+} llama_block_dims;
+
+/* Device pointers, element type = dims.dtype.
+ *   g_attn, g_ffn   [d_model]                 RMSNorm gains
+ *   wq              [n_heads*head_dim, d]     wk, wv [n_kv_heads*head_dim, d]
+ *   wo              [d, n_heads*head_dim]
+ *   w_gate, w_up    [d_ff, d]                 w_down [d, d_ff]
+ * ("How Llama 3.1 Generates the Next Token", Weight dimensions, transposed to
+ * [out, in] as in "Llama 3 8B · Prepare Q, K, V", layers.py excerpt.) */
+typedef struct {
+    const void *g_attn, *wq, *wk, *wv, *wo, *g_ffn, *w_gate, *w_up, *w_down;
+} llama_block_weights;
+
+/* K and V rows are stored after RoPE (K) at KV-head size ("Llama 3 8B ·
+ * Prepare Q, K, V", Explanation).  batch and max_seq describe the buffers;
+ * max_seq may differ from the handle's but positions must fit both. */
+typedef struct {
+    void *k, *v;
+    int32_t batch, max_seq;
+} llama_kv_cache;
+
+typedef struct llama_block_s* llama_block;
+
+/* Validate dims, borrow weight pointers, build the TMA descriptors over the
+ * weights and upload the fp32 cos/sin table [max_seq, head_dim/2] (computed
+ * in fp64 on the host).  This is the only call that allocates device memory
+ * (the table and a 4-byte error word).  On success *out holds the handle. */
+int llama_block_create(const llama_block_dims* dims, const llama_block_weights* w, llama_block* out);
+
+/* Free the handle's table, error word and host state.  NULL is a no-op. */
+void llama_block_destroy(llama_block blk);
+
+/* Bytes of device workspace that prefill (tokens = T) or decode (tokens = 1)
+ * needs for batch B.  Returns 0 for invalid arguments. */
+size_t llama_block_workspace_bytes(llama_block blk, int batch, int tokens);
+
+/* Causal prefill of T tokens per sequence at positions 0..T-1.
+ *   x  [batch, T, d]   input residual stream
+ *   y  [batch, T, d]   output; may alias x
+ *   kv cache rows 0..T-1 of sequences 0..batch-1 are overwritten with the
+ *      rotated keys and the values.
+ * Attention follows "Llama 3.1 70B", Grouped-Query Attention (scaled dot
+ * product, causal, 1/sqrt(head_dim)); the query at position p sees keys 0..p. */
+int llama_block_prefill(llama_block blk, const void* x, int batch, int tokens, const llama_kv_cache* kv, void* y,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step at position pos for every sequence of the batch.
+ *   x [batch, 1, d] in, y [batch, 1, d] out (may alias x).
+ *   kv rows 0..pos-1 must hold the cached keys/values; row pos is written;
+ *   attention reads keys 0..pos (L = pos + 1, "Llama 3 8B · Prepare Q, K, V",
+ *   decode mode) and nothing beyond.
+ * The result for position pos is bit-identical to row pos of a prefill of
+ * the same tokens (both paths share one reduction schedule). */
+int llama_block_decode(llama_block blk, const void* x, int batch, const llama_kv_cache* kv, int pos, void* y,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same as llama_block_decode with the position read on the device from
+ * *pos_dev (int32) when the kernels run, so one captured CUDA graph can be
+ * replayed for successive positions.  The value must lie in [0, max_seq);
+ * a value outside that range makes the kernels record LLAMA_ERR_POS_RANGE in
+ * the handle's error word (read it with llama_block_poll_error); no cache row
+ * is written and y is left undefined. */
+int llama_block_decode_devpos(llama_block blk, const void* x, int batch, const llama_kv_cache* kv,
+                              const int32_t* pos_dev, void* y, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Synchronise `stream`, read and clear the handle's device error word.
+ * Returns LLAMA_OK or the code a kernel recorded (LLAMA_ERR_DEVICE_TIMEOUT,
+ * LLAMA_ERR_POS_RANGE). */
+int llama_block_poll_error(llama_block blk, void* stream);
+
+/* Message of the last failure on this handle ("" if none).  Valid until the
+ * next call on the handle. */
+const char* llama_block_last_error(llama_block blk);
+
+/* Stage timing.  events = NULL disables it; otherwise an array of 8 cudaEvent_t
+ * (passed as void*) that every later prefill/decode on this handle records on
+ * its stream: events[i] before stage i and events[7] after the last, for the
+ * stages RMSNorm_1, QKV+RoPE+append, attention, O+residual, RMSNorm_2,
+ * gate/up+SwiGLU, down+residual.  The array is borrowed until disabled. */
+#define LLAMA_BLOCK_STAGES 7
+int llama_block_set_stage_events(llama_block blk, void* const* events, int n_events);
+
+/* ---------------------------------------------------------------------------
+ * Stack head (32-layer generation loop): embedding gather, final RMSNorm,
+ * LM head with greedy choice.  bf16 only.
+ * ------------------------------------------------------------------------- */
+
+/* x[n, :] = w_embed[ids[n], :] for n < n_tokens ("Llama 3.1 70B", Token
+ * embedding: a row gather, no positional term).  ids int32 in [0, vocab);
+ * an id outside that range writes a zero row and records
+ * LLAMA_ERR_INVALID_ARG in *err_dev (may be NULL). */
+int llama_embed(const int32_t* ids, int n_tokens, const void* w_embed, int vocab, int d_model, void* x,
+                int32_t* err_dev, void* stream);
+
+/* ids[b] = argmax_v (RMSNorm_final(h[b]) . w_out[v]), fp32 logits, ties to the
+ * lowest index ("How Llama 3.1 Generates the Next Token", Unembedding and
+ * Sampling: greedy choice).  h [batch, d_model] (stride h_stride elements
+ * between rows), g_final [d_model], w_out [vocab, d_model].  logits, if not
+ * NULL, receives [batch, vocab] fp32.  workspace: llama_lmhead_workspace_bytes. */
+size_t llama_lmhead_workspace_bytes(int batch, int d_model, int vocab);
+int llama_lmhead_argmax(const void* h, int batch, int h_stride, const void* g_final, const void* w_out, int vocab,
+                        int d_model, float eps, int32_t* ids, float* logits, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Step-level entry points (the block's individual steps, for unit tests and
+ * for callers that compose their own schedule).  Same conventions as above.
+ * ------------------------------------------------------------------------- */
+
+/* y = bf16(bf16(x * r) * g), r = 1/sqrt(mean(x^2) + eps) per row
+ * ("Llama 3.1 70B", RMSNorm reference implementation).  rows x d. */
+int llama_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLAMA_BLOCK_H_ */

@@ -151,7 +151,7 @@ def swiglu_hidden(hn, w_gate, w_up, rnd=round_bf16):
 
 def block_forward(x: np.ndarray, w: Dict[str, np.ndarray], g: Dict[str, np.ndarray], dims,
                   k_cache: np.ndarray, v_cache: np.ndarray, start_pos: int,
-                  rnd=round_bf16, out_rows: Optional[Sequence[int]] = None):
+                  rnd=round_bf16, out_rows: Optional[Sequence[int]] = None, trace: Optional[dict] = None):
     """One decoder block over T new tokens per sequence at positions
     start_pos..start_pos+T-1 (prefill: start_pos = 0; decode: T = 1, start_pos = pos).
 
@@ -161,6 +161,11 @@ def block_forward(x: np.ndarray, w: Dict[str, np.ndarray], g: Dict[str, np.ndarr
     IN PLACE at rows start_pos..start_pos+T-1 (the cache stores K and V at KV-head
     size, [QKV] Explanation).  ``out_rows`` restricts steps 5-9 to those token
     indices (the cache is still filled for all T).  Returns y [B, len(rows), d].
+
+    ``trace``, if given, receives the values just before their last rounding:
+    "y_exact" [B, rows, d], "k_exact" and "v_exact" [B, Hkv, T, dh].  An output
+    stored in bf16 cannot be closer to the exact value than half an ulp, so
+    parity is measured against these.
     """
     B, T, d = x.shape
     hq, hkv, dh = dims.n_heads, dims.n_kv_heads, dims.head_dim
@@ -171,10 +176,15 @@ def block_forward(x: np.ndarray, w: Dict[str, np.ndarray], g: Dict[str, np.ndarr
     for b in range(B):
         xn = rmsnorm(x[b], g["g_attn"], dims.eps, rnd)
         k = rnd(xn @ w["wk"].T).reshape(T, hkv, dh).transpose(1, 0, 2)
-        v = rnd(xn @ w["wv"].T).reshape(T, hkv, dh).transpose(1, 0, 2)
-        k = rnd(rope_rotate(k, ang))
+        v_exact = (xn @ w["wv"].T).reshape(T, hkv, dh).transpose(1, 0, 2)
+        v = rnd(v_exact)
+        k_exact = rope_rotate(k, ang)
+        k = rnd(k_exact)
         k_cache[b, :, start_pos:start_pos + T] = k
         v_cache[b, :, start_pos:start_pos + T] = v
+        if trace is not None:
+            trace.setdefault("k_exact", []).append(k_exact)
+            trace.setdefault("v_exact", []).append(v_exact)
         xr = x[b][rows]
         xnr = xn[rows]
         q = rnd(xnr @ w["wq"].T).reshape(len(rows), hq, dh).transpose(1, 0, 2)
@@ -185,7 +195,13 @@ def block_forward(x: np.ndarray, w: Dict[str, np.ndarray], g: Dict[str, np.ndarr
         h = rnd(xr + rnd(o @ w["wo"].T))
         hn = rmsnorm(h, g["g_ffn"], dims.eps, rnd)
         u = swiglu_hidden(hn, w["w_gate"], w["w_up"], rnd)
-        ys.append(rnd(h + rnd(u @ w["w_down"].T)))
+        y_exact = h + rnd(u @ w["w_down"].T)
+        if trace is not None:
+            trace.setdefault("y_exact", []).append(y_exact)
+        ys.append(rnd(y_exact))
+    if trace is not None:
+        for key in ("k_exact", "v_exact", "y_exact"):
+            trace[key] = np.stack(trace[key])
     return np.stack(ys)
 
 

@@ -1,0 +1,202 @@
+"""GPU parity of the decoder block against the CPU oracle, element by element, at
+sizes the oracle finishes in seconds (several tiles, ragged tails), plus the
+decode/prefill bit-identity contract, error paths and graph replay."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import block as ob
+from tests.blockrun import (BF16_TOL, F32_TOL, check_bf16_output, gpu_block, oracle_weights, rel_err, rnd_for,
+                            run_decode, run_prefill)
+
+pytestmark = pytest.mark.gpu
+
+MID = workloads.BlockDims(d_model=2048, n_heads=16, n_kv_heads=4, head_dim=128, d_ff=4096)
+
+
+def _oracle_prefill(inp, T_total, max_seq, trace=None):
+    w, g = oracle_weights(inp)
+    B = inp.x.shape[0]
+    kc = np.zeros((B, inp.dims.n_kv_heads, max_seq, inp.dims.head_dim))
+    vc = np.zeros_like(kc)
+    x = workloads.to_numpy64(inp.x[:, :T_total])
+    y = ob.block_forward(x, w, g, inp.dims, kc, vc, 0, rnd_for(inp.dtype), trace=trace)
+    return y, kc, vc
+
+
+def _prefill_then_decode(inp, T, steps, max_seq):
+    """GPU: prefill T tokens, then `steps` decode steps; returns y [B, T+steps, d] and caches."""
+    blk, ddb = gpu_block(inp, max_seq)
+    dev = torch.device("cuda:0")
+    kc = inp.k_cache.to(dev)
+    vc = inp.v_cache.to(dev)
+    x = inp.x.to(dev)
+    ys = [run_prefill(blk, ddb, x[:, :T].contiguous(), kc, vc)]
+    for s in range(steps):
+        ys.append(run_decode(blk, ddb, x[:, T + s:T + s + 1].contiguous(), kc, vc, T + s))
+    torch.cuda.synchronize()
+    assert blk.poll_error() == 0
+    return torch.cat(ys, dim=1), kc, vc, blk, ddb
+
+
+@pytest.mark.parametrize("random_gains", [False, True])
+def test_tiny_fp32_prefill16_decode4(random_gains):
+    """The fp32 workload: d=256, 4/2 heads, head_dim 64, prefill 16 then 4 decode steps."""
+    cfg = workloads.TINY_FP32
+    T, steps = cfg["prefill_tokens"], cfg["decode_steps"]
+    max_seq = T + steps + 4
+    inp = workloads.make_block_inputs(cfg["dims"], cfg["batch"], T + steps, dtype=torch.float32,
+                                      max_seq=max_seq, random_gains=random_gains)
+    y_gpu, kc, vc, _, _ = _prefill_then_decode(inp, T, steps, max_seq)
+    y_ref, kref, vref = _oracle_prefill(inp, T + steps, max_seq)
+    got = workloads.to_numpy64(y_gpu)
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, y_ref) <= F32_TOL
+    n = T + steps
+    assert rel_err(workloads.to_numpy64(kc[:, :, :n]), kref[:, :, :n]) <= F32_TOL
+    assert rel_err(workloads.to_numpy64(vc[:, :, :n]), vref[:, :, :n]) <= F32_TOL
+
+
+def test_tiny_fp32_decode_bit_identical_to_prefill():
+    cfg = workloads.TINY_FP32
+    T, steps = cfg["prefill_tokens"], cfg["decode_steps"]
+    max_seq = 32
+    inp = workloads.make_block_inputs(cfg["dims"], 1, T + steps, dtype=torch.float32, max_seq=max_seq)
+    y_mix, kc_mix, vc_mix, blk, ddb = _prefill_then_decode(inp, T, steps, max_seq)
+    dev = torch.device("cuda:0")
+    kc = inp.k_cache.to(dev)
+    vc = inp.v_cache.to(dev)
+    y_full = run_prefill(blk, ddb, inp.x.to(dev), kc, vc)
+    torch.cuda.synchronize()
+    assert torch.equal(y_full, y_mix)
+    n = T + steps
+    assert torch.equal(kc[:, :, :n], kc_mix[:, :, :n]) and torch.equal(vc[:, :, :n], vc_mix[:, :, :n])
+
+
+@pytest.mark.parametrize("B,T,steps", [(2, 300, 3), (1, 129, 2), (3, 17, 2)])
+def test_bf16_mid_block_parity(B, T, steps):
+    """bf16, 128-wide heads, d=2048 (2 K-segments) and d_ff=4096 (4 K-segments):
+    token-tiled prefill (ragged token tiles) and weight-streaming decode."""
+    max_seq = T + steps + 5
+    inp = workloads.make_block_inputs(MID, B, T + steps, max_seq=max_seq, random_gains=True)
+    y_gpu, kc, vc, _, _ = _prefill_then_decode(inp, T, steps, max_seq)
+    tr = {}
+    _oracle_prefill(inp, T + steps, max_seq, trace=tr)
+    n = T + steps
+    check_bf16_output(workloads.to_numpy64(y_gpu), tr["y_exact"], what="y")
+    check_bf16_output(workloads.to_numpy64(kc[:, :, :n]), tr["k_exact"], what="k cache")
+    check_bf16_output(workloads.to_numpy64(vc[:, :, :n]), tr["v_exact"], what="v cache")
+    # rows past the last written position are untouched (still the NaN poison)
+    assert torch.isnan(kc[:, :, n:]).all() and torch.isnan(vc[:, :, n:]).all()
+
+
+@pytest.mark.parametrize("B,T,steps", [(2, 300, 3), (1, 64, 2)])
+def test_bf16_decode_bit_identical_to_prefill(B, T, steps):
+    """Decode rows (weight-streaming projections, split-KV attention) equal the
+    prefill rows (token-tiled projections, in-CTA attention fold) bit for bit."""
+    max_seq = T + steps + 5
+    inp = workloads.make_block_inputs(MID, B, T + steps, max_seq=max_seq)
+    y_mix, kc_mix, vc_mix, blk, ddb = _prefill_then_decode(inp, T, steps, max_seq)
+    dev = torch.device("cuda:0")
+    kc = inp.k_cache.to(dev)
+    vc = inp.v_cache.to(dev)
+    y_full = run_prefill(blk, ddb, inp.x.to(dev), kc, vc)
+    torch.cuda.synchronize()
+    n = T + steps
+    assert torch.equal(kc[:, :, :n], kc_mix[:, :, :n]) and torch.equal(vc[:, :, :n], vc_mix[:, :, :n])
+    assert torch.equal(y_full, y_mix)
+
+
+def test_bf16_zero_branches_return_input():
+    """Wo = 0 and W_down = 0: y = x exactly (both residual adds of zero)."""
+    inp = workloads.make_block_inputs(MID, 2, 40, max_seq=48)
+    inp.weights["wo"].zero_()
+    inp.weights["w_down"].zero_()
+    y, _, _, _, _ = _prefill_then_decode(inp, 38, 2, 48)
+    assert torch.equal(y.cpu(), inp.x)
+
+
+def test_decode_devpos_matches_decode_and_graph_replay():
+    import dense_decoder_block_gb300 as ddb
+    T = 70
+    max_seq = 80
+    inp = workloads.make_block_inputs(MID, 2, T + 3, max_seq=max_seq)
+    y_ref, kc_ref, vc_ref, blk, _ = _prefill_then_decode(inp, T, 3, max_seq)
+    dev = torch.device("cuda:0")
+    kc = inp.k_cache.to(dev)
+    vc = inp.v_cache.to(dev)
+    x = inp.x.to(dev)
+    run_prefill(blk, ddb, x[:, :T].contiguous(), kc, vc)
+    kv = ddb.KVCache(kc, vc)
+    pos = torch.tensor([T], dtype=torch.int32, device=dev)
+    xin = torch.empty(2, 1, MID.d_model, dtype=torch.bfloat16, device=dev)
+    yout = torch.empty_like(xin)
+    ws = blk.workspace(2, 1)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        xin.copy_(x[:, T:T + 1])
+        blk.decode_devpos(xin, kv, pos, yout, ws, stream)   # warm-up outside capture
+        with torch.cuda.graph(graph, stream=stream):
+            blk.decode_devpos(xin, kv, pos, yout, ws, stream)
+    torch.cuda.current_stream().wait_stream(stream)
+    outs = []
+    for s in range(3):
+        xin.copy_(x[:, T + s:T + s + 1])
+        pos.fill_(T + s)
+        graph.replay()
+        outs.append(yout.clone())
+    torch.cuda.synchronize()
+    assert blk.poll_error() == 0
+    assert torch.equal(torch.cat(outs, dim=1), y_ref[:, T:T + 3])
+    n = T + 3
+    assert torch.equal(kc[:, :, :n], kc_ref[:, :, :n])
+
+
+def test_error_paths():
+    import dense_decoder_block_gb300 as ddb
+    inp = workloads.make_block_inputs(MID, 1, 4, max_seq=8)
+    blk, _ = gpu_block(inp, 8)
+    dev = torch.device("cuda:0")
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    kv = ddb.KVCache(kc, vc)
+    x = inp.x[:, :1].to(dev)
+    y = torch.empty_like(x)
+    ws = blk.workspace(1, 1)
+    with pytest.raises(ddb.LlamaError) as e:
+        blk.decode(x, kv, 8, y, ws)
+    assert e.value.code == ddb.LLAMA_ERR_POS_RANGE
+    with pytest.raises(ddb.LlamaError) as e:
+        blk.decode(x, kv, 0, y, ws[:16])
+    assert e.value.code == ddb.LLAMA_ERR_WORKSPACE
+    # device-side position check: out of range -> error word, nothing written
+    pos = torch.tensor([9], dtype=torch.int32, device=dev)
+    before = kc.clone()
+    blk.decode_devpos(x, kv, pos, y, ws)
+    assert blk.poll_error() == ddb.LLAMA_ERR_POS_RANGE
+    assert blk.poll_error() == 0
+    assert torch.equal(before.isnan(), kc.isnan()) and torch.equal(before.nan_to_num(), kc.nan_to_num())
+    # bad dims
+    bad = ddb.llama_block_dims(2048, 16, 5, 128, 4096, 8, 1e-5, 5e5, ddb.LLAMA_BF16)
+    with pytest.raises(ddb.LlamaError) as e:
+        ddb.llama_block_create(bad, blk.c_w)
+    assert e.value.code == ddb.LLAMA_ERR_UNSUPPORTED_DIMS
+
+
+def test_rmsnorm_step_matches_oracle():
+    import dense_decoder_block_gb300 as ddb
+    from oracle.bf16 import round_bf16
+    gen = torch.Generator().manual_seed(5)
+    x = (torch.randn(37, 4096, generator=gen) * 3).to(torch.bfloat16)
+    g = (torch.rand(4096, generator=gen) + 0.5).to(torch.bfloat16)
+    dev = torch.device("cuda:0")
+    y = torch.empty_like(x, device=dev)
+    ddb.llama_rmsnorm(x.to(dev), g.to(dev), y, 37, 4096, 1e-5)
+    torch.cuda.synchronize()
+    ref = ob.rmsnorm(x.double().numpy(), g.double().numpy(), 1e-5, round_bf16)
+    got = y.double().cpu().numpy()
+    # fp32 reduction vs fp64: at most one bf16 ulp apart, almost always equal
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30)
+    assert np.mean(got == ref) > 0.99

@@ -12,12 +12,14 @@ Shapes follow the pages:
   * 70B block: d=8192, 64 query / 8 KV heads, head_dim 128, d_ff 28672
     ("Llama 3.1 70B", Grouped-Query Attention and SwiGLU MLP boxes).
 
-Draw recipe (one torch CPU generator per workload, seed 0): the activations x
-first, then the seven projection matrices in ABI order (wq, wk, wv, wo,
-w_gate, w_up, w_down), then the KV cache rows that precede the first decode
-position.  Every draw is fp32 N(0, std) from ``torch.randn``; bf16 workloads
-round it to bf16 (round-to-nearest-even) and both the GPU path and the oracle
-consume those rounded values.  RMSNorm gains are ones (the page's init) unless
+Draw recipe (torch CPU generators): the seven projection matrices in ABI
+order (wq, wk, wv, wo, w_gate, w_up, w_down) from a generator seeded with
+``seed`` (0 by default), the activations x from ``seed + 1``, then the K and
+V cache rows that precede the first decode position from ``seed + 2``.  The
+weights therefore do not depend on the batch size.  Every draw is fp32
+N(0, std) from ``torch.randn``; bf16 workloads round it to bf16
+(round-to-nearest-even) and both the GPU path and the oracle consume those
+rounded values.  RMSNorm gains are ones (the page's init) unless
 ``random_gains`` is set, in which case they are U(0.5, 1.5) drawn after the
 matrices.
 """
@@ -84,20 +86,13 @@ class BlockInputs:
     start_pos: int
 
 
-def make_block_inputs(dims: BlockDims, batch: int, tokens: int, *, dtype=torch.bfloat16,
-                      weight_std: float = 0.02, cache_len: int = 0, max_seq: Optional[int] = None,
-                      seed: int = 0, random_gains: bool = False, poison_tail: bool = True,
-                      device: str = "cpu") -> BlockInputs:
-    """Draw one workload.
-
-    ``tokens`` rows of x per sequence; ``cache_len`` rows 0..cache_len-1 of the
-    K and V caches are N(0,1) (taken as already-rotated keys); the rows from
-    cache_len + tokens up to max_seq are NaN when ``poison_tail`` so that any
-    read past the attended range shows up as a non-finite output.
-    """
+def make_weights(dims: BlockDims, *, dtype=torch.bfloat16, weight_std: float = 0.02, seed: int = 0,
+                 random_gains: bool = False):
+    """The seven projection matrices (ABI order, fp32 N(0, weight_std) rounded to
+    ``dtype``) and the two RMSNorm gains (ones, or U(0.5, 1.5) drawn after the
+    matrices when ``random_gains``).  Generator seeded with ``seed``."""
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
-    x = _randn(gen, (batch, tokens, dims.d_model), 1.0, dtype)
     weights = {}
     for name in WEIGHT_NAMES:
         weights[name] = _randn(gen, dims.weight_shapes()[name], weight_std, dtype)
@@ -105,22 +100,52 @@ def make_block_inputs(dims: BlockDims, batch: int, tokens: int, *, dtype=torch.b
         gains = {n: (torch.rand(dims.d_model, generator=gen) + 0.5).to(dtype) for n in GAIN_NAMES}
     else:
         gains = {n: torch.ones(dims.d_model, dtype=dtype) for n in GAIN_NAMES}
+    return weights, gains
+
+
+def make_x(batch: int, tokens: int, d_model: int, *, dtype=torch.bfloat16, seed: int = 1) -> torch.Tensor:
+    """Block input x [B, T, d], N(0, 1), generator seeded with ``seed``."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    return _randn(gen, (batch, tokens, d_model), 1.0, dtype)
+
+
+def make_cache(dims: BlockDims, batch: int, max_seq: int, cache_len: int, tokens: int, *, dtype=torch.bfloat16,
+               seed: int = 2, poison_tail: bool = True):
+    """K and V caches [B, Hkv, max_seq, dh]: rows 0..cache_len-1 N(0, 1) (K first,
+    then V, generator seeded with ``seed``; taken as already-rotated keys), rows
+    cache_len..cache_len+tokens-1 zero (the call writes them), the rest NaN when
+    ``poison_tail`` so that any read past the attended range shows."""
+    shape = (batch, dims.n_kv_heads, max_seq, dims.head_dim)
+    k_cache = torch.zeros(shape, dtype=dtype)
+    v_cache = torch.zeros(shape, dtype=dtype)
+    if cache_len > 0:
+        gen = torch.Generator(device="cpu")
+        gen.manual_seed(seed)
+        k_cache[:, :, :cache_len] = _randn(gen, (batch, dims.n_kv_heads, cache_len, dims.head_dim), 1.0, dtype)
+        v_cache[:, :, :cache_len] = _randn(gen, (batch, dims.n_kv_heads, cache_len, dims.head_dim), 1.0, dtype)
+    if poison_tail and cache_len + tokens < max_seq:
+        k_cache[:, :, cache_len + tokens:] = float("nan")
+        v_cache[:, :, cache_len + tokens:] = float("nan")
+    return k_cache, v_cache
+
+
+def make_block_inputs(dims: BlockDims, batch: int, tokens: int, *, dtype=torch.bfloat16,
+                      weight_std: float = 0.02, cache_len: int = 0, max_seq: Optional[int] = None,
+                      seed: int = 0, random_gains: bool = False, poison_tail: bool = True,
+                      device: str = "cpu", weights=None) -> BlockInputs:
+    """One workload: weights (seed), x (seed + 1), cache (seed + 2).  ``tokens``
+    rows of x per sequence start at position ``cache_len``.  Pass ``weights`` =
+    (weights, gains) to reuse already drawn matrices."""
+    if weights is None:
+        weights = make_weights(dims, dtype=dtype, weight_std=weight_std, seed=seed, random_gains=random_gains)
+    w, gains = weights
+    x = make_x(batch, tokens, dims.d_model, dtype=dtype, seed=seed + 1)
     if max_seq is None:
         max_seq = cache_len + tokens
-    k_cache = v_cache = None
-    if max_seq > 0:
-        shape = (batch, dims.n_kv_heads, max_seq, dims.head_dim)
-        k_cache = torch.zeros(shape, dtype=dtype)
-        v_cache = torch.zeros(shape, dtype=dtype)
-        if cache_len > 0:
-            kc = _randn(gen, (batch, dims.n_kv_heads, cache_len, dims.head_dim), 1.0, dtype)
-            vc = _randn(gen, (batch, dims.n_kv_heads, cache_len, dims.head_dim), 1.0, dtype)
-            k_cache[:, :, :cache_len] = kc
-            v_cache[:, :, :cache_len] = vc
-        if poison_tail and cache_len + tokens < max_seq:
-            k_cache[:, :, cache_len + tokens:] = float("nan")
-            v_cache[:, :, cache_len + tokens:] = float("nan")
-    inp = BlockInputs(dims, dtype, x, weights, gains, k_cache, v_cache, cache_len)
+    k_cache, v_cache = make_cache(dims, batch, max_seq, cache_len, tokens, dtype=dtype, seed=seed + 2,
+                                  poison_tail=poison_tail)
+    inp = BlockInputs(dims, dtype, x, w, gains, k_cache, v_cache, cache_len)
     if device != "cpu":
         inp = to_device(inp, device)
     return inp
