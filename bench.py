@@ -178,8 +178,29 @@ def run_ours(args, rank, world, device):
     ws = blk.workspace(B, 1)
     stream = torch.cuda.current_stream(device)
 
-    def step():
+    pos_dev = torch.tensor([POS], dtype=torch.int32, device=device)
+
+    def eager_step():
         blk.decode(x, kv, POS, y, ws)
+
+    # One decode step captured once as a CUDA graph (position read on the device),
+    # replayed per step: no host work between the block's kernels.
+    for _ in range(args.warmup):
+        eager_step()
+    torch.cuda.synchronize(device)
+    assert blk.poll_error() == 0
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        blk.decode_devpos(x, kv, pos_dev, y, ws, cap)
+        with torch.cuda.graph(graph, stream=cap):
+            blk.decode_devpos(x, kv, pos_dev, y, ws, cap)
+    stream.wait_stream(cap)
+    torch.cuda.synchronize(device)
+
+    def step():
+        graph.replay()
 
     for _ in range(args.warmup):
         step()
@@ -221,7 +242,7 @@ def run_ours(args, rank, world, device):
     value = tokens / (ms / 1e3)
 
     # --- per-stage durations (second pass, events between the block's kernels)
-    stage_ms = stage_profile(blk, x, kv, y, ws, stream, args.steps)
+    stage_ms = stage_profile(blk, x, kv, y, ws, pos_dev, device, args.steps)
 
     # --- end to end through the public API with host buffers
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -232,6 +253,7 @@ def run_ours(args, rank, world, device):
         step()
         yh.copy_(y, non_blocking=True)
     barrier()
+    # (the graph replays llama_block_decode_devpos on x / y, the C-ABI call)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -288,6 +310,7 @@ def run_ours(args, rank, world, device):
         "e2e": {"value": round(e2e_value, 1), "unit": "tok/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": y.numel() * y.element_size()},
         "gpu_launches": args.steps * blk_launches_per_decode(),
+        "launch": "one CUDA graph per step (llama_block_decode_devpos captured once)",
     }
     if args.extra and rank == 0:
         out["extra"] = extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind)
@@ -302,21 +325,35 @@ def blk_launches_per_decode():
 STAGES = ("rmsnorm_1", "qkv", "attention", "o_proj", "rmsnorm_2", "gate_up", "down")
 
 
-def stage_profile(blk, x, kv, y, ws, stream, steps):
-    """Average device time of each stage of the decode step, from CUDA events the
-    library records between its kernels on the launching stream."""
+def stage_profile(blk, x, kv, y, ws, pos_dev, device, steps):
+    """Average device time of each stage of the decode step.  The library records
+    CUDA events between its kernels on the launching stream; the step (with those
+    event records) is captured as a graph and replayed, so the stages run back to
+    back as in the timed region."""
     import dense_decoder_block_gb300 as ddb
     n = len(STAGES) + 1
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    cap = torch.cuda.Stream(device)
+    for ev in evs:           # torch creates the CUDA event on first record
+        ev.record(cap)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    ddb.llama_block_set_stage_events(blk.h, evs)
+    try:
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                blk.decode_devpos(x, kv, pos_dev, y, ws, cap)
+    finally:
+        ddb.llama_block_set_stage_events(blk.h, None)
     sums = [0.0] * len(STAGES)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(steps)]
-    for s in range(steps):
-        ddb.llama_block_set_stage_events(blk.h, evs[s])
-        blk.decode(x, kv, POS, y, ws)
-    ddb.llama_block_set_stage_events(blk.h, None)
-    torch.cuda.synchronize()
-    for s in range(steps):
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(device)
+    for _ in range(steps):
+        g.replay()
+        torch.cuda.synchronize(device)
         for i in range(len(STAGES)):
-            sums[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+            sums[i] += evs[i].elapsed_time(evs[i + 1])
     return {name: sums[i] / steps for i, name in enumerate(STAGES)}
 
 
@@ -398,17 +435,18 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def cpu_baseline_line(dims, seqs=2, reps=3):
+def cpu_baseline_line(dims, seqs=4, min_seconds=10.0, max_reps=400):
     w32 = oracle_weights32(dims)
     oracle_decode_sample(dims, w32, 1)   # warm caches / BLAS threads
-    tot_s, tot_tok = 0.0, 0
-    for _ in range(reps):
+    tot_s, tot_tok, reps = 0.0, 0, 0
+    while reps < max_reps and (reps == 0 or tot_s < min_seconds):
         s, t = oracle_decode_sample(dims, w32, seqs)
         tot_s += s
         tot_tok += t
+        reps += 1
     return {"value": round(tot_tok / tot_s, 3), "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{reps} x {seqs} sequences of the batch-32 decode step (fp32 NumPy oracle, "
-                      f"bf16 rounding emulated), {tot_s:.1f} s total"}
+            "sample": f"{reps} x {seqs} sequences of the batch-32 decode step at pos 1000 (fp32 NumPy oracle, "
+                      f"bf16 rounding emulated), {tot_s:.1f} s of CPU time"}
 
 
 def run_reference(args):

@@ -177,8 +177,13 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         if (e != cudaSuccess) return cuda_fail(b, e, where); \
     } while (0)
     int stage = 0;
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if (b->timing) cudaStreamIsCapturing(s, &capturing);
     auto mark = [&]() {
-        if (b->timing && stage <= LLAMA_BLOCK_STAGES) cudaEventRecord(b->stage_events[stage], s);
+        // inside stream capture an external record becomes a timing event node of the graph
+        if (b->timing && stage <= LLAMA_BLOCK_STAGES)
+            cudaEventRecordWithFlags(b->stage_events[stage], s,
+                                     capturing == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0);
         ++stage;
     };
 

@@ -28,6 +28,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRowsMax = 64;    // query rows per prefill CTA (n_rep * tokens)
 constexpr unsigned kFull = 0xffffffffu;
 
+__device__ __forceinline__ void ptx_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void ptx_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ void from_f(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
@@ -164,6 +167,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_prefill(const AttnK a) {
     T* Vs = Ks + kAttnChunk * TL::LD;
     float* qs = reinterpret_cast<float*>(Vs + kAttnChunk * TL::LD);
 
+    if (threadIdx.x == 0) ptx_launch_dependents();
+    ptx_wait();
     const int g = blockIdx.y, b = blockIdx.z;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int t0 = blockIdx.x * a.tq;
@@ -236,6 +241,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
     T* Vs = Ks + kAttnChunk * TL::LD;
     float* qs = reinterpret_cast<float*>(Vs + kAttnChunk * TL::LD);
 
+    if (threadIdx.x == 0) ptx_launch_dependents();
+    ptx_wait();
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int pos = base_position(a);
@@ -272,6 +279,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
 template <typename T, int DH>
 __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     constexpr int DPL = DH / 32;
+    if (threadIdx.x == 0) ptx_launch_dependents();
+    ptx_wait();
     const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int g = h / n_rep, r = h % n_rep;
@@ -332,8 +341,7 @@ cudaError_t prefill_impl(const AttnArgs& a, cudaStream_t s) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (r != cudaSuccess) return r;
     dim3 grid((a.tokens + k.tq - 1) / k.tq, a.n_kv_heads, a.batch);
-    kern<<<grid, kThreads, sm, s>>>(k);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kThreads), sm, s, k);
 }
 
 template <typename T, int DH>
@@ -345,11 +353,9 @@ cudaError_t decode_impl(const AttnArgs& a, cudaStream_t s) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (r != cudaSuccess) return r;
     dim3 grid(a.n_chunks, a.n_kv_heads, a.batch);
-    kern<<<grid, kThreads, sm, s>>>(k);
-    r = cudaGetLastError();
+    r = launch_pdl(kern, grid, dim3(kThreads), sm, s, k);
     if (r != cudaSuccess) return r;
-    k_attn_decode_combine<T, DH><<<dim3(a.n_heads, a.batch), 32, 0, s>>>(k);
-    return cudaGetLastError();
+    return launch_pdl(k_attn_decode_combine<T, DH>, dim3(a.n_heads, a.batch), dim3(32), 0, s, k);
 }
 
 }  // namespace

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "../../include/llama_block.h"
 
 namespace llama {
@@ -43,5 +45,24 @@ __device__ __forceinline__ float rope_rotate_elem(float self, float other, float
 
 // SiLU(z) = z / (1 + e^-z)
 __device__ __forceinline__ float silu_f(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, expf(-z))); }
+
+// Launch with programmatic stream serialization: the kernel may begin while the
+// previous kernel on the stream drains; every kernel of the block calls
+// griddepcontrol.wait before it reads anything an earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 }  // namespace llama

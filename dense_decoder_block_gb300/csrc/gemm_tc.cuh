@@ -169,6 +169,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else if (tile >= a.q_tiles) { mapA = &mA1; arow = (tile - a.q_tiles) * kTileF; }
     }
 
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
+
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -176,21 +178,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (DUAL) ptx::prefetch_tmap(&mA1);
             ptx::prefetch_tmap(&mB);
             const uint64_t pol_w = ptx::policy_evict_first();
-            int stage = 0;
-            uint32_t phase = 0;
+            // k-blocks this CTA walks, segment after segment (only the last segment may be short)
+            const int kb_first = seg_begin * a.seg_kb;
+            const int n_iter = min(seg_end * a.seg_kb, total_kb) - kb_first;
+            auto load_a = [&](int st, int kb) {
+                uint8_t* dst = smem + st * C::STAGE_BYTES;
+                ptx::tma_load_2d_hint(dst, mapA, &full[st], kb * kBlockK, arow, pol_w);
+                if (DUAL) ptx::tma_load_2d_hint(dst + kABytes, &mA1, &full[st], kb * kBlockK, arow, pol_w);
+            };
+            auto load_b = [&](int st, int kb) {
+                ptx::tma_load_2d(smem + st * C::STAGE_BYTES + NACC * kABytes, &mB, &full[st], kb * kBlockK, n0);
+            };
+            // The weights do not depend on the previous kernel: stream the first stages
+            // of them before waiting for it, then fetch the activations.
+            const int n_pre = min(C::STAGES, n_iter);
+            for (int it = 0; it < n_pre; ++it) {
+                ptx::mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
+                load_a(it, kb_first + it);
+            }
+            ptx::griddep_wait();
+            for (int it = 0; it < n_pre; ++it) load_b(it, kb_first + it);
+            int stage = n_pre % C::STAGES;
+            uint32_t phase = (n_pre == C::STAGES) ? 1u : 0u;
             bool ok = true;
-            for (int seg = seg_begin; seg < seg_end && ok; ++seg) {
-                const int kb0 = seg * a.seg_kb;
-                const int kb1 = min(kb0 + a.seg_kb, total_kb);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1, err)) { ok = false; break; }
-                    uint8_t* st = smem + stage * C::STAGE_BYTES;
-                    ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    ptx::tma_load_2d_hint(st, mapA, &full[stage], kb * kBlockK, arow, pol_w);
-                    if (DUAL) ptx::tma_load_2d_hint(st + kABytes, &mA1, &full[stage], kb * kBlockK, arow, pol_w);
-                    ptx::tma_load_2d(st + NACC * kABytes, &mB, &full[stage], kb * kBlockK, n0);
-                    if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
-                }
+            for (int it = n_pre; it < n_iter; ++it) {
+                if (!ptx::mbar_wait(&empty[stage], phase ^ 1, err)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                load_a(stage, kb_first + it);
+                load_b(stage, kb_first + it);
+                if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
             }
             if (!ok) {
                 // drain: wait (bounded) for loads this thread issued that nobody consumed
@@ -232,6 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- epilogue (8 warps)
+        ptx::griddep_wait();   // residuals, partials and tickets come from earlier kernels
         const int ew = warp - 2;
         const int quarter = warp & 3;
         const int half = ew >> 2;

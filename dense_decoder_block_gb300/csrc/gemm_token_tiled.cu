@@ -17,8 +17,7 @@ static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUten
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
     dim3 grid(p.F / kTileF, (p.M + BN - 1) / BN);
-    kern<<<grid, kGemmThreads, C::SMEM_BYTES, s>>>(a0, a1, a2, mb, ka);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kGemmThreads), C::SMEM_BYTES, s, a0, a1, a2, mb, ka);
 }
 
 cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,

@@ -17,8 +17,7 @@ static cudaError_t run_ws(const GemmProblem& p, const GemmKArgs& ka, const CUten
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
     dim3 grid(p.F / kTileF, ka.n_segs);
-    kern<<<grid, kGemmThreads, C::SMEM_BYTES, s>>>(a0, a1, a2, mb, ka);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kGemmThreads), C::SMEM_BYTES, s, a0, a1, a2, mb, ka);
 }
 
 template <int BN>

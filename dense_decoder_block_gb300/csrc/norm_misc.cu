@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ 
                                                           int n_zero) {
     __shared__ float red[kNormThreads / 32];
     __shared__ float s_scale;
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (blockIdx.x == 0 && zero)
         for (int i = tid; i < n_zero; i += kNormThreads) zero[i] = 0u;
@@ -165,12 +167,10 @@ cudaError_t launch_rmsnorm(const void* x, const void* g, void* y, int rows, int 
                            unsigned* zero_words, int n_zero, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     if (dtype == LLAMA_BF16)
-        k_rmsnorm<bf16><<<rows, kNormThreads, 0, s>>>((const bf16*)x, (const bf16*)g, (bf16*)y, d, eps, zero_words,
-                                                      n_zero);
-    else
-        k_rmsnorm<float><<<rows, kNormThreads, 0, s>>>((const float*)x, (const float*)g, (float*)y, d, eps,
-                                                       zero_words, n_zero);
-    return cudaGetLastError();
+        return launch_pdl(k_rmsnorm<bf16>, dim3(rows), dim3(kNormThreads), 0, s, (const bf16*)x, (const bf16*)g,
+                          (bf16*)y, d, eps, zero_words, n_zero);
+    return launch_pdl(k_rmsnorm<float>, dim3(rows), dim3(kNormThreads), 0, s, (const float*)x, (const float*)g,
+                      (float*)y, d, eps, zero_words, n_zero);
 }
 
 cudaError_t launch_linear_f32(const float* x, const float* w, const float* w2, const float* resid, float* y, int M,

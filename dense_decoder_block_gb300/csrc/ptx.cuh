@@ -28,6 +28,15 @@ __device__ __forceinline__ bool elect_one() {   // lane 0 of the warp
     return (threadIdx.x & 31) == 0;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Let the next kernel on the stream start its prologue (it still waits for this
+// grid's results with griddep_wait before touching them).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Block until every grid this one depends on has completed and its memory is visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
