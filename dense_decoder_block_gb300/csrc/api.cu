@@ -22,6 +22,9 @@ struct llama_block_s {
     std::string last_error;
     cudaEvent_t stage_events[LLAMA_BLOCK_STAGES + 1] = {};
     bool timing = false;
+    // K-segment length (64-element k-blocks) of each projection: QKV, O, gate/up, down.
+    // Fixed at create and shared by prefill and decode (it is part of the arithmetic).
+    int seg_kb[4] = {0, 0, 0, 0};
 };
 
 namespace {
@@ -70,6 +73,7 @@ GemmProblem problem_qkv(const llama_block_s* b, int M, const void* x) {
     p.a_maps[1] = &b->m_wk;
     p.a_maps[2] = &b->m_wv;
     p.n_maps = 3;
+    p.seg_kb = b->seg_kb[0];
     p.x = (const bf16*)x;
     return p;
 }
@@ -79,6 +83,7 @@ GemmProblem problem_o(const llama_block_s* b, int M, const void* x) {
     p.F = b->dims.d_model;
     p.K = b->dims.n_heads * b->dims.head_dim;
     p.a_maps[0] = &b->m_wo;
+    p.seg_kb = b->seg_kb[1];
     p.x = (const bf16*)x;
     return p;
 }
@@ -91,6 +96,7 @@ GemmProblem problem_gateup(const llama_block_s* b, int M, const void* x) {
     p.a_maps[1] = &b->m_wu;
     p.n_maps = 2;
     p.dual = true;
+    p.seg_kb = b->seg_kb[2];
     p.x = (const bf16*)x;
     return p;
 }
@@ -100,6 +106,7 @@ GemmProblem problem_down(const llama_block_s* b, int M, const void* x) {
     p.F = b->dims.d_model;
     p.K = b->dims.d_ff;
     p.a_maps[0] = &b->m_wd;
+    p.seg_kb = b->seg_kb[3];
     p.x = (const bf16*)x;
     return p;
 }
@@ -373,6 +380,12 @@ extern "C" int llama_block_create(const llama_block_dims* dims, const llama_bloc
             delete b;
             return LLAMA_ERR_CUDA;
         }
+        const int n_sm = device_sm_count();
+        const int qkv_tiles = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim / 128;
+        b->seg_kb[0] = choose_seg_kb(qkv_tiles, d.d_model / 64, n_sm);
+        b->seg_kb[1] = choose_seg_kb(d.d_model / 128, d.n_heads * d.head_dim / 64, n_sm);
+        b->seg_kb[2] = choose_seg_kb(d.d_ff / 128, d.d_model / 64, n_sm);
+        b->seg_kb[3] = choose_seg_kb(d.d_model / 128, d.d_ff / 64, n_sm);
     }
     // cos/sin of p * theta^(-2i/head_dim), computed in fp64, stored fp32, padded to 64 pairs
     const size_t n = (size_t)d.max_seq * kRopeMaxPairs;

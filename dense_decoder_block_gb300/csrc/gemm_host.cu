@@ -53,13 +53,42 @@ int pick_gemm_path(const GemmProblem& p, int path) {
     return path;
 }
 
-static int n_segments(const GemmProblem& p) { return (p.K + kSegK - 1) / kSegK; }
+static int seg_kb_of(const GemmProblem& p) { return p.seg_kb > 0 ? p.seg_kb : kSegK / kBlockK; }
+static int n_segments(const GemmProblem& p) {
+    const int kb = p.K / kBlockK, s = seg_kb_of(p);
+    return (kb + s - 1) / s;
+}
+
+int choose_seg_kb(int n_tiles, int total_kb, int n_sm) {
+    int best = total_kb;
+    long best_span = -1;
+    for (int s = 1; s <= total_kb; ++s) {
+        const int seg = (total_kb + s - 1) / s;
+        if (seg < 8 && s > 1) break;
+        const int segs = (total_kb + seg - 1) / seg;
+        const long units = (long)n_tiles * segs;
+        const long span = ((units + n_sm - 1) / n_sm) * seg;
+        if (best_span < 0 || span < best_span) {
+            best_span = span;
+            best = seg;
+        }
+    }
+    return best;
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
 
 size_t gemm_partial_bytes(const GemmProblem& p, int path) {
     if (pick_gemm_path(p, path) != PATH_WEIGHT_STREAM) return 0;
     const int segs = n_segments(p);
     if (segs <= 1) return 0;
-    return (size_t)segs * p.M * (p.dual ? 2 : 1) * p.F * sizeof(float);
+    const int bn = p.M <= 16 ? 16 : 32;   // the weight-streaming tile width for this M
+    return (size_t)segs * bn * (p.dual ? 2 : 1) * p.F * sizeof(float);
 }
 
 int gemm_counter_slots(const GemmProblem& p) { return p.F / kTileF; }
@@ -78,7 +107,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float*
     ka.M = p.M;
     ka.F = p.F;
     ka.K = p.K;
-    ka.seg_kb = kSegK / kBlockK;
+    ka.seg_kb = seg_kb_of(p);
     ka.n_segs = n_segments(p);
     ka.e = e;
     ka.partial = partial;

@@ -6,19 +6,18 @@
 // The accumulator tile is [128 features (TMEM lanes)] x [N tokens (columns)].
 //
 // Reduction schedule (the same in every mode, which is what makes decode
-// results bit-identical to prefill rows): K is cut into segments of kSegK
-// elements; each segment is one tcgen05.mma chain (64-element k-blocks, four
+// results bit-identical to prefill rows): K is cut into segments of seg_kb
+// 64-element k-blocks (fixed per projection when the handle is created); each segment is one tcgen05.mma chain (64-element k-blocks, four
 // K=16 instructions each, ascending) started from zero; the segment results
 // are added in fp32 in ascending segment order.
 //
 // Two schedules share that arithmetic:
-//   token-tiled  (prefill): grid = (feature tiles, token tiles); one CTA runs
-//                every segment of its tile into alternating TMEM buffers and the
-//                epilogue warps keep the running sum in registers.
-//   weight-stream (decode, M <= 32): grid = (feature tiles, segments); each CTA
-//                streams one 128 x kSegK weight slab, stores its fp32 segment
-//                result, and the last CTA of a feature tile (atomic ticket) adds
-//                the segments in order and runs the epilogue.
+//   token-tiled  (prefill, this file): grid = (feature tiles, token tiles); one
+//                CTA runs every segment of its tile into alternating TMEM buffers
+//                and the epilogue warps keep the running sum in registers.
+//   weight-stream (decode, M <= 32, gemm_ws.cuh): persistent CTAs stream
+//                (tile, segment) units, store fp32 segment results, and the last
+//                CTA of a feature tile (atomic ticket) adds them in order.
 //
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
 // issuer, warps 2..9 = epilogue.  Epilogue warp w reads TMEM lane quarter
@@ -120,7 +119,7 @@ __device__ __forceinline__ void epi_store(const GemmKArgs& a, int tile, int row,
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int BN, bool DUAL, bool WSTREAM, int EPI>
+template <int BN, bool DUAL, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
               const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mB,
@@ -141,9 +140,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x;
-    const int n0 = WSTREAM ? 0 : blockIdx.y * BN;
-    const int seg_begin = WSTREAM ? blockIdx.y : 0;
-    const int seg_end = WSTREAM ? blockIdx.y + 1 : a.n_segs;
+    const int n0 = blockIdx.y * BN;
+    const int seg_begin = 0;
+    const int seg_end = a.n_segs;
     const int total_kb = a.K / kBlockK;
     int* err = a.e.err;
 
@@ -280,55 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
         }
 
-        const int f = tile * kTileF + row;
         const int ncol0 = n0 + half * CPT;
-        if (WSTREAM && a.n_segs > 1) {
-            // store this segment, take a ticket; the last CTA of the tile adds the
-            // segments in ascending order.  Both named barriers are reached by all
-            // 256 epilogue threads whatever happened before (waits are bounded).
-            float* part = a.partial;
-            if (ok) {
-#pragma unroll
-                for (int ac = 0; ac < NACC; ++ac)
-#pragma unroll
-                    for (int j = 0; j < CPT; ++j) {
-                        const int n = ncol0 + j;
-                        if (n < a.M) part[(((size_t)seg_begin * a.M + n) * NACC + ac) * a.F + f] = acc[ac][j];
-                    }
-            } else {
-                *s_last = -1;
-            }
-            __threadfence();
-            named_bar_sync(1, 256);
-            if (ew == 0 && lane == 0) {
-                if (*s_last == -1) {
-                    *s_last = 0;   // this CTA failed: never complete the tile
-                } else {
-                    const unsigned prev = atomicAdd(&a.counters[tile], 1u);
-                    *s_last = (prev == (unsigned)(a.n_segs - 1)) ? 1 : 0;
-                }
-            }
-            named_bar_sync(1, 256);
-            if (*s_last == 1) {
-                __threadfence();
-#pragma unroll
-                for (int ac = 0; ac < NACC; ++ac)
-#pragma unroll
-                    for (int j = 0; j < CPT; ++j) {
-                        const int n = ncol0 + j;
-                        if (n < a.M) {
-                            float s = __ldcg(&part[(((size_t)0 * a.M + n) * NACC + ac) * a.F + f]);
-                            for (int sg = 1; sg < a.n_segs; ++sg)
-                                s = __fadd_rn(s, __ldcg(&part[(((size_t)sg * a.M + n) * NACC + ac) * a.F + f]));
-                            acc[ac][j] = s;
-                        }
-                    }
-                if (ew == 0 && lane == 0) a.counters[tile] = 0u;   // re-arm for the next call
-                ok = true;
-            } else {
-                ok = false;   // another CTA finishes this tile
-            }
-        }
         if (ok) {
 #pragma unroll
             for (int j = 0; j < CPT; ++j) {

@@ -7,7 +7,7 @@ template <int BN, bool DUAL, int EPI>
 static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0, const CUtensorMap& a1,
                           const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
     using C = GemmCfg<BN, DUAL>;
-    auto kern = k_gemm_tc<BN, DUAL, false, EPI>;
+    auto kern = k_gemm_tc<BN, DUAL, EPI>;
     static bool attr = false;
     if (!attr) {
         cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

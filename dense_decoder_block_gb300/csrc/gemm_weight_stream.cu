@@ -1,13 +1,13 @@
-// Weight-streaming (decode, M <= 32) instantiations of the tcgen05 projection kernel.
-#include "gemm_tc.cuh"
+// Weight-streaming (decode, M <= 32) instantiations of the persistent tcgen05 projection kernel.
+#include "gemm_ws.cuh"
 
 namespace llama {
 
 template <int BN, bool DUAL, int EPI>
 static cudaError_t run_ws(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0, const CUtensorMap& a1,
                           const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
-    using C = GemmCfg<BN, DUAL>;
-    auto kern = k_gemm_tc<BN, DUAL, true, EPI>;
+    using C = WsCfg<BN, DUAL>;
+    auto kern = k_gemm_ws<BN, DUAL, EPI>;
     static bool attr = false;
     if (!attr) {
         cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -16,7 +16,9 @@ static cudaError_t run_ws(const GemmProblem& p, const GemmKArgs& ka, const CUten
     }
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
-    dim3 grid(p.F / kTileF, ka.n_segs);
+    static const int n_sm = device_sm_count();
+    const int units = (p.F / kTileF) * ka.n_segs;
+    dim3 grid(units < n_sm ? units : n_sm);
     return launch_pdl(kern, grid, dim3(kGemmThreads), C::SMEM_BYTES, s, a0, a1, a2, mb, ka);
 }
 

@@ -37,6 +37,7 @@ struct GemmEpi {
 // blocks (wq / wk / wv) or as the gate/up pair (dual).
 struct GemmProblem {
     int M = 0, F = 0, K = 0;
+    int seg_kb = 0;              // k-blocks (64 elements) per K-segment; 0 = kSegK / 64
     const CUtensorMap* a_maps[3] = {nullptr, nullptr, nullptr};   // host copies, [rows, K] bf16
     int n_maps = 1;
     bool dual = false;           // a_maps[0] = gate, a_maps[1] = up, F = d_ff
@@ -49,6 +50,11 @@ enum GemmPath : int { PATH_AUTO = 0, PATH_TOKEN_TILED = 1, PATH_WEIGHT_STREAM = 
 size_t gemm_partial_bytes(const GemmProblem& p, int path);
 int gemm_counter_slots(const GemmProblem& p);
 int pick_gemm_path(const GemmProblem& p, int path);
+// K-segment length (in 64-element k-blocks) for a projection of n_tiles feature
+// tiles and total_kb k-blocks: the one that minimises the weight-streaming
+// makespan over n_sm SMs, at least 8 k-blocks per segment.
+int choose_seg_kb(int n_tiles, int total_kb, int n_sm);
+int device_sm_count();
 
 cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, unsigned* counters,
                         cudaStream_t s);
