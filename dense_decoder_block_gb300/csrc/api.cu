@@ -30,8 +30,6 @@ struct llama_block_s {
 namespace {
 
 constexpr size_t kAlign = 1024;
-constexpr int kCounterSlots = 256;   // per projection
-constexpr int kNumCounters = 4 * kCounterSlots;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
@@ -57,7 +55,6 @@ struct Ws {
     void* v_raw = nullptr;
     void* q_raw = nullptr;
     float* gemm_partial = nullptr;
-    unsigned* counters = nullptr;
     float* attn_partial = nullptr;
     size_t total = 0;
 };
@@ -139,7 +136,6 @@ Ws layout(const llama_block_s* b, int B, int T, uint8_t* base, bool decode) {
                                    problem_gateup(b, (int)M, nullptr), problem_down(b, (int)M, nullptr)};
         for (const auto& p : ps) part = std::max(part, gemm_partial_bytes(p, PATH_AUTO));
         w.gemm_partial = (float*)take(part);
-        w.counters = (unsigned*)take(kNumCounters * sizeof(unsigned));
     }
     if (decode) {
         const int n_rep = d.n_heads / d.n_kv_heads;
@@ -214,10 +210,21 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
     at.err = b->err_dev;
 
     if (d.dtype == LLAMA_BF16) {
-        // 1. RMSNorm_1 (also re-zeroes the projection tickets)
+        // Projections with a weight-streaming schedule leave fp32 segment results that a
+        // reduction kernel adds (ascending) before the same epilogue the token-tiled
+        // schedule fuses.
+        auto reduce = [&](const GemmProblem& p, const GemmEpi& ep, int kind) -> cudaError_t {
+            ReduceArgs r;
+            r.partial = w.gemm_partial;
+            r.n_segs = gemm_num_segments(p);
+            r.M = p.M;
+            r.F = p.F;
+            r.e = ep;
+            return launch_reduce(r, kind, s);
+        };
+        // 1. RMSNorm_1
         mark();
-        LLAMA_TRY(launch_rmsnorm(x, b->w.g_attn, w.xn, M, d.d_model, d.eps, d.dtype, w.counters, kNumCounters, s),
-                  "rmsnorm_1");
+        LLAMA_TRY(launch_rmsnorm(x, b->w.g_attn, w.xn, M, d.d_model, d.eps, d.dtype, s), "rmsnorm_1");
         // 2. QKV projection + RoPE + KV append
         mark();
         GemmEpi eq;
@@ -235,32 +242,46 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         eq.cos_tab = b->cos_tab;
         eq.sin_tab = b->sin_tab;
         eq.err = b->err_dev;
-        LLAMA_TRY(launch_gemm(problem_qkv(b, M, w.xn), eq, PATH_AUTO, w.gemm_partial, w.counters, s), "qkv");
+        const GemmProblem pq = problem_qkv(b, M, w.xn);
+        LLAMA_TRY(launch_gemm(pq, eq, PATH_AUTO, w.gemm_partial, s), "qkv");
+        if (gemm_needs_reduce(pq, PATH_AUTO)) LLAMA_TRY(reduce(pq, eq, EPI_QKV), "qkv_reduce");
         // 3. attention
         mark();
         if (decode) LLAMA_TRY(launch_attention_decode(at, s), "attention_decode");
         else LLAMA_TRY(launch_attention_prefill(at, s), "attention_prefill");
-        // 4. O projection + residual -> h
+        // 4. O projection + residual -> h, 5. RMSNorm_2 -> hn
         mark();
         GemmEpi eo;
         eo.kind = EPI_RESID;
         eo.out = (bf16*)w.h;
         eo.resid = (const bf16*)x;
         eo.err = b->err_dev;
-        LLAMA_TRY(launch_gemm(problem_o(b, M, w.o), eo, PATH_AUTO, w.gemm_partial, w.counters + kCounterSlots, s),
-                  "o_proj");
-        // 5. RMSNorm_2
-        mark();
-        LLAMA_TRY(launch_rmsnorm(w.h, b->w.g_ffn, w.hn, M, d.d_model, d.eps, d.dtype, nullptr, 0, s), "rmsnorm_2");
+        const GemmProblem po = problem_o(b, M, w.o);
+        LLAMA_TRY(launch_gemm(po, eo, PATH_AUTO, w.gemm_partial, s), "o_proj");
+        const bool o_red = gemm_needs_reduce(po, PATH_AUTO);
+        if (o_red && reduce_resid_norm_supported(d.d_model)) {
+            ReduceArgs r;
+            r.partial = w.gemm_partial;
+            r.n_segs = gemm_num_segments(po);
+            r.M = po.M;
+            r.F = po.F;
+            r.e = eo;
+            mark();
+            LLAMA_TRY(launch_reduce_resid_norm(r, b->w.g_ffn, w.hn, d.eps, s), "o_reduce_rmsnorm_2");
+        } else {
+            if (o_red) LLAMA_TRY(reduce(po, eo, EPI_RESID), "o_reduce");
+            mark();
+            LLAMA_TRY(launch_rmsnorm(w.h, b->w.g_ffn, w.hn, M, d.d_model, d.eps, d.dtype, s), "rmsnorm_2");
+        }
         // 6. gate/up + SwiGLU
         mark();
         GemmEpi eg;
         eg.kind = EPI_SWIGLU;
         eg.out = (bf16*)w.u;
         eg.err = b->err_dev;
-        LLAMA_TRY(launch_gemm(problem_gateup(b, M, w.hn), eg, PATH_AUTO, w.gemm_partial,
-                              w.counters + 2 * kCounterSlots, s),
-                  "gate_up");
+        const GemmProblem pg = problem_gateup(b, M, w.hn);
+        LLAMA_TRY(launch_gemm(pg, eg, PATH_AUTO, w.gemm_partial, s), "gate_up");
+        if (gemm_needs_reduce(pg, PATH_AUTO)) LLAMA_TRY(reduce(pg, eg, EPI_SWIGLU), "gate_up_reduce");
         // 7. down + residual -> y
         mark();
         GemmEpi ed;
@@ -268,14 +289,14 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         ed.out = (bf16*)y;
         ed.resid = (const bf16*)w.h;
         ed.err = b->err_dev;
-        LLAMA_TRY(launch_gemm(problem_down(b, M, w.u), ed, PATH_AUTO, w.gemm_partial,
-                              w.counters + 3 * kCounterSlots, s),
-                  "down");
+        const GemmProblem pd = problem_down(b, M, w.u);
+        LLAMA_TRY(launch_gemm(pd, ed, PATH_AUTO, w.gemm_partial, s), "down");
+        if (gemm_needs_reduce(pd, PATH_AUTO)) LLAMA_TRY(reduce(pd, ed, EPI_RESID), "down_reduce");
         mark();
     } else {
         const int qd = d.n_heads * d.head_dim, kvd = d.n_kv_heads * d.head_dim;
         const float* xf = (const float*)x;
-        LLAMA_TRY(launch_rmsnorm(x, b->w.g_attn, w.xn, M, d.d_model, d.eps, d.dtype, nullptr, 0, s), "rmsnorm_1");
+        LLAMA_TRY(launch_rmsnorm(x, b->w.g_attn, w.xn, M, d.d_model, d.eps, d.dtype, s), "rmsnorm_1");
         LLAMA_TRY(launch_linear_f32((const float*)w.xn, (const float*)b->w.wq, nullptr, nullptr, (float*)w.q_raw, M,
                                     qd, d.d_model, 0, s),
                   "q_proj");
@@ -295,7 +316,7 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         LLAMA_TRY(launch_linear_f32((const float*)w.o, (const float*)b->w.wo, nullptr, xf, (float*)w.h, M, d.d_model,
                                     qd, 1, s),
                   "o_proj");
-        LLAMA_TRY(launch_rmsnorm(w.h, b->w.g_ffn, w.hn, M, d.d_model, d.eps, d.dtype, nullptr, 0, s), "rmsnorm_2");
+        LLAMA_TRY(launch_rmsnorm(w.h, b->w.g_ffn, w.hn, M, d.d_model, d.eps, d.dtype, s), "rmsnorm_2");
         LLAMA_TRY(launch_linear_f32((const float*)w.hn, (const float*)b->w.w_gate, (const float*)b->w.w_up, nullptr,
                                     (float*)w.u, M, d.d_ff, d.d_model, 2, s),
                   "gate_up");
@@ -498,7 +519,7 @@ extern "C" int llama_rmsnorm(const void* x, const void* g, void* y, int rows, in
     if (rows == 0) return LLAMA_OK;
     if (!x || !g || !y) return LLAMA_ERR_INVALID_ARG;
     if (dtype != LLAMA_BF16 && dtype != LLAMA_F32) return LLAMA_ERR_INVALID_ARG;
-    return launch_rmsnorm(x, g, y, rows, d, eps, dtype, nullptr, 0, (cudaStream_t)stream) == cudaSuccess
+    return launch_rmsnorm(x, g, y, rows, d, eps, dtype, (cudaStream_t)stream) == cudaSuccess
                ? LLAMA_OK
                : LLAMA_ERR_CUDA;
 }
@@ -517,8 +538,6 @@ namespace {
 struct HeadWs {
     void* hn;
     float* logits;
-    float* partial;
-    unsigned* counters;
     size_t total;
 };
 HeadWs head_layout(int batch, int d_model, int vocab, uint8_t* base, bool own_logits) {
@@ -558,9 +577,9 @@ extern "C" int llama_lmhead_argmax(const void* h, int batch, int h_stride, const
     if (h_stride != d_model) {
         for (int r = 0; r < batch; ++r)
             if (launch_rmsnorm((const uint8_t*)h + (size_t)r * h_stride * 2, g_final, (uint8_t*)w.hn + (size_t)r * d_model * 2,
-                               1, d_model, eps, LLAMA_BF16, nullptr, 0, s) != cudaSuccess)
+                               1, d_model, eps, LLAMA_BF16, s) != cudaSuccess)
                 return LLAMA_ERR_CUDA;
-    } else if (launch_rmsnorm(h, g_final, w.hn, batch, d_model, eps, LLAMA_BF16, nullptr, 0, s) != cudaSuccess) {
+    } else if (launch_rmsnorm(h, g_final, w.hn, batch, d_model, eps, LLAMA_BF16, s) != cudaSuccess) {
         return LLAMA_ERR_CUDA;
     }
     CUtensorMap mw;

@@ -46,6 +46,33 @@ __device__ __forceinline__ float rope_rotate_elem(float self, float other, float
 // SiLU(z) = z / (1 + e^-z)
 __device__ __forceinline__ float silu_f(float z) { return __fdiv_rn(z, __fadd_rn(1.0f, expf(-z))); }
 
+// Epilogue arithmetic shared by every schedule (fused GEMM epilogues and the
+// decode segment reductions), so both produce the same bits.
+// Residual: bf16(x + bf16(branch)).
+__device__ __forceinline__ float epi_resid(float x, float acc) { return __fadd_rn(x, bf16_round(acc)); }
+// SwiGLU: bf16(silu(bf16(gate))) * bf16(up), to be rounded by the caller.
+__device__ __forceinline__ float epi_swiglu(float gate_acc, float up_acc) {
+    const float g = bf16_round(gate_acc);
+    const float u = bf16_round(up_acc);
+    return __fmul_rn(bf16_round(silu_f(g)), u);
+}
+
+// RMSNorm sum-of-squares tree for a 256-thread CTA: each thread's partial (its
+// elements tid, tid+256, ... in ascending order), a butterfly inside each warp
+// read at lane 0, then the 8 warps in ascending order.  `red` is 8 floats of
+// shared memory.  Returns the row total in every thread.
+__device__ __forceinline__ float rms_tree_256(float ss, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+    __syncthreads();   // red may still be read from a previous use
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float t = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) t = __fadd_rn(t, red[w]);
+    return t;
+}
+
 // Launch with programmatic stream serialization: the kernel may begin while the
 // previous kernel on the stream drains; every kernel of the block calls
 // griddepcontrol.wait before it reads anything an earlier kernel wrote.

@@ -91,7 +91,11 @@ size_t gemm_partial_bytes(const GemmProblem& p, int path) {
     return (size_t)segs * bn * (p.dual ? 2 : 1) * p.F * sizeof(float);
 }
 
-int gemm_counter_slots(const GemmProblem& p) { return p.F / kTileF; }
+int gemm_num_segments(const GemmProblem& p) { return n_segments(p); }
+
+bool gemm_needs_reduce(const GemmProblem& p, int path) {
+    return pick_gemm_path(p, path) == PATH_WEIGHT_STREAM && n_segments(p) > 1;
+}
 
 // Instantiated in gemm_token_tiled.cu / gemm_weight_stream.cu
 cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
@@ -99,8 +103,7 @@ cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const 
 cudaError_t launch_weight_stream(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
                                  const CUtensorMap& a1, const CUtensorMap& a2, const bf16* x, cudaStream_t s);
 
-cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, unsigned* counters,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, cudaStream_t s) {
     if (p.M <= 0) return cudaSuccess;
     if (p.F % kTileF != 0 || p.K % kBlockK != 0) return cudaErrorInvalidValue;
     GemmKArgs ka{};
@@ -111,7 +114,6 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float*
     ka.n_segs = n_segments(p);
     ka.e = e;
     ka.partial = partial;
-    ka.counters = counters;
     const CUtensorMap& a0 = *p.a_maps[0];
     const CUtensorMap& a1 = p.a_maps[1] ? *p.a_maps[1] : a0;
     const CUtensorMap& a2 = p.a_maps[2] ? *p.a_maps[2] : a0;
@@ -122,7 +124,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float*
     const int chosen = pick_gemm_path(p, path);
     if (chosen == PATH_WEIGHT_STREAM) {
         if (p.M > 32) return cudaErrorInvalidValue;
-        if (ka.n_segs > 1 && (!partial || !counters)) return cudaErrorInvalidValue;
+        if (ka.n_segs > 1 && !partial) return cudaErrorInvalidValue;
         return launch_weight_stream(p, ka, a0, a1, a2, p.x, s);
     }
     return launch_token_tiled(p, ka, a0, a1, a2, p.x, s);

@@ -56,8 +56,7 @@ struct GemmKArgs {
     int n_segs, seg_kb;
     int q_tiles, k_tiles;     // QKV: feature tiles per map (wq, wk); the rest are wv
     GemmEpi e;
-    float* partial;
-    unsigned* counters;
+    float* partial;   // weight-streaming: fp32 segment results [seg][acc][M][F]
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -103,13 +102,9 @@ __device__ __forceinline__ void epi_store(const GemmKArgs& a, int tile, int row,
         if (!valid) return;
         const size_t idx = (size_t)n * a.F + f;
         if constexpr (EPI == EPI_RESID) {
-            const float x = __bfloat162float(e.resid[idx]);
-            e.out[idx] = __float2bfloat16_rn(__fadd_rn(x, bf16_round(acc)));
+            e.out[idx] = __float2bfloat16_rn(epi_resid(__bfloat162float(e.resid[idx]), acc));
         } else if constexpr (EPI == EPI_SWIGLU) {
-            const float g = bf16_round(acc);
-            const float u = bf16_round(acc_up);
-            const float sg = bf16_round(silu_f(g));
-            e.out[idx] = __float2bfloat16_rn(__fmul_rn(sg, u));
+            e.out[idx] = __float2bfloat16_rn(epi_swiglu(acc, acc_up));
         } else if constexpr (EPI == EPI_PLAIN) {
             e.out[idx] = __float2bfloat16_rn(acc);
         } else {  // EPI_LOGITS
@@ -136,7 +131,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = empty + C::STAGES;
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = (uint32_t*)(tempty + 2);
-    volatile int* s_last = (volatile int*)(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x;

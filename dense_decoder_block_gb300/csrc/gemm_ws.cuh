@@ -7,9 +7,9 @@
 // blockIdx.x + gridDim.x, ... with a single TMA ring that never drains between
 // units.  The MMA warp accumulates each unit into one of two TMEM buffers; the
 // epilogue warps drain a buffer while the next unit streams, store the unit's
-// fp32 segment result to the workspace and take a ticket for its tile; the CTA
-// that takes the last ticket adds the tile's segments in order and runs the
-// fused epilogue.
+// fp32 segment result to the workspace; a small reduction kernel (reduce.cu),
+// launched right behind it, adds each output's segments in ascending order and
+// runs the fused epilogue.  With a single segment the epilogue runs here.
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -46,8 +46,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = empty + C::STAGES;
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = (uint32_t*)(tempty + 2);
-    volatile int* s_last = (volatile int*)(tmem_holder + 1);
-    volatile int* s_fail = s_last + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total_kb = a.K / kBlockK;
@@ -58,8 +56,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) { ptx::mbar_init(&full[i], 1); ptx::mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; ++i) { ptx::mbar_init(&tfull[i], 1); ptx::mbar_init(&tempty[i], 8); }
-        *s_last = 0;
-        *s_fail = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -187,60 +183,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
             if (a.n_segs > 1) {
-                // Segment results live per epilogue thread, contiguous (16-byte stores):
-                // part[((seg * n_tiles + tile) * 256 + thread) * NACC * CPT + ac * CPT + j]
-                constexpr int V = NACC * CPT;
-                const int ept = ew * 32 + lane;
-                const size_t tstride = (size_t)n_tiles * 256 * V;
-                float* mine = a.partial + ((size_t)tile * 256 + ept) * V;
+                // fp32 segment result, [seg][acc][token][feature]; the reduction kernel of
+                // this projection adds the segments in ascending order and runs the epilogue
                 if (ok) {
-                    float4* dst = reinterpret_cast<float4*>(mine + seg * tstride);
 #pragma unroll
-                    for (int q = 0; q < V / 4; ++q)
-                        dst[q] = make_float4(acc[(4 * q) / CPT][(4 * q) % CPT], acc[(4 * q + 1) / CPT][(4 * q + 1) % CPT],
-                                             acc[(4 * q + 2) / CPT][(4 * q + 2) % CPT],
-                                             acc[(4 * q + 3) / CPT][(4 * q + 3) % CPT]);
-                } else {
-                    *s_fail = 1;
-                }
-                // ticket: CTA barrier, then one release/acquire by one thread
-                named_bar_sync(1, 256);
-                if (ew == 0 && lane == 0) {
-                    if (*s_fail) {
-                        *s_last = 0;   // a failed CTA never completes a tile
-                    } else {
-                        __threadfence();
-                        const unsigned prev = atomicAdd(&a.counters[tile], 1u);
-                        __threadfence();
-                        *s_last = (prev == (unsigned)(a.n_segs - 1)) ? 1 : 0;
-                    }
-                }
-                named_bar_sync(1, 256);
-                ok = (*s_last == 1);
-                if (ok) {
-                    // ascending segment sum, the next segment's loads in flight while adding
-                    float sum[V], nxt[V];
-                    const float4* src = reinterpret_cast<const float4*>(mine);
+                    for (int ac = 0; ac < NACC; ++ac)
 #pragma unroll
-                    for (int q = 0; q < V / 4; ++q) {
-                        const float4 t = __ldcg(src + q);
-                        sum[4 * q] = t.x; sum[4 * q + 1] = t.y; sum[4 * q + 2] = t.z; sum[4 * q + 3] = t.w;
-                    }
-                    for (int sg = 1; sg < a.n_segs; ++sg) {
-                        const float4* sp = reinterpret_cast<const float4*>(mine + sg * tstride);
-#pragma unroll
-                        for (int q = 0; q < V / 4; ++q) {
-                            const float4 t = __ldcg(sp + q);
-                            nxt[4 * q] = t.x; nxt[4 * q + 1] = t.y; nxt[4 * q + 2] = t.z; nxt[4 * q + 3] = t.w;
+                        for (int j = 0; j < CPT; ++j) {
+                            const int n = ncol0 + j;
+                            if (n < a.M) a.partial[(((size_t)seg * NACC + ac) * a.M + n) * a.F + f] = acc[ac][j];
                         }
-#pragma unroll
-                        for (int v = 0; v < V; ++v) sum[v] = __fadd_rn(sum[v], nxt[v]);
-                    }
-#pragma unroll
-                    for (int v = 0; v < V; ++v) acc[v / CPT][v % CPT] = sum[v];
-                    if (ew == 0 && lane == 0) a.counters[tile] = 0u;   // re-arm for the next call
                 }
-                named_bar_sync(1, 256);   // every thread has read s_last before the next unit rewrites it
+                continue;
             }
             if (ok) {
 #pragma unroll

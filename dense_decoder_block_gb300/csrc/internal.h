@@ -46,18 +46,32 @@ struct GemmProblem {
 
 enum GemmPath : int { PATH_AUTO = 0, PATH_TOKEN_TILED = 1, PATH_WEIGHT_STREAM = 2 };
 
-// Scratch for the weight-streaming path: fp32 partials and per-tile counters.
+// Scratch for the weight-streaming path: fp32 segment results [seg][acc][M][F].
 size_t gemm_partial_bytes(const GemmProblem& p, int path);
-int gemm_counter_slots(const GemmProblem& p);
 int pick_gemm_path(const GemmProblem& p, int path);
+int gemm_num_segments(const GemmProblem& p);
+// True when the projection leaves segment results for a reduction kernel
+// (weight-streaming schedule with more than one K-segment).
+bool gemm_needs_reduce(const GemmProblem& p, int path);
 // K-segment length (in 64-element k-blocks) for a projection of n_tiles feature
 // tiles and total_kb k-blocks: the one that minimises the weight-streaming
 // makespan over n_sm SMs, at least 8 k-blocks per segment.
 int choose_seg_kb(int n_tiles, int total_kb, int n_sm);
 int device_sm_count();
 
-cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, unsigned* counters,
-                        cudaStream_t s);
+cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, cudaStream_t s);
+
+// Segment reductions (decode): add each output's segments in ascending order and
+// apply the projection's epilogue (kind = EPI_QKV, EPI_RESID or EPI_SWIGLU).
+struct ReduceArgs {
+    const float* partial = nullptr;
+    int n_segs = 0, M = 0, F = 0;
+    GemmEpi e;
+};
+cudaError_t launch_reduce(const ReduceArgs& r, int kind, cudaStream_t s);
+// Residual epilogue followed by RMSNorm of each row (d = F), writing h (e.out) and hn.
+bool reduce_resid_norm_supported(int d);
+cudaError_t launch_reduce_resid_norm(const ReduceArgs& r, const void* gain, void* hn, float eps, cudaStream_t s);
 
 // Whole-K dot products per CTA (no segment split), weight-streaming, M <= 32.
 // For outputs that have no token-tiled counterpart (the LM head logits).
@@ -69,7 +83,7 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 // ---------------------------------------------------------------- other kernels
 cudaError_t launch_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype,
-                           unsigned* zero_words, int n_zero, cudaStream_t s);
+                           cudaStream_t s);
 
 // Attention (SIMT).  q, o [M, Hq*dh]; caches [Bc, Hkv, kv_seq, dh].
 struct AttnArgs {

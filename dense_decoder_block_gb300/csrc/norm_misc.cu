@@ -14,47 +14,68 @@ __device__ __forceinline__ float to_f(float v) { return v; }
 
 // "Llama 3.1 70B", RMSNorm reference implementation: fp32 mean of squares,
 // eps inside the square root, the scaled row cast to the trunk dtype before the
-// gain multiplies it.  One CTA per row; the sum of squares uses one fixed tree
-// (thread-sequential, warp butterfly read at lane 0, warps in ascending order),
-// the same for every caller, so prefill and decode rows agree bit for bit.
-template <typename T>
+// gain multiplies it.  One 256-thread CTA per row; thread t owns elements
+// t, t+256, ... (kept in registers when d/256 is a small power of two); the sum
+// of squares uses rms_tree_256, the tree every RMSNorm of the library uses, so
+// prefill and decode rows agree bit for bit.
+template <typename T, int EPT>
 __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ x, const T* __restrict__ g,
-                                                          T* __restrict__ y, int d, float eps, unsigned* zero,
-                                                          int n_zero) {
+                                                          T* __restrict__ y, int d, float eps) {
     __shared__ float red[kNormThreads / 32];
-    __shared__ float s_scale;
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (blockIdx.x == 0 && zero)
-        for (int i = tid; i < n_zero; i += kNormThreads) zero[i] = 0u;
+    const int row = blockIdx.x, tid = threadIdx.x;
     const T* xr = x + (size_t)row * d;
-    float ss = 0.f;
-    for (int i = tid; i < d; i += kNormThreads) {
-        const float v = to_f(xr[i]);
-        ss = __fmaf_rn(v, v, ss);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (tid == 0) {
-        float t = red[0];
-        for (int w = 1; w < kNormThreads / 32; ++w) t = __fadd_rn(t, red[w]);
-        s_scale = rms_scale(t, d, eps);
-    }
-    __syncthreads();
-    const float r = s_scale;
     T* yr = y + (size_t)row * d;
-    for (int i = tid; i < d; i += kNormThreads) {
-        const float v = to_f(xr[i]);
-        if constexpr (sizeof(T) == 2) {
-            const float xs = bf16_round(__fmul_rn(v, r));
-            yr[i] = __float2bfloat16_rn(__fmul_rn(xs, to_f(g[i])));
-        } else {
-            yr[i] = __fmul_rn(__fmul_rn(v, r), to_f(g[i]));
+    if constexpr (EPT > 0) {
+        float v[EPT];
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+            v[e] = to_f(xr[tid + kNormThreads * e]);
+            ss = __fmaf_rn(v[e], v[e], ss);
+        }
+        const float r = rms_scale(rms_tree_256(ss, red), d, eps);
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+            const int i = tid + kNormThreads * e;
+            if constexpr (sizeof(T) == 2)
+                yr[i] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(v[e], r)), to_f(g[i])));
+            else
+                yr[i] = __fmul_rn(__fmul_rn(v[e], r), to_f(g[i]));
+        }
+    } else {
+        float ss = 0.f;
+        for (int i = tid; i < d; i += kNormThreads) {
+            const float v = to_f(xr[i]);
+            ss = __fmaf_rn(v, v, ss);
+        }
+        const float r = rms_scale(rms_tree_256(ss, red), d, eps);
+        for (int i = tid; i < d; i += kNormThreads) {
+            const float v = to_f(xr[i]);
+            if constexpr (sizeof(T) == 2)
+                yr[i] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(v, r)), to_f(g[i])));
+            else
+                yr[i] = __fmul_rn(__fmul_rn(v, r), to_f(g[i]));
         }
     }
+}
+
+template <typename T>
+cudaError_t rmsnorm_dispatch(const T* x, const T* g, T* y, int rows, int d, float eps, cudaStream_t s) {
+    const dim3 grid(rows), block(kNormThreads);
+    if (d % kNormThreads == 0) {
+        switch (d / kNormThreads) {
+            case 1: return launch_pdl(k_rmsnorm<T, 1>, grid, block, 0, s, x, g, y, d, eps);
+            case 2: return launch_pdl(k_rmsnorm<T, 2>, grid, block, 0, s, x, g, y, d, eps);
+            case 4: return launch_pdl(k_rmsnorm<T, 4>, grid, block, 0, s, x, g, y, d, eps);
+            case 8: return launch_pdl(k_rmsnorm<T, 8>, grid, block, 0, s, x, g, y, d, eps);
+            case 16: return launch_pdl(k_rmsnorm<T, 16>, grid, block, 0, s, x, g, y, d, eps);
+            case 32: return launch_pdl(k_rmsnorm<T, 32>, grid, block, 0, s, x, g, y, d, eps);
+            default: break;
+        }
+    }
+    return launch_pdl(k_rmsnorm<T, 0>, grid, block, 0, s, x, g, y, d, eps);
 }
 
 // fp32 projection: one thread per output, ascending K (the same order for any M).
@@ -164,13 +185,10 @@ __global__ void __launch_bounds__(1024) k_argmax_rows(const float* __restrict__ 
 }  // namespace
 
 cudaError_t launch_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype,
-                           unsigned* zero_words, int n_zero, cudaStream_t s) {
+                           cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    if (dtype == LLAMA_BF16)
-        return launch_pdl(k_rmsnorm<bf16>, dim3(rows), dim3(kNormThreads), 0, s, (const bf16*)x, (const bf16*)g,
-                          (bf16*)y, d, eps, zero_words, n_zero);
-    return launch_pdl(k_rmsnorm<float>, dim3(rows), dim3(kNormThreads), 0, s, (const float*)x, (const float*)g,
-                      (float*)y, d, eps, zero_words, n_zero);
+    if (dtype == LLAMA_BF16) return rmsnorm_dispatch((const bf16*)x, (const bf16*)g, (bf16*)y, rows, d, eps, s);
+    return rmsnorm_dispatch((const float*)x, (const float*)g, (float*)y, rows, d, eps, s);
 }
 
 cudaError_t launch_linear_f32(const float* x, const float* w, const float* w2, const float* resid, float* y, int M,
