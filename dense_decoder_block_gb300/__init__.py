@@ -26,7 +26,7 @@ __all__ = [
     "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_destroy",
     "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_decode", "llama_block_decode_devpos",
     "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_embed", "llama_lmhead_workspace_bytes",
-    "llama_lmhead_argmax", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
+    "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
 ]
 
 
@@ -145,6 +145,15 @@ def llama_lmhead_argmax(h, batch, h_stride, g_final, w_out, vocab, d_model, eps,
                                    C.c_float(eps), _ptr(ids), _ptr(logits), _ptr(ws), ws_bytes, _stream(stream))
     if rc != LLAMA_OK:
         raise LlamaError(rc, "llama_lmhead_argmax")
+
+
+def llama_lmhead_argmax_noalloc(h, batch, h_stride, g_final, w_out, vocab, d_model, eps, ids, logits,
+                                stream=None) -> None:
+    """The LM head + greedy choice without a workspace (library-owned scratch; see the header)."""
+    rc = lib().llama_lmhead_argmax_noalloc(_ptr(h), batch, h_stride, _ptr(g_final), _ptr(w_out), vocab, d_model,
+                                           C.c_float(eps), _ptr(ids), _ptr(logits), _stream(stream))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_lmhead_argmax_noalloc")
 
 
 # ----------------------------------------------------------------------------- convenience

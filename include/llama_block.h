@@ -170,6 +170,21 @@ int llama_lmhead_argmax(const void* h, int batch, int h_stride, const void* g_fi
                         int d_model, float eps, int32_t* ids, float* logits, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* Same result as llama_lmhead_argmax, for callers that cannot allocate device
+ * memory (no workspace to pass: code running where cudaMalloc is not allowed or
+ * must not happen on the hot path).  There is no counterpart on the pages; it is
+ * a deployment variant.  The normalised rows live in a library-owned device
+ * array of 32 x 8192 bf16 (512 KiB), held by every GPU that loads the library
+ * until the process exits; batch > 32 or d_model > 8192 returns
+ * LLAMA_ERR_WORKSPACE.  logits [batch, vocab] fp32 is required (it is an
+ * output).  Nothing is allocated.  The first call on a device looks up the
+ * array's device address (with that device current) and caches it: make that
+ * first call before any stream capture.  Every call shares the one array, which
+ * keeps the last call's rows; calls that overlap on the GPU (other streams,
+ * other threads) race on it. */
+int llama_lmhead_argmax_noalloc(const void* h, int batch, int h_stride, const void* g_final, const void* w_out,
+                                int vocab, int d_model, float eps, int32_t* ids, float* logits, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Step-level entry points (the block's individual steps, for unit tests and
  * for callers that compose their own schedule).  Same conventions as above.
