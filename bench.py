@@ -135,7 +135,7 @@ class ClockSampler:
 def kernel_source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_decoder_block_gb300", "csrc")
-    for f in ("gemm_tc.cuh", "gemm_weight_stream.cu", "ptx.cuh", "common.cuh"):
+    for f in ("gemm_tc.cuh", "gemm_ws.cuh", "gemm_weight_stream.cu", "ptx.cuh", "common.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
