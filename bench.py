@@ -317,6 +317,37 @@ def run_ours(args, rank, world, device):
     return out
 
 
+def run_prefill(args, rank, world, device):
+    """The 8B-shaped causal prefill block (batch 1, T = --tokens): TFLOP/s against the
+    measured bf16 peak.  One step = one prefill of the whole block."""
+    import dense_decoder_block_gb300 as ddb
+    ddb.lib()
+    dims = workloads.LLAMA3_8B
+    T = args.tokens
+    wts = workloads.make_weights(dims, weight_std=0.02)
+    inp = workloads.make_block_inputs(dims, 1, T, max_seq=T, weights=wts, poison_tail=False)
+    w = {k: v.to(device) for k, v in inp.weights.items()}
+    g = {k: v.to(device) for k, v in inp.gains.items()}
+    blk = ddb.LlamaBlock(dims, w, g, T)
+    kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+    x = inp.x.to(device)
+    y = torch.empty_like(x)
+    ws = blk.workspace(1, T)
+    stream = torch.cuda.current_stream(device)
+    ms = time_region(lambda: blk.prefill(x, kv, y, ws), args.steps, args.warmup, stream)
+    assert blk.poll_error() == 0
+    _, bf16_peak, _, peak_kind = peaks()
+    fl = prefill_flops(dims, 1, T)
+    tf = fl / (ms / 1e3) / 1e12
+    return {"metric": METRIC, "value": round(T * world / (ms / 1e3), 1), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) x)",
+            "config": {"workload": f"Llama-3 8B-shaped causal prefill block, batch 1, T={T}", "tokens": T},
+            "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind,
+            "gpu_launches": args.steps * 7}
+
+
 def blk_launches_per_decode():
     # rmsnorm, qkv, attention chunks, attention combine, o, rmsnorm, gate/up, down
     return 8
@@ -483,6 +514,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("decode", "prefill"), default="decode",
+                    help="decode: the 8B decode block (default); prefill: the 8B causal prefill block at --tokens")
+    ap.add_argument("--tokens", type=int, default=2048, help="prefill tokens (with --workload prefill)")
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     args = ap.parse_args()
@@ -503,7 +537,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    out = run_ours(args, rank, world, device)
+    out = run_ours(args, rank, world, device) if args.workload == "decode" else run_prefill(args, rank, world, device)
     if rank == 0 and args.cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline_line(workloads.LLAMA3_8B)
     if rank == 0:

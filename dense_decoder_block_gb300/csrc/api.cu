@@ -245,10 +245,15 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         const GemmProblem pq = problem_qkv(b, M, w.xn);
         LLAMA_TRY(launch_gemm(pq, eq, PATH_AUTO, w.gemm_partial, s), "qkv");
         if (gemm_needs_reduce(pq, PATH_AUTO)) LLAMA_TRY(reduce(pq, eq, EPI_QKV), "qkv_reduce");
-        // 3. attention
+        // 3. attention (tensor cores when the group size divides 128; one choice per handle)
         mark();
-        if (decode) LLAMA_TRY(launch_attention_decode(at, s), "attention_decode");
-        else LLAMA_TRY(launch_attention_prefill(at, s), "attention_prefill");
+        if (attention_tc_supported(d.n_heads, d.n_kv_heads, d.head_dim)) {
+            if (decode) LLAMA_TRY(launch_attention_tc_decode(at, 0, s), "attention_decode");
+            else LLAMA_TRY(launch_attention_tc_prefill(at, s), "attention_prefill");
+        } else {
+            if (decode) LLAMA_TRY(launch_attention_decode(at, s), "attention_decode");
+            else LLAMA_TRY(launch_attention_prefill(at, s), "attention_prefill");
+        }
         // 4. O projection + residual -> h, 5. RMSNorm_2 -> hn
         mark();
         GemmEpi eo;

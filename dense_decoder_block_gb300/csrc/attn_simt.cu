@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_prefill(const AttnK a) {
     T* Vs = Ks + kAttnChunk * TL::LD;
     float* qs = reinterpret_cast<float*>(Vs + kAttnChunk * TL::LD);
 
-    if (threadIdx.x == 0) ptx_launch_dependents();
     ptx_wait();
+    if (threadIdx.x == 0) ptx_launch_dependents();
     const int g = blockIdx.y, b = blockIdx.z;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int t0 = blockIdx.x * a.tq;
@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
     T* Vs = Ks + kAttnChunk * TL::LD;
     float* qs = reinterpret_cast<float*>(Vs + kAttnChunk * TL::LD);
 
-    if (threadIdx.x == 0) ptx_launch_dependents();
     ptx_wait();
+    if (threadIdx.x == 0) ptx_launch_dependents();
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int pos = base_position(a);
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
     for (int r = warp; r < n_rep; r += kWarps) {
         float m, l, o[DPL];
         chunk_partial<T, DH>(qs + r * DH, Ks, Vs, jmax, a.scale_log2, m, l, o);
-        float* dst = a.partial + ((((size_t)b * a.n_kv_heads + g) * a.n_chunks + c) * n_rep + r) * (DH + 2);
+        float* dst = a.partial + ((((size_t)b * a.n_kv_heads + g) * a.n_chunks + c) * n_rep + r) * part_stride(DH);
 #pragma unroll
         for (int e = 0; e < DPL; ++e) dst[lane * DPL + e] = o[e];
         if (lane == 0) {
@@ -279,16 +279,16 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
 template <typename T, int DH>
 __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     constexpr int DPL = DH / 32;
-    if (threadIdx.x == 0) ptx_launch_dependents();
     ptx_wait();
+    if (threadIdx.x == 0) ptx_launch_dependents();
     const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int g = h / n_rep, r = h % n_rep;
     const int pos = base_position(a);
     if (pos < 0 || pos >= a.max_pos) return;
     const int n_chunks = pos / kAttnChunk + 1;
-    const float* base = a.partial + (((size_t)b * a.n_kv_heads + g) * a.n_chunks * n_rep + r) * (DH + 2);
-    const size_t cstride = (size_t)n_rep * (DH + 2);
+    const float* base = a.partial + (((size_t)b * a.n_kv_heads + g) * a.n_chunks * n_rep + r) * part_stride(DH);
+    const size_t cstride = (size_t)n_rep * part_stride(DH);
     float M = base[DH], L = base[DH + 1], O[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) O[e] = base[lane * DPL + e];
@@ -358,10 +358,29 @@ cudaError_t decode_impl(const AttnArgs& a, cudaStream_t s) {
     return launch_pdl(k_attn_decode_combine<T, DH>, dim3(a.n_heads, a.batch), dim3(32), 0, s, k);
 }
 
+template <typename T, int DH>
+cudaError_t combine_impl(const AttnArgs& a, cudaStream_t s) {
+    return launch_pdl(k_attn_decode_combine<T, DH>, dim3(a.n_heads, a.batch), dim3(32), 0, s, make_k(a));
+}
+
 }  // namespace
 
 size_t attn_decode_partial_bytes(int batch, int n_kv_heads, int n_chunks, int n_rep, int head_dim) {
-    return (size_t)batch * n_kv_heads * n_chunks * n_rep * (head_dim + 2) * sizeof(float);
+    return (size_t)batch * n_kv_heads * n_chunks * n_rep * part_stride(head_dim) * sizeof(float);
+}
+
+cudaError_t launch_attention_combine(const AttnArgs& a, cudaStream_t s) {
+    if (a.batch <= 0) return cudaSuccess;
+    if (a.dtype == LLAMA_BF16) {
+        if (a.head_dim == 128) return combine_impl<bf16, 128>(a, s);
+        return cudaErrorInvalidValue;
+    }
+    switch (a.head_dim) {
+        case 32: return combine_impl<float, 32>(a, s);
+        case 64: return combine_impl<float, 64>(a, s);
+        case 128: return combine_impl<float, 128>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s) {

@@ -22,6 +22,9 @@ constexpr int kAttnChunk = 128;
 // in prefill and decode alike.
 constexpr int kSegK = 1024;
 constexpr int kRopeMaxPairs = 64;   // head_dim <= 128
+// Floats per decode attention chunk partial of one query row: o[head_dim], m, l, 2 pad.
+__host__ __device__ constexpr int part_stride(int head_dim) { return head_dim + 4; }
+constexpr int kPartStride = part_stride(128);
 
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 __device__ __forceinline__ float ld_bf16(const bf16* p) { return __bfloat162float(*p); }
@@ -74,8 +77,13 @@ __device__ __forceinline__ float rms_tree_256(float ss, float* red) {
 }
 
 // Launch with programmatic stream serialization: the kernel may begin while the
-// previous kernel on the stream drains; every kernel of the block calls
-// griddepcontrol.wait before it reads anything an earlier kernel wrote.
+// previous kernel on the stream drains.  Every kernel of the library calls
+// griddepcontrol.wait before it reads anything an earlier kernel wrote, and lets
+// its own dependents start (griddepcontrol.launch_dependents) only after that
+// wait: so when a kernel starts, the kernel two places earlier and everything
+// before it have completed, and only the immediately preceding kernel may still
+// be running.  Reading data that predecessor did not write before the wait
+// (weights, older KV-cache rows) is therefore safe.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args&&... args) {

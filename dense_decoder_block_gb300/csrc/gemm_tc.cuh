@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else if (tile >= a.q_tiles) { mapA = &mA1; arow = (tile - a.q_tiles) * kTileF; }
     }
 
-    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -190,6 +189,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 load_a(it, kb_first + it);
             }
             ptx::griddep_wait();
+            ptx::griddep_launch_dependents();
             for (int it = 0; it < n_pre; ++it) load_b(it, kb_first + it);
             int stage = n_pre % C::STAGES;
             uint32_t phase = (n_pre == C::STAGES) ? 1u : 0u;

@@ -66,7 +66,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
     // unit u -> (tile, segment), segments of one tile on neighbouring CTAs
     auto unit_tile = [&](int u) { return u / a.n_segs; };
@@ -110,6 +109,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         pre_kb[it] = kb;
                         if (it == n_pre - 1) {
                             ptx::griddep_wait();
+                            ptx::griddep_launch_dependents();
                             for (int j = 0; j < n_pre; ++j)
                                 ptx::tma_load_2d(smem + j * C::STAGE_BYTES + NACC * kABytes, &mB, &full[j],
                                                  pre_kb[j] * kBlockK, 0);

@@ -102,8 +102,14 @@ struct AttnArgs {
     int* err = nullptr;
 };
 size_t attn_decode_partial_bytes(int batch, int n_kv_heads, int n_chunks, int n_rep, int head_dim);
-cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);
-cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention_prefill(const AttnArgs& a, cudaStream_t s);   // CUDA cores
+cudaError_t launch_attention_decode(const AttnArgs& a, cudaStream_t s);    // CUDA cores, + combine
+// Ascending fold of the decode chunk partials into o (shared by both decode kernels).
+cudaError_t launch_attention_combine(const AttnArgs& a, cudaStream_t s);
+// Tensor-core attention (bf16, head_dim 128, n_heads / n_kv_heads dividing 128).
+bool attention_tc_supported(int n_heads, int n_kv_heads, int head_dim);
+cudaError_t launch_attention_tc_prefill(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention_tc_decode(const AttnArgs& a, int chunks_per_cta, cudaStream_t s);
 
 // fp32 SIMT block pieces
 cudaError_t launch_linear_f32(const float* x, const float* w, const float* w2, const float* resid, float* y, int M,

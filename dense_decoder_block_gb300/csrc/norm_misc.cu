@@ -22,8 +22,8 @@ template <typename T, int EPT>
 __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ x, const T* __restrict__ g,
                                                           T* __restrict__ y, int d, float eps) {
     __shared__ float red[kNormThreads / 32];
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x, tid = threadIdx.x;
     const T* xr = x + (size_t)row * d;
     T* yr = y + (size_t)row * d;

@@ -20,8 +20,8 @@ constexpr int kThreads = 256;
 constexpr int kBatch = 16;   // segments loaded per round trip
 
 __device__ __forceinline__ void griddep() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Ascending sum over segments of 4 consecutive fp32 values at `off`.
