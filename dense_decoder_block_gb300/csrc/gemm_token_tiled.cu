@@ -1,40 +1,46 @@
-// Token-tiled (prefill) instantiations of the tcgen05 projection kernel.
-#include "gemm_tc.cuh"
+// Token-tiled (prefill) instantiations of the persistent tcgen05 projection kernel.
+#include "gemm_tt.cuh"
 
 namespace llama {
 
 template <int BN, bool DUAL, int EPI>
 static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0, const CUtensorMap& a1,
                           const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
-    using C = GemmCfg<BN, DUAL>;
-    auto kern = k_gemm_tc<BN, DUAL, EPI>;
+    using C = TtCfg<BN, DUAL>;
+    auto kern = k_gemm_tt<BN, DUAL, EPI>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        // The register split inside the kernel must fit the block's launch allocation.
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+        if (r != cudaSuccess) return r;
+        if (fa.numRegs * C::THREADS < C::REGS_NEEDED) return cudaErrorInvalidConfiguration;
+        r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (r != cudaSuccess) return r;
         attr = true;
     }
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
-    dim3 grid(p.F / kTileF, (p.M + BN - 1) / BN);
-    return launch_pdl(kern, grid, dim3(kGemmThreads), C::SMEM_BYTES, s, a0, a1, a2, mb, ka);
+    const int tiles = (p.F / kTileF) * ((p.M + BN - 1) / BN);
+    const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, a0, a1, a2, mb, ka);
 }
 
 cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
                                const CUtensorMap& a1, const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
     if (p.dual) {
         if (ka.e.kind != EPI_SWIGLU) return cudaErrorInvalidValue;
-        return run_tt<64, true, EPI_SWIGLU>(p, ka, a0, a1, a2, x, s);
+        return run_tt<128, true, EPI_SWIGLU>(p, ka, a0, a1, a2, x, s);
     }
     switch (ka.e.kind) {
         case EPI_QKV:
-            return run_tt<128, false, EPI_QKV>(p, ka, a0, a1, a2, x, s);
+            return run_tt<256, false, EPI_QKV>(p, ka, a0, a1, a2, x, s);
         case EPI_RESID:
-            return run_tt<128, false, EPI_RESID>(p, ka, a0, a1, a2, x, s);
+            return run_tt<256, false, EPI_RESID>(p, ka, a0, a1, a2, x, s);
         case EPI_PLAIN:
-            return run_tt<128, false, EPI_PLAIN>(p, ka, a0, a1, a2, x, s);
+            return run_tt<256, false, EPI_PLAIN>(p, ka, a0, a1, a2, x, s);
         case EPI_LOGITS:
-            return run_tt<128, false, EPI_LOGITS>(p, ka, a0, a1, a2, x, s);
+            return run_tt<256, false, EPI_LOGITS>(p, ka, a0, a1, a2, x, s);
         default:
             return cudaErrorInvalidValue;
     }

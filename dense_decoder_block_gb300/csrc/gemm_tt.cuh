@@ -1,0 +1,239 @@
+// Persistent token-tiled projection (prefill, M > 32 tokens).
+//
+// Same arithmetic as the weight-streaming kernel (gemm_ws.cuh): per output, one
+// tcgen05.mma chain per K-segment of seg_kb k-blocks, segment results added in
+// ascending fp32 order.  Here one CTA per SM walks output tiles of 128 features
+// x BN tokens (BN = 256; 128 with the gate/up pair); for every tile it runs the
+// segments' chains into two alternating TMEM buffers while sixteen epilogue
+// warps (four per TMEM lane quarter, each owning a quarter of the columns) keep
+// the running sums in registers; after a tile's last segment they apply the
+// fused epilogue and store, while the MMAs of the next tile already run.
+// Tiles are taken in groups of up to 8 token blocks per feature tile, so a
+// weight tile is reused from L2 by the CTAs working on the group.
+//
+// Warp roles (640 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
+// issuer, warps 2-3 idle; warps 4..19 = epilogue, warp w reading TMEM lane
+// quarter w % 4 and column quarter (w - 4) / 4.  Warpgroup 0 gives registers
+// to the epilogue warpgroups, whose running sums take 64 per thread.
+#pragma once
+#include "gemm_tc.cuh"
+
+namespace llama {
+
+template <int BN, bool DUAL>
+struct TtCfg {
+    static constexpr int NACC = DUAL ? 2 : 1;
+    static constexpr int B_BYTES = BN * kBlockK * 2;
+    static constexpr int STAGE_BYTES = NACC * kABytes + B_BYTES;
+    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
+    static constexpr int ACC_COLS = NACC * BN;                 // one TMEM buffer
+    static constexpr int TMEM_COLS = 512;                      // two buffers
+    static constexpr int EPI_WARPS = 16;
+    static constexpr int CPT = BN / 4;                         // columns per thread per accumulator
+    static constexpr int THREADS = 128 + 32 * EPI_WARPS;       // warpgroup 0 + four epilogue warpgroups
+    static constexpr int REGS_CTRL = 56;                       // warpgroup 0 after the split
+    static constexpr int REGS_EPI = 104;                       // epilogue warpgroups after the split
+    static constexpr int REGS_NEEDED = 128 * REGS_CTRL + 32 * EPI_WARPS * REGS_EPI;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static_assert(2 * ACC_COLS <= 512, "two TMEM buffers");
+};
+constexpr int kTtGroup = 8;   // token blocks per feature tile, consecutively
+
+template <int BN, bool DUAL, int EPI>
+__global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
+    k_gemm_tt(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+              const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mB, const GemmKArgs a) {
+    using C = TtCfg<BN, DUAL>;
+    constexpr int NACC = C::NACC;
+    constexpr int CPT = C::CPT;
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* tfull = empty + C::STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint32_t* tmem_holder = (uint32_t*)(tempty + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total_kb = a.K / kBlockK;
+    const int m_tiles = a.F / kTileF;
+    const int n_blocks = (a.M + BN - 1) / BN;
+    const int n_tiles = m_tiles * n_blocks;
+    int* err = a.e.err;
+
+    // tile t -> (feature tile m, token block n), groups of kTtGroup token blocks
+    auto tile_mn = [&](int t, int& m, int& n) {
+        const int grp = t / (kTtGroup * m_tiles);
+        const int rem = t - grp * kTtGroup * m_tiles;
+        const int gn = min(kTtGroup, n_blocks - grp * kTtGroup);
+        m = rem / gn;
+        n = grp * kTtGroup + (rem - m * gn);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::STAGES; ++i) { ptx::mbar_init(&full[i], 1); ptx::mbar_init(&empty[i], 1); }
+        for (int i = 0; i < 2; ++i) { ptx::mbar_init(&tfull[i], 1); ptx::mbar_init(&tempty[i], C::EPI_WARPS); }
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    if (warp < 4) {
+        ptx::setmaxnreg_dec<C::REGS_CTRL>();
+        if (warp == 0) {
+            // ---------------------------------------------------------- TMA producer
+            if (lane == 0) {
+                ptx::prefetch_tmap(&mA0);
+                if (EPI == EPI_QKV || DUAL) ptx::prefetch_tmap(&mA1);
+                if (EPI == EPI_QKV) ptx::prefetch_tmap(&mA2);
+                ptx::prefetch_tmap(&mB);
+                int stage = 0;
+                uint32_t phase = 0;
+                int it = 0;
+                bool waited = false, ok = true;
+                // Token block of this CTA's i-th k-block load (i < total k-blocks of the CTA).
+                auto load_b_of = [&](int i) {
+                    int m, n;
+                    tile_mn(blockIdx.x + (i / total_kb) * gridDim.x, m, n);
+                    ptx::tma_load_2d(smem + (i % C::STAGES) * C::STAGE_BYTES + NACC * kABytes, &mB,
+                                     &full[i % C::STAGES], (i % total_kb) * kBlockK, n * BN);
+                };
+                for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                    int m, n;
+                    tile_mn(t, m, n);
+                    const CUtensorMap* mapA = &mA0;
+                    int arow = m * kTileF;
+                    if constexpr (EPI == EPI_QKV) {
+                        if (m >= a.q_tiles + a.k_tiles) { mapA = &mA2; arow = (m - a.q_tiles - a.k_tiles) * kTileF; }
+                        else if (m >= a.q_tiles) { mapA = &mA1; arow = (m - a.q_tiles) * kTileF; }
+                    }
+                    for (int kb = 0; kb < total_kb; ++kb, ++it) {
+                        uint8_t* dst = smem + stage * C::STAGE_BYTES;
+                        if (it >= C::STAGES && !ptx::mbar_wait(&empty[stage], phase ^ 1, err)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        ptx::tma_load_2d(dst, mapA, &full[stage], kb * kBlockK, arow);
+                        if (DUAL) ptx::tma_load_2d(dst + kABytes, &mA1, &full[stage], kb * kBlockK, arow);
+                        if (waited) {
+                            ptx::tma_load_2d(dst + NACC * kABytes, &mB, &full[stage], kb * kBlockK, n * BN);
+                        } else if (it == C::STAGES - 1) {
+                            // The weights do not depend on the previous kernel: the first stages
+                            // of them are in flight before waiting for it; then the activations.
+                            ptx::griddep_wait();
+                            ptx::griddep_launch_dependents();
+                            for (int j = 0; j <= it; ++j) load_b_of(j);
+                            waited = true;
+                        }
+                        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                    }
+                }
+                if (!waited && ok) {   // fewer k-blocks than stages in total
+                    ptx::griddep_wait();
+                    ptx::griddep_launch_dependents();
+                    for (int j = 0; j < it; ++j) load_b_of(j);
+                }
+                if (!ok) {
+                    for (int i = 0; i < C::STAGES; ++i) ptx::mbar_wait_drain(&full[i], phase ^ (i < stage ? 0u : 1u));
+                }
+            }
+        } else if (warp == 1) {
+            // ---------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                int stage = 0, use = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                    for (int seg = 0; seg < a.n_segs && ok; ++seg, ++use) {
+                        const int buf = use & 1;
+                        if (!ptx::mbar_wait(&tempty[buf], ((use >> 1) & 1) ^ 1, err)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        const uint32_t d = tmem_base + buf * C::ACC_COLS;
+                        const int kb0 = seg * a.seg_kb;
+                        const int kb1 = min(kb0 + a.seg_kb, total_kb);
+                        for (int kb = kb0; kb < kb1; ++kb) {
+                            if (!ptx::mbar_wait(&full[stage], phase, err)) { ok = false; break; }
+                            ptx::tc_fence_after();
+                            const uint32_t sa = ptx::smem_u32(smem + stage * C::STAGE_BYTES);
+                            const uint32_t sb = sa + NACC * kABytes;
+#pragma unroll
+                            for (int k = 0; k < kBlockK / 16; ++k) {
+                                const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+                                const uint64_t bdesc = ptx::sw128_kmajor_desc(sb + 32 * k);
+                                ptx::umma_bf16(d, ptx::sw128_kmajor_desc(sa + 32 * k), bdesc, IDESC, accum);
+                                if (DUAL)
+                                    ptx::umma_bf16(d + BN, ptx::sw128_kmajor_desc(sa + kABytes + 32 * k), bdesc, IDESC, accum);
+                            }
+                            ptx::umma_commit(&empty[stage]);
+                            if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+                        }
+                        if (ok) ptx::umma_commit(&tfull[buf]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue (16 warps)
+        ptx::setmaxnreg_inc<C::REGS_EPI>();
+        ptx::griddep_wait();   // residuals come from earlier kernels
+        const int ew = warp - 4;
+        const int quarter = warp & 3;
+        const int cg = ew >> 2;                   // column group 0..3
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        int use = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+            int m, n;
+            tile_mn(t, m, n);
+            // -0 + s == s for every fp32 s, so the sum starts exactly at segment 0
+            float acc[NACC][CPT];
+#pragma unroll
+            for (int ac = 0; ac < NACC; ++ac)
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) acc[ac][j] = -0.0f;
+            for (int seg = 0; seg < a.n_segs; ++seg, ++use) {
+                const int buf = use & 1;
+                if (ok) ok = ptx::mbar_wait(&tfull[buf], (use >> 1) & 1, err);
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int ac = 0; ac < NACC; ++ac) {
+                    constexpr int CH = 16;
+#pragma unroll
+                    for (int c = 0; c < CPT / CH; ++c) {
+                        float tmp[CH];
+                        ptx::tmem_ld<CH>(tmem_base + lane_addr + buf * C::ACC_COLS + ac * BN + cg * CPT + c * CH, tmp);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < CH; ++j) acc[ac][c * CH + j] = __fadd_rn(acc[ac][c * CH + j], tmp[j]);
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
+            }
+            if (ok) {
+                const int ncol0 = n * BN + cg * CPT;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    const int col = ncol0 + j;
+                    epi_store<EPI>(a, m, row, col, acc[0][j], acc[NACC - 1][j], col < a.M);
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace llama

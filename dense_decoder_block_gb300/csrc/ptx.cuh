@@ -37,6 +37,16 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // Block until every grid this one depends on has completed and its memory is visible.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------- register split
+// Move registers between warpgroups (every warp of a warpgroup executes the same
+// one).  An increase waits until enough registers are free in the block's pool,
+// which is threads x registers-per-thread at launch: the host checks that the
+// split fits that pool before launching.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
