@@ -72,6 +72,15 @@ def gateup_launch_bytes(dims, B):
     return 2 * (2 * dims.d_ff * dims.d_model + B * dims.d_model + B * dims.d_ff)
 
 
+def prefill_stage_flops(dims, B, T):
+    """Algorithmic FLOPs of each tensor-core stage of a causal prefill step."""
+    d, f = dims.d_model, dims.d_ff
+    q, kv = dims.n_heads * dims.head_dim, dims.n_kv_heads * dims.head_dim
+    n = B * T
+    return {"qkv": 2 * n * d * (q + 2 * kv), "attention": B * 4 * dims.n_heads * dims.head_dim * (T * (T + 1) // 2),
+            "o_proj": 2 * n * q * d, "gate_up": 2 * n * d * 2 * f, "down": 2 * n * f * d}
+
+
 def prefill_flops(dims, B, T):
     d, f = dims.d_model, dims.d_ff
     q, kv = dims.n_heads * dims.head_dim, dims.n_kv_heads * dims.head_dim
@@ -242,7 +251,7 @@ def run_ours(args, rank, world, device):
     value = tokens / (ms / 1e3)
 
     # --- per-stage durations (second pass, events between the block's kernels)
-    stage_ms = stage_profile(blk, x, kv, y, ws, pos_dev, device, args.steps)
+    stage_ms = stage_profile(blk, lambda st: blk.decode_devpos(x, kv, pos_dev, y, ws, st), device, args.steps)
 
     # --- end to end through the public API with host buffers
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -336,6 +345,7 @@ def run_prefill(args, rank, world, device):
     stream = torch.cuda.current_stream(device)
     ms = time_region(lambda: blk.prefill(x, kv, y, ws), args.steps, args.warmup, stream)
     assert blk.poll_error() == 0
+    stage_ms = stage_profile(blk, lambda st: blk.prefill(x, kv, y, ws, st), device, max(3, args.steps))
     _, bf16_peak, _, peak_kind = peaks()
     fl = prefill_flops(dims, 1, T)
     tf = fl / (ms / 1e3) / 1e12
@@ -345,6 +355,9 @@ def run_prefill(args, rank, world, device):
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) x)",
             "config": {"workload": f"Llama-3 8B-shaped causal prefill block, batch 1, T={T}", "tokens": T},
             "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind,
+            "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+            "stage_tflops": {k: round(v / (stage_ms[k] / 1e3) / 1e12, 1)
+                             for k, v in prefill_stage_flops(dims, 1, T).items()},
             "gpu_launches": args.steps * 7}
 
 
@@ -356,11 +369,11 @@ def blk_launches_per_decode():
 STAGES = ("rmsnorm_1", "qkv", "attention", "o_proj", "rmsnorm_2", "gate_up", "down")
 
 
-def stage_profile(blk, x, kv, y, ws, pos_dev, device, steps):
-    """Average device time of each stage of the decode step.  The library records
-    CUDA events between its kernels on the launching stream; the step (with those
-    event records) is captured as a graph and replayed, so the stages run back to
-    back as in the timed region."""
+def stage_profile(blk, launch, device, steps):
+    """Average device time of each stage of one block step (`launch(stream)` runs
+    it).  The library records CUDA events between its kernels on the launching
+    stream; the step (with those event records) is captured as a graph and
+    replayed, so the stages run back to back as in the timed region."""
     import dense_decoder_block_gb300 as ddb
     n = len(STAGES) + 1
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -373,7 +386,7 @@ def stage_profile(blk, x, kv, y, ws, pos_dev, device, steps):
     try:
         with torch.cuda.stream(cap):
             with torch.cuda.graph(g, stream=cap):
-                blk.decode_devpos(x, kv, pos_dev, y, ws, cap)
+                launch(cap)
     finally:
         ddb.llama_block_set_stage_events(blk.h, None)
     sums = [0.0] * len(STAGES)

@@ -226,8 +226,9 @@ __global__ void __launch_bounds__(kThreads) k_attn_prefill(const AttnK a) {
         if (t >= a.tokens) continue;
         const int h = g * n_rep + r % n_rep;
         T* dst = out + ((size_t)b * a.tokens + t) * qld + (size_t)h * DH + lane * DPL;
+        const float inv_l = __frcp_rn(L[rr]);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) from_f(dst + e, __fdiv_rn(O[rr][e], L[rr]));
+        for (int e = 0; e < DPL; ++e) from_f(dst + e, __fmul_rn(O[rr][e], inv_l));
     }
 }
 
@@ -300,8 +301,9 @@ __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
         fold<DPL>(M, L, O, p[DH], p[DH + 1], o);
     }
     T* dst = reinterpret_cast<T*>(a.o) + (size_t)b * a.n_heads * DH + (size_t)h * DH + lane * DPL;
+    const float inv_l = __frcp_rn(L);
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) from_f(dst + e, __fdiv_rn(O[e], L));
+    for (int e = 0; e < DPL; ++e) from_f(dst + e, __fmul_rn(O[e], inv_l));
 }
 
 template <typename T, int DH>

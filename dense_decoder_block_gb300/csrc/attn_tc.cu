@@ -9,19 +9,17 @@
 // Unit of work: a 128-row query tile of one KV group against one 128-key chunk.
 // Prefill tiles hold 128 / n_rep consecutive tokens x the n_rep heads of the
 // group (row = token * n_rep + head); decode tiles hold the group's n_rep heads
-// of one token (the other rows are zero).
+// of one token.
 //   S   = Q K^T        tcgen05.mma M=128 N=128 K=128, both operands K-major
-//   softmax, one thread per row (sequential over the chunk's keys):
-//         t_j = S_j * log2(e)/sqrt(d_h); m = max_{j<=jmax} t_j;
-//         p_j = bf16(2^(t_j - m)) (0 past jmax); l = sum_j p_j in key order
+//   softmax of each row over the chunk (softmax_keys below gives the exact
+//         definition every kernel follows), P rounded to bf16
 //   O_c = P V          tcgen05.mma M=128 N=128 K=128, V MN-major (as cached)
 // Chunks are folded in ascending order from chunk 0 with one fold formula:
-// prefill folds in TMEM as it walks the chunks, decode stores each chunk's
-// (O_c, m, l) and the combine kernel (attn_simt.cu) folds them in the same order,
-// so a decode row equals the prefill row at the same position bit for bit.
-//
-// Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..5 = softmax / fold
-// (thread = row; warp w reads TMEM lane quarter w % 4).
+// prefill folds as it walks the chunks, decode stores each chunk's (O_c, m, l)
+// and the combine kernel (attn_simt.cu) folds them in the same order, so a
+// decode row equals the prefill row at the same position bit for bit.
+// Kernels: k_attn_pf (prefill), k_attn_tc_dec (decode, up to 8 query heads per
+// KV head), k_attn_tc_wide (decode, larger groups).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -42,7 +40,7 @@ constexpr int KV_STAGE = 4 * kSub;
 constexpr int OFF_P = OFF_KV + 2 * KV_STAGE;    // P: 2 sub-tiles (keys 0-63, 64-127)
 constexpr int OFF_BAR = OFF_P + 2 * kSub;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-constexpr int TM_S = 0, TM_OC = 128, TM_O = 256;   // TMEM columns
+constexpr int TM_S = 0, TM_OC = 128;   // TMEM columns
 constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128);
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32_bmn(128, 128);
 
@@ -62,35 +60,45 @@ struct TcArgs {
 // Byte offset of the 16-byte chunk `c16` (0..7) of row `r` in a 128-byte-swizzled sub-tile.
 __device__ __forceinline__ uint32_t sw_off(int r, int c16) { return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4)); }
 
-// 2^x on the special-function unit (PTX ex2.approx: max relative error 2^-22,
-// far below the bf16 rounding of p that follows).
+// 2^x on the special-function unit (PTX ex2.approx.ftz: max relative error
+// 2^-22, far below the bf16 rounding of p that follows; results below the
+// smallest normal float are flushed to zero).
 __device__ __forceinline__ float ex2(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-// The softmax of one query row over one 128-key chunk.  Both kernels compute
+// The softmax of one query row over one 128-key chunk.  Every kernel computes
 // exactly this (prefill with one thread per row, decode with four lanes per row):
-//   t_j = S_j * scale_log2                      (keys 0..jmax visible; jmax < 0: none)
-//   m   = max_{j <= jmax} t_j                   (exact, any order)
-//   p_j = bf16(2^(t_j - m)), 0 for hidden keys
+//   m   = c * max_{j <= jmax} S_j,  c = log2(e) / sqrt(d_h)   (keys 0..jmax visible;
+//         jmax < 0: none, m = -inf); rounding is monotonic, so this equals the
+//         max of the rounded products c * S_j whatever the order
+//   p_j = bf16(2^fma(S_j, c, -m)), 0 for hidden keys
 //   l   = ((L0 + L1) + L2) + L3,  Lq = sum of p_j over keys 32q..32q+31 in key order
 // The P row goes to the two 64-key sub-tiles of the swizzled K-major P operand
-// (p_sub_stride bytes apart) at row `prow` when write_p.
-__device__ __forceinline__ void softmax_quarter(const float* sv, int j0, int jmax, float scale_log2, float m,
-                                                uint32_t (&packed)[16], float& lq) {
-    lq = 0.f;
+// (p_sub_stride bytes apart) at row `prow`.
+__device__ __forceinline__ float softmax_p(float s, float scale_log2, float m) {
+    return ex2(__fmaf_rn(s, scale_log2, -m));
+}
+template <int N>
+__device__ __forceinline__ void softmax_keys(const float* sv, int j0, int jmax, float scale_log2, float m,
+                                             uint32_t* packed, float& lq) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
+    for (int j = 0; j < N; j += 2) {
         float p0 = 0.f, p1 = 0.f;
-        if (j0 + j <= jmax) p0 = ex2(__fsub_rn(__fmul_rn(sv[j], scale_log2), m));
-        if (j0 + j + 1 <= jmax) p1 = ex2(__fsub_rn(__fmul_rn(sv[j + 1], scale_log2), m));
+        if (j0 + j <= jmax) p0 = softmax_p(sv[j], scale_log2, m);
+        if (j0 + j + 1 <= jmax) p1 = softmax_p(sv[j + 1], scale_log2, m);
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         lq = __fadd_rn(lq, __low2float(pb));
         lq = __fadd_rn(lq, __high2float(pb));
         packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
     }
+}
+__device__ __forceinline__ void softmax_quarter(const float* sv, int j0, int jmax, float scale_log2, float m,
+                                                uint32_t (&packed)[16], float& lq) {
+    lq = 0.f;
+    softmax_keys<32>(sv, j0, jmax, scale_log2, m, packed, lq);
 }
 __device__ __forceinline__ void store_p_quarter(uint8_t* p_base, uint32_t p_sub_stride, int prow, int q,
                                                 const uint32_t (&packed)[16]) {
@@ -100,12 +108,72 @@ __device__ __forceinline__ void store_p_quarter(uint8_t* p_base, uint32_t p_sub_
         *reinterpret_cast<uint4*>(psub + sw_off(prow, (q & 1) * 4 + q4)) =
             make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
 }
-__device__ __forceinline__ float quarter_max(const float* sv, int j0, int jmax, float scale_log2) {
+// max of the visible raw scores among sv[0..31] (keys j0..j0+31); -inf if none
+__device__ __forceinline__ float quarter_max_raw(const float* sv, int j0, int jmax) {
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-        if (j0 + j <= jmax) mx[j & 3] = fmaxf(mx[j & 3], __fmul_rn(sv[j], scale_log2));
+        if (j0 + j <= jmax) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
     return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// Thread-per-row form for the prefill kernel, with compact code (its rolled
+// loops keep the instruction stream small enough for the instruction cache
+// while several warps run it).  Pass 1 takes the max of the raw scores; pass 2
+// walks 8-key groups of all four quarters at once, so the four quarter sums are
+// independent chains (each still adds its keys in key order).  A hidden key is
+// set to -inf before the exponential, which gives exactly p = 0.
+__device__ __forceinline__ void softmax_row_regs(uint32_t s_taddr, int jmax, float scale_log2, uint8_t* p_base,
+                                                 uint32_t p_sub_stride, int prow, float& m_out, float& l_out) {
+    const bool full = __all_sync(0xffffffffu, jmax >= kAttnChunk - 1);
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+        float v[32];
+        ptx::tmem_ld<32>(s_taddr + cb * 32, v);
+        ptx::tmem_wait_ld();
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (cb * 32 + j <= jmax) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+        }
+    }
+    const float m = __fmul_rn(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), scale_log2);
+    const float m_use = (jmax >= 0) ? m : 0.f;   // a row with no visible key: every p is 0
+    float lq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {   // keys 8g..8g+7 of every quarter
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ptx::tmem_ld<8>(s_taddr + q * 32 + g * 8, v + q * 8);
+        ptx::tmem_wait_ld();
+        if (!full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    if (q * 32 + g * 8 + t > jmax) v[q * 8 + t] = -INFINITY;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t packed[4];
+#pragma unroll
+            for (int t = 0; t < 8; t += 2) {
+                const __nv_bfloat162 pb = __floats2bfloat162_rn(softmax_p(v[q * 8 + t], scale_log2, m_use),
+                                                                softmax_p(v[q * 8 + t + 1], scale_log2, m_use));
+                lq[q] = __fadd_rn(lq[q], __low2float(pb));
+                lq[q] = __fadd_rn(lq[q], __high2float(pb));
+                packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+            }
+            *reinterpret_cast<uint4*>(p_base + (q >> 1) * p_sub_stride + sw_off(prow, (q & 1) * 4 + g)) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+    m_out = m;
+    l_out = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), lq[2]), lq[3]);
 }
 
 // Thread-per-row form (prefill): this thread's S row is at s_taddr in TMEM.
@@ -118,17 +186,29 @@ __device__ __forceinline__ void softmax_row(uint32_t s_taddr, int jmax, float sc
         float sv[32];
         ptx::tmem_ld<32>(s_taddr + cb * 32, sv);
         ptx::tmem_wait_ld();
-        m = fmaxf(m, quarter_max(sv, cb * 32, jmax, scale_log2));
+        m = fmaxf(m, quarter_max_raw(sv, cb * 32, jmax));
     }
+    m = __fmul_rn(m, scale_log2);
     float lq[4];
 #pragma unroll
     for (int cb = 0; cb < 4; ++cb) {
-        float sv[32];
-        ptx::tmem_ld<32>(s_taddr + cb * 32, sv);
-        ptx::tmem_wait_ld();
-        uint32_t packed[16];
-        softmax_quarter(sv, cb * 32, jmax, scale_log2, m, packed, lq[cb]);
-        if (write_p) store_p_quarter(p_base, p_sub_stride, prow, cb, packed);
+        // 16 keys at a time (fewer live registers); the sum runs on in key order
+        lq[cb] = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float sv[16];
+            ptx::tmem_ld<16>(s_taddr + cb * 32 + hh * 16, sv);
+            ptx::tmem_wait_ld();
+            uint32_t packed[8];
+            softmax_keys<16>(sv, cb * 32 + hh * 16, jmax, scale_log2, m, packed, lq[cb]);
+            if (write_p) {
+                uint8_t* psub = p_base + (cb >> 1) * p_sub_stride;
+#pragma unroll
+                for (int q4 = 0; q4 < 2; ++q4)
+                    *reinterpret_cast<uint4*>(psub + sw_off(prow, (cb & 1) * 4 + hh * 2 + q4)) =
+                        make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
+            }
+        }
     }
     m_out = m;
     l_out = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), lq[2]), lq[3]);
@@ -160,9 +240,10 @@ __device__ __forceinline__ void softmax_rows8(uint32_t s_taddr, float* srow, int
         sv[4 * q4] = v.x; sv[4 * q4 + 1] = v.y; sv[4 * q4 + 2] = v.z; sv[4 * q4 + 3] = v.w;
     }
     const int jmax = __shfl_sync(0xffffffffu, jmax_of_row, r);
-    float m = quarter_max(sv, q * 32, jmax, scale_log2);
+    float m = quarter_max_raw(sv, q * 32, jmax);
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = __fmul_rn(m, scale_log2);
     uint32_t packed[16];
     float lq;
     softmax_quarter(sv, q * 32, jmax, scale_log2, m, packed, lq);
@@ -176,14 +257,17 @@ __device__ __forceinline__ void softmax_rows8(uint32_t s_taddr, float* srow, int
     __syncwarp();
 }
 
-template <bool DECODE>
+// Decode attention for groups of more than 8 query heads per KV head (a query
+// tile holds the group's heads, the other rows are zero).  The chunks of one
+// (sequence, KV head) are split over CTAs; each CTA stores every chunk's
+// (O_c, m, l) for the combine kernel.  Warps: 0 = TMA producer, 1 = TMEM owner +
+// MMA issuer, 2..5 = softmax + partial store (thread = row; warp w reads TMEM
+// lane quarter w % 4).
 __global__ void __launch_bounds__(kThreads, 1)
-    k_attn_tc(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-              const __grid_constant__ CUtensorMap mV, const TcArgs a) {
+    k_attn_tc_wide(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
-    uint64_t* q_full = bars + 0;
     uint64_t* kv_full = bars + 1;    // [2]
     uint64_t* kv_empty = bars + 3;   // [2]
     uint64_t* s_full = bars + 5;
@@ -192,41 +276,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* o_full = bars + 8;
     uint64_t* oc_empty = bars + 9;
     uint32_t* tmem_holder = (uint32_t*)(bars + 10);
-    constexpr uint32_t TMEM_COLS = DECODE ? 256 : 512;
+    constexpr uint32_t TMEM_COLS = 256;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
-    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
     const int g = blockIdx.y, b = blockIdx.z;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int base = a.pos_dev ? *a.pos_dev : a.start_pos;
-    int t0 = 0, c_begin = 0, c_end = 0, kv_last = 0;
-    if constexpr (DECODE) {
-        if (base < 0 || base >= a.max_pos) {
-            if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0 && b == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
-            return;
-        }
-        kv_last = base;
-        const int n_total = base / kAttnChunk + 1;
-        c_begin = blockIdx.x * a.chunks_per_cta;
-        c_end = min(c_begin + a.chunks_per_cta, n_total);
-        if (c_begin >= c_end) return;
-    } else {
-        t0 = (gridDim.x - 1 - blockIdx.x) * a.tq;   // longest tiles first
-        const int t_last = min(t0 + a.tq, a.tokens) - 1;
-        if (base < 0 || base + t_last >= a.max_pos) {
-            if (threadIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
-            return;
-        }
-        kv_last = base + t_last;
-        c_end = kv_last / kAttnChunk + 1;
+    if (base < 0 || base >= a.max_pos) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0 && b == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
+        return;
     }
+    const int kv_last = base;
+    const int n_total = base / kAttnChunk + 1;
+    const int c_begin = blockIdx.x * a.chunks_per_cta;
+    const int c_end = min(c_begin + a.chunks_per_cta, n_total);
+    if (c_begin >= c_end) return;
     const int n_iter = c_end - c_begin;
     int* err = a.err;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(q_full, 1);
         for (int i = 0; i < 2; ++i) { ptx::mbar_init(&kv_full[i], 1); ptx::mbar_init(&kv_empty[i], 1); }
         ptx::mbar_init(s_full, 1);
         ptx::mbar_init(s_empty, 4);
@@ -239,49 +309,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(tmem_holder, TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    if constexpr (DECODE) {
-        // decode query tile: rows 0..n_rep-1 = the group's heads, the rest zero
-        if (warp >= 2) {
-            const int r = threadIdx.x - 64;
-            for (int half = 0; half < 2; ++half) {
-                uint8_t* sub = sm + OFF_Q + half * kSub;
-                for (int c = 0; c < 8; ++c) {
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (r < n_rep)
-                        v = *reinterpret_cast<const uint4*>(a.q + (size_t)b * a.n_heads * 128 +
-                                                            (size_t)(g * n_rep + r) * 128 + half * 64 + c * 8);
-                    *reinterpret_cast<uint4*>(sub + sw_off(r, c)) = v;
-                }
+    // query tile: rows 0..n_rep-1 = the group's heads, the rest zero
+    if (warp >= 2) {
+        const int r = threadIdx.x - 64;
+        for (int half = 0; half < 2; ++half) {
+            uint8_t* sub = sm + OFF_Q + half * kSub;
+            for (int c = 0; c < 8; ++c) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (r < n_rep)
+                    v = *reinterpret_cast<const uint4*>(a.q + (size_t)b * a.n_heads * 128 +
+                                                        (size_t)(g * n_rep + r) * 128 + half * 64 + c * 8);
+                *reinterpret_cast<uint4*>(sub + sw_off(r, c)) = v;
             }
-            ptx::fence_proxy_async_smem();
         }
+        ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // dependents start only once this CTA holds its tensor memory (one that started
+    // earlier on this SM could take the columns and then wait for this grid)
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             ptx::prefetch_tmap(&mK);
             ptx::prefetch_tmap(&mV);
-            if constexpr (!DECODE) {
-                ptx::prefetch_tmap(&mQ);
-                ptx::mbar_arrive_expect_tx(q_full, 2 * kSub);
-                asm volatile(
-                    "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                    " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(ptx::smem_u32(sm + OFF_Q)),
-                    "l"(reinterpret_cast<uint64_t>(&mQ)), "r"(ptx::smem_u32(q_full)), "r"(0), "r"(g * n_rep),
-                    "r"(b * a.tokens + t0)
-                    : "memory");
-                asm volatile(
-                    "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                    " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(ptx::smem_u32(sm + OFF_Q + kSub)),
-                    "l"(reinterpret_cast<uint64_t>(&mQ)), "r"(ptx::smem_u32(q_full)), "r"(64), "r"(g * n_rep),
-                    "r"(b * a.tokens + t0)
-                    : "memory");
-            }
             const int head_row0 = (b * a.n_kv_heads + g) * a.kv_seq;
             for (int i = 0; i < n_iter; ++i) {
                 const int st = i & 1;
@@ -298,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool ok = DECODE ? true : ptx::mbar_wait(q_full, 0, err);
+            bool ok = true;
             const uint32_t q_addr = ptx::smem_u32(sm + OFF_Q);
             const uint32_t p_addr = ptx::smem_u32(sm + OFF_P);
             for (int i = 0; i < n_iter && ok; ++i) {
@@ -329,21 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------------ softmax + fold, thread = row
+        // ------------------------------------------------------------------ softmax + partial store, thread = row
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        const int t_local = row / n_rep, h_local = row - t_local * n_rep;
-        bool valid;
-        int pos_r;
-        if constexpr (DECODE) {
-            valid = row < n_rep;
-            pos_r = base;
-        } else {
-            valid = (t_local < a.tq) && (t0 + t_local < a.tokens);
-            pos_r = base + t0 + t_local;
-        }
-        float M = -INFINITY, L = 0.f;
+        const bool valid = row < n_rep;
+        const int pos_r = base;
         bool ok = true;
         for (int i = 0; i < n_iter; ++i) {
             const int c = c_begin + i;
@@ -372,80 +418,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok) ok = ptx::mbar_wait(o_full, i & 1, err);
             ptx::tc_fence_after();
-            if constexpr (DECODE) {
-                float* dst = a.partial + ((((size_t)b * a.n_kv_heads + g) * a.n_chunks + c) * n_rep + row) * kPartStride;
+            float* dst = a.partial + ((((size_t)b * a.n_kv_heads + g) * a.n_chunks + c) * n_rep + row) * kPartStride;
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    float ov[32];
-                    ptx::tmem_ld<32>(tmem + lane_addr + TM_OC + cb * 32, ov);
-                    ptx::tmem_wait_ld();
-                    if (valid)
+            for (int cb = 0; cb < 4; ++cb) {
+                float ov[32];
+                ptx::tmem_ld<32>(tmem + lane_addr + TM_OC + cb * 32, ov);
+                ptx::tmem_wait_ld();
+                if (valid)
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            *reinterpret_cast<float4*>(dst + cb * 32 + 4 * q4) =
-                                make_float4(ov[4 * q4], ov[4 * q4 + 1], ov[4 * q4 + 2], ov[4 * q4 + 3]);
-                }
-                if (valid) {
-                    dst[128] = m;
-                    dst[129] = l;
-                }
-            } else {
-                // fold the chunk into the running state (the combine kernel's formula)
-                float alpha = 1.f, beta = 0.f;
-                const bool first = (i == 0);
-                if (!first) {
-                    const float Mn = fmaxf(M, m);
-                    alpha = exp2f(__fsub_rn(M, Mn));
-                    beta = exp2f(__fsub_rn(m, Mn));
-                    L = __fmaf_rn(L, alpha, __fmul_rn(l, beta));
-                    M = Mn;
-                } else {
-                    M = m;
-                    L = l;
-                }
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    float oc[32], orun[32];
-                    ptx::tmem_ld<32>(tmem + lane_addr + TM_OC + cb * 32, oc);
-                    if (!first) ptx::tmem_ld<32>(tmem + lane_addr + TM_O + cb * 32, orun);
-                    ptx::tmem_wait_ld();
-                    if (first) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) orun[j] = oc[j];
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) orun[j] = __fmaf_rn(orun[j], alpha, __fmul_rn(oc[j], beta));
-                    }
-                    ptx::tmem_st32(tmem + lane_addr + TM_O + cb * 32, orun);
-                }
-                ptx::tmem_wait_st();
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        *reinterpret_cast<float4*>(dst + cb * 32 + 4 * q4) =
+                            make_float4(ov[4 * q4], ov[4 * q4 + 1], ov[4 * q4 + 2], ov[4 * q4 + 3]);
+            }
+            if (valid) {
+                dst[128] = m;
+                dst[129] = l;
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(oc_empty);
-        }
-        if constexpr (!DECODE) {
-            // o = O / L, rounded to bf16
-            ptx::tc_fence_after();
-            bf16* dst = a.o + ((size_t)b * a.tokens + t0 + t_local) * a.n_heads * 128 + (size_t)(g * n_rep + h_local) * 128;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                float ov[32];
-                ptx::tmem_ld<32>(tmem + lane_addr + TM_O + cb * 32, ov);
-                ptx::tmem_wait_ld();
-                if (valid && ok) {
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(__fdiv_rn(ov[j], L), __fdiv_rn(ov[j + 1], L));
-                        packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
-                    }
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        *reinterpret_cast<uint4*>(dst + cb * 32 + 8 * q4) =
-                            make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
-                }
-            }
         }
     }
 
@@ -453,6 +444,308 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------------------- prefill
+// Pipelined prefill attention.  Same unit (one 128-row query tile of a KV group,
+// its chunks in ascending order) and the same arithmetic as above, split over
+// roles that overlap:
+//   warp 0       TMA: the Q tile once, then K chunks through a two-stage ring
+//   warp 2       TMA: V chunks through a two-stage ring (K(i+2) loads once S(i)
+//                has read K(i); V(i+2) once PV(i) has read V(i))
+//   warp 1       TMEM owner + MMA: PV(i) into O_c[i % 2], then S(i+2) = Q K^T
+//                into the S buffer that chunk i used (S and O_c are both
+//                double-buffered in TMEM)
+//   warps 4-7    softmax of the even chunks, warps 8-11 of the odd chunks
+//                (thread = row); P goes to one of two smem tiles, the row's
+//                (m, l) to the first two columns of the S buffer it read
+//   warps 12-15  fold of every chunk into the running (O, M, L), thread = row,
+//                with the row's O in registers; then o = O * (1 / L)
+// Warp 3 only keeps the roles aligned to warpgroups.  A chunk that is wholly
+// in a row's future (all its keys hidden) is skipped by that row's fold, so the
+// row folds exactly chunks 0 .. pos / 128 -- the chunks a decode step at the
+// same position folds.
+constexpr int kPfThreads = 512;
+// register split (launch: 128 per thread): warpgroup 0 and the softmax give up
+// registers so that each fold thread can hold its row of O (128 floats)
+constexpr int kPfRegsCtrl = 56;
+constexpr int kPfRegsSoftmax = 104;
+constexpr int kPfRegsFold = 232;
+constexpr int kPfRegsNeeded = 128 * kPfRegsCtrl + 256 * kPfRegsSoftmax + 128 * kPfRegsFold;
+static_assert(kPfRegsNeeded <= 128 * kPfThreads, "register split exceeds the launch allocation");
+constexpr int PF_OFF_Q = 0;                          // Q: 2 sub-tiles
+constexpr int PF_OFF_K = 2 * kSub;                   // [stage] K: 2 sub-tiles
+constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
+constexpr int PF_OFF_P = PF_OFF_V + 4 * kSub;        // [parity] P: 2 sub-tiles
+constexpr int PF_OFF_BAR = PF_OFF_P + 4 * kSub;
+constexpr int PF_SMEM_BYTES = PF_OFF_BAR + 256 + 1024;
+constexpr int PF_TM_S = 0, PF_TM_OC = 256;   // S[parity] at 0 / 128, O_c[parity] at 256 / 384
+static_assert(PF_SMEM_BYTES <= 232448, "shared memory per CTA");
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    k_attn_pf(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+              const __grid_constant__ CUtensorMap mV, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = (uint64_t*)(sm + PF_OFF_BAR);
+    uint64_t* q_full = bars + 0;
+    uint64_t* k_full = bars + 1;     // [2] TMA -> MMA
+    uint64_t* k_empty = bars + 3;    // [2] MMA (after S) -> TMA
+    uint64_t* v_full = bars + 5;     // [2] TMA -> MMA (and the softmax, before it zeroes rows)
+    uint64_t* v_empty = bars + 7;    // [2] MMA (after PV) -> TMA
+    uint64_t* s_full = bars + 9;     // [2] MMA (after S) -> softmax
+    uint64_t* p_full = bars + 11;    // [2] softmax (P, m, l written) -> MMA, fold
+    uint64_t* s_free = bars + 13;    // [2] fold (m, l read) -> MMA
+    uint64_t* oc_full = bars + 15;   // [2] MMA (after PV) -> fold
+    uint64_t* oc_free = bars + 17;   // [2] fold (O_c read) -> MMA
+    uint32_t* tmem_holder = (uint32_t*)(bars + 19);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_wait();   // q and the cache rows come from the projection kernels
+
+    const int g = blockIdx.y, b = blockIdx.z;
+    const int n_rep = a.n_heads / a.n_kv_heads;
+    const int base = a.pos_dev ? *a.pos_dev : a.start_pos;
+    const int t0 = (gridDim.x - 1 - blockIdx.x) * a.tq;   // longest tiles first
+    const int t_last = min(t0 + a.tq, a.tokens) - 1;
+    if (base < 0 || base + t_last >= a.max_pos) {
+        if (threadIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
+        return;
+    }
+    const int kv_last = base + t_last;
+    const int n_iter = kv_last / kAttnChunk + 1;
+    int* err = a.err;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&k_full[i], 1);
+            ptx::mbar_init(&k_empty[i], 1);
+            ptx::mbar_init(&v_full[i], 1);
+            ptx::mbar_init(&v_empty[i], 1);
+            ptx::mbar_init(&s_full[i], 1);
+            ptx::mbar_init(&p_full[i], 4);
+            ptx::mbar_init(&s_free[i], 4);
+            ptx::mbar_init(&oc_full[i], 1);
+            ptx::mbar_init(&oc_free[i], 4);
+        }
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_holder, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    // dependents start only once this CTA holds its tensor memory (one that started
+    // earlier on this SM could take the columns and then wait for this grid)
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
+
+    if (warp < 4) {
+        ptx::setmaxnreg_dec<kPfRegsCtrl>();
+        if (warp == 0 || warp == 2) {
+            // ------------------------------------------------------------------ TMA producers
+            if (lane == 0) {
+                const bool is_k = (warp == 0);
+                const CUtensorMap* map = is_k ? &mK : &mV;
+                uint64_t* full = is_k ? k_full : v_full;
+                uint64_t* empty = is_k ? k_empty : v_empty;
+                uint8_t* ring = sm + (is_k ? PF_OFF_K : PF_OFF_V);
+                ptx::prefetch_tmap(map);
+                if (is_k) {
+                    ptx::prefetch_tmap(&mQ);
+                    ptx::mbar_arrive_expect_tx(q_full, 2 * kSub);
+                    for (int half = 0; half < 2; ++half)
+                        asm volatile(
+                            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(ptx::smem_u32(sm + PF_OFF_Q + half * kSub)),
+                            "l"(reinterpret_cast<uint64_t>(&mQ)), "r"(ptx::smem_u32(q_full)), "r"(half * 64),
+                            "r"(g * n_rep), "r"(b * a.tokens + t0)
+                            : "memory");
+                }
+                const int head_row0 = (b * a.n_kv_heads + g) * a.kv_seq;
+                int issued = 0;
+                for (int i = 0; i < n_iter; ++i, ++issued) {
+                    const int st = i & 1;
+                    if (i >= 2 && !ptx::mbar_wait(&empty[st], ((i >> 1) & 1) ^ 1, err)) break;
+                    uint8_t* dst = ring + st * 2 * kSub;
+                    const int row = head_row0 + i * kAttnChunk;
+                    ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
+                    ptx::tma_load_2d(dst, map, &full[st], 0, row);
+                    ptx::tma_load_2d(dst + kSub, map, &full[st], 64, row);
+                }
+                // no copy may still be landing when the CTA exits (it has landed already
+                // unless a wait above gave up)
+                if (is_k) ptx::mbar_wait_drain(q_full, 0);
+                for (int i = max(0, issued - 2); i < issued; ++i) ptx::mbar_wait_drain(&full[i & 1], (i >> 1) & 1);
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                const uint32_t q_addr = ptx::smem_u32(sm + PF_OFF_Q);
+                auto issue_s = [&](int i) -> bool {
+                    const int k = i & 1;
+                    if (!ptx::mbar_wait(&k_full[k], (i >> 1) & 1, err)) return false;
+                    if (i >= 2 && !ptx::mbar_wait(&s_free[k], ((i >> 1) & 1) ^ 1, err)) return false;
+                    ptx::tc_fence_after();
+                    const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
+                        ptx::umma_bf16(tmem + PF_TM_S + k * 128, ptx::sw128_kmajor_desc(q_addr + off),
+                                       ptx::sw128_kmajor_desc(k_addr + off), IDESC_S, ks > 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(&s_full[k]);
+                    ptx::umma_commit(&k_empty[k]);
+                    return true;
+                };
+                bool ok = ptx::mbar_wait(q_full, 0, err);
+                if (ok) ok = issue_s(0);
+                if (ok && n_iter > 1) ok = issue_s(1);
+                for (int i = 0; i < n_iter && ok; ++i) {
+                    const int k = i & 1;
+                    if (!ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err)) break;
+                    if (i >= 2 && !ptx::mbar_wait(&oc_free[k], ((i >> 1) & 1) ^ 1, err)) break;
+                    if (!ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err)) break;
+                    ptx::tc_fence_after();
+                    const uint32_t p_addr = ptx::smem_u32(sm + PF_OFF_P + k * 2 * kSub);
+                    const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + k * 2 * kSub);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t aoff = (ks >> 2) * kSub + (ks & 3) * 32;
+                        ptx::umma_bf16(tmem + PF_TM_OC + k * 128, ptx::sw128_kmajor_desc(p_addr + aoff),
+                                       ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(&oc_full[k]);
+                    ptx::umma_commit(&v_empty[k]);
+                    if (i + 2 < n_iter) ok = issue_s(i + 2);
+                }
+            }
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------------------------ softmax, thread = row
+        ptx::setmaxnreg_dec<kPfRegsSoftmax>();
+        const int k = (warp - 4) >> 2;   // chunk parity of this warpgroup
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const int t_local = row / n_rep;
+        const bool valid = (t_local < a.tq) && (t0 + t_local < a.tokens);
+        const int pos_r = base + t0 + t_local;
+        const uint32_t s_addr = tmem + lane_addr + PF_TM_S + k * 128;
+        uint8_t* p_base = sm + PF_OFF_P + k * 2 * kSub;
+        bool ok = true;
+        for (int i = k; i < n_iter; i += 2) {
+            // s_full(i) also means PV(i - 2) -- issued before S(i) -- is done with P[k]
+            if (ok) ok = ptx::mbar_wait(&s_full[k], (i >> 1) & 1, err);
+            ptx::tc_fence_after();
+            const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
+            float m, l;
+            softmax_row_regs(s_addr, jmax, a.scale_log2, p_base, kSub, row, m, l);
+            ptx::tmem_st2(s_addr, m, l);
+            ptx::tmem_wait_st();
+            // value rows past the last visible key of this tile are zeroed (they may hold
+            // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
+            // the chunk's V has landed
+            if (i * kAttnChunk + kAttnChunk - 1 > kv_last && ok) ok = ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err);
+            if (i * kAttnChunk + row > kv_last) {
+                uint8_t* vrow = sm + PF_OFF_V + k * 2 * kSub + row * 128;
+#pragma unroll
+                for (int c16 = 0; c16 < 8; ++c16) {
+                    *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(vrow + kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p_full[k]);
+        }
+    } else {
+        // ------------------------------------------------------------------ fold + output
+        ptx::setmaxnreg_inc<kPfRegsFold>();
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const int t_local = row / n_rep, h_local = row - t_local * n_rep;
+        const bool valid = (t_local < a.tq) && (t0 + t_local < a.tokens);
+        float O[128];
+        float M = -INFINITY, L = 0.f;
+        bool started = false, ok = true;
+#pragma unroll 1
+        for (int i = 0; i < n_iter; ++i) {
+            const int k = i & 1;
+            if (ok) ok = ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err);
+            ptx::tc_fence_after();
+            float ml[2];
+            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + k * 128, ml);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s_free[k]);
+            const float m = ml[0], l = ml[1];
+            if (ok) ok = ptx::mbar_wait(&oc_full[k], (i >> 1) & 1, err);
+            ptx::tc_fence_after();
+            // Per row: skip a chunk with no visible key, start from the first one, fold the
+            // rest (the combine kernel's formula).  The TMEM loads are issued by the whole
+            // warp whatever each row does (they are warp-collective).
+            const bool use = (m != -INFINITY);
+            const bool fold = use && started;
+            float alpha = 1.f, beta = 0.f;
+            if (fold) {
+                const float Mn = fmaxf(M, m);
+                alpha = exp2f(__fsub_rn(M, Mn));
+                beta = exp2f(__fsub_rn(m, Mn));
+                L = __fmaf_rn(L, alpha, __fmul_rn(l, beta));
+                M = Mn;
+            } else if (use) {
+                M = m;
+                L = l;
+            }
+            const uint32_t oc_addr = tmem + lane_addr + PF_TM_OC + k * 128;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                float oc[32];
+                ptx::tmem_ld<32>(oc_addr + cb * 32, oc);
+                ptx::tmem_wait_ld();
+                if (cb == 3) {   // O_c[k] fully read: PV(i + 2) may overwrite it
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&oc_free[k]);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float& o = O[cb * 32 + j];
+                    o = fold ? __fmaf_rn(o, alpha, __fmul_rn(oc[j], beta)) : (use ? oc[j] : o);
+                }
+            }
+            started = started || use;
+        }
+        // o = O * (1 / L), rounded to bf16
+        if (valid && ok && started) {
+            const float inv_l = __frcp_rn(L);
+            bf16* dst = a.o + ((size_t)b * a.tokens + t0 + t_local) * a.n_heads * 128 + (size_t)(g * n_rep + h_local) * 128;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; ++c8) {
+                uint32_t packed[4];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    const __nv_bfloat162 v2 =
+                        __floats2bfloat162_rn(__fmul_rn(O[c8 * 8 + j], inv_l), __fmul_rn(O[c8 * 8 + j + 1], inv_l));
+                    packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
+                }
+                *reinterpret_cast<uint4*>(dst + c8 * 8) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
     }
 }
 
@@ -746,15 +1039,19 @@ cudaError_t launch_attention_tc_prefill(const AttnArgs& a, cudaStream_t s) {
     if (!make_tmap_bf16(&mk, a.kc, cache_rows, 128, 128, nullptr) ||
         !make_tmap_bf16(&mv, a.vc, cache_rows, 128, 128, nullptr))
         return cudaErrorInvalidValue;
-    auto kern = k_attn_tc<false>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        // the register split inside the kernel must fit the block's launch allocation
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaFuncGetAttributes(&fa, k_attn_pf);
+        if (r != cudaSuccess) return r;
+        if (fa.numRegs * kPfThreads < kPfRegsNeeded) return cudaErrorInvalidConfiguration;
+        r = cudaFuncSetAttribute(k_attn_pf, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES);
         if (r != cudaSuccess) return r;
         attr = true;
     }
     dim3 grid((a.tokens + k.tq - 1) / k.tq, a.n_kv_heads, a.batch);
-    return launch_pdl(kern, grid, dim3(kThreads), SMEM_BYTES, s, mq, mk, mv, k);
+    return launch_pdl(k_attn_pf, grid, dim3(kPfThreads), PF_SMEM_BYTES, s, mq, mk, mv, k);
 }
 
 cudaError_t launch_attention_tc_decode(const AttnArgs& a, int chunks_per_cta, cudaStream_t s) {
@@ -785,7 +1082,7 @@ cudaError_t launch_attention_tc_decode(const AttnArgs& a, int chunks_per_cta, cu
     }
     if (chunks_per_cta <= 0) chunks_per_cta = 2;
     k.chunks_per_cta = chunks_per_cta;
-    auto kern = k_attn_tc<true>;
+    auto kern = k_attn_tc_wide;
     static bool attr = false;
     if (!attr) {
         cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -793,7 +1090,7 @@ cudaError_t launch_attention_tc_decode(const AttnArgs& a, int chunks_per_cta, cu
         attr = true;
     }
     dim3 grid((a.n_chunks + chunks_per_cta - 1) / chunks_per_cta, a.n_kv_heads, a.batch);
-    cudaError_t r = launch_pdl(kern, grid, dim3(kThreads), SMEM_BYTES, s, mk, mk, mv, k);
+    cudaError_t r = launch_pdl(kern, grid, dim3(kThreads), SMEM_BYTES, s, mk, mv, k);
     if (r != cudaSuccess) return r;
     return launch_attention_combine(a, s);
 }

@@ -83,7 +83,10 @@ __device__ __forceinline__ float rms_tree_256(float ss, float* red) {
 // wait: so when a kernel starts, the kernel two places earlier and everything
 // before it have completed, and only the immediately preceding kernel may still
 // be running.  Reading data that predecessor did not write before the wait
-// (weights, older KV-cache rows) is therefore safe.
+// (weights, older KV-cache rows) is therefore safe.  A kernel that allocates
+// tensor memory also triggers only after its allocation: a dependent CTA that
+// started earlier on the same SM could otherwise hold the columns while it
+// waits for this grid.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args&&... args) {

@@ -73,7 +73,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait.  Returns false (and sets *err) when the budget runs out or when
-// another thread of the grid already reported an error.
+// another thread of the grid already reported an error.  The error word is read
+// only once a wait has lasted kErrPollNs: every waiting warp of every CTA polling
+// one global address would keep that address's L2 slice busy and slow all the
+// loads that go through it.
+constexpr uint64_t kErrPollNs = 200000ull;   // 200 us
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -81,8 +85,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((++spins & 63u) == 0) {
-            if (*((volatile int*)err) != 0) return false;
-            if (globaltimer() - t0 > kWaitBudgetNs) {
+            const uint64_t dt = globaltimer() - t0;
+            if (dt > kErrPollNs && (spins & 4095u) == 0 && *((volatile int*)err) != 0) return false;
+            if (dt > kWaitBudgetNs) {
                 atomicCAS(err, 0, -6 /* LLAMA_ERR_DEVICE_TIMEOUT */);
                 return false;
             }
@@ -173,6 +178,13 @@ template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float* out);
 
 template <>
+__device__ __forceinline__ void tmem_ld<2>(uint32_t taddr, float* o) {
+    uint32_t r0, r1;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(taddr));
+    o[0] = __uint_as_float(r0);
+    o[1] = __uint_as_float(r1);
+}
+template <>
 __device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float* o) {
     uint32_t r[8];
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -208,6 +220,22 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float* o) {
 }
 
 // tcgen05.st: 32 lanes x 32 bits, 32 consecutive columns per thread.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, float a, float b) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(__float_as_uint(a)),
+                 "r"(__float_as_uint(b))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::
+                     "r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+                 "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+                 "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+                 "r"(__float_as_uint(v[15]))
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"

@@ -13,6 +13,10 @@ from tests.blockrun import (BF16_TOL, F32_TOL, check_bf16_output, gpu_block, ora
 pytestmark = pytest.mark.gpu
 
 MID = workloads.BlockDims(d_model=2048, n_heads=16, n_kv_heads=4, head_dim=128, d_ff=4096)
+# 16 query heads per KV head (the wide-group decode kernel, 8-token prefill tiles)
+WIDE = workloads.BlockDims(d_model=2048, n_heads=16, n_kv_heads=1, head_dim=128, d_ff=4096)
+# one query head per KV head (128-token prefill tiles)
+MHA = workloads.BlockDims(d_model=1024, n_heads=8, n_kv_heads=8, head_dim=128, d_ff=2048)
 
 
 def _oracle_prefill(inp, T_total, max_seq, trace=None):
@@ -74,12 +78,15 @@ def test_tiny_fp32_decode_bit_identical_to_prefill():
     assert torch.equal(kc[:, :, :n], kc_mix[:, :, :n]) and torch.equal(vc[:, :, :n], vc_mix[:, :, :n])
 
 
-@pytest.mark.parametrize("B,T,steps", [(2, 300, 3), (1, 129, 2), (3, 17, 2)])
-def test_bf16_mid_block_parity(B, T, steps):
+@pytest.mark.parametrize("dims,B,T,steps", [(MID, 2, 300, 3), (MID, 1, 129, 2), (MID, 3, 17, 2), (WIDE, 2, 200, 3),
+                                             (MHA, 2, 260, 2)], ids=["mid-2x300", "mid-1x129", "mid-3x17",
+                                                                     "wide-2x200", "mha-2x260"])
+def test_bf16_mid_block_parity(dims, B, T, steps):
     """bf16, 128-wide heads, d=2048 (2 K-segments) and d_ff=4096 (4 K-segments):
-    token-tiled prefill (ragged token tiles) and weight-streaming decode."""
+    token-tiled prefill (ragged token tiles) and weight-streaming decode; GQA
+    groups of 4, 16 and 1 query heads per KV head."""
     max_seq = T + steps + 5
-    inp = workloads.make_block_inputs(MID, B, T + steps, max_seq=max_seq, random_gains=True)
+    inp = workloads.make_block_inputs(dims, B, T + steps, max_seq=max_seq, random_gains=True)
     y_gpu, kc, vc, _, _ = _prefill_then_decode(inp, T, steps, max_seq)
     tr = {}
     _oracle_prefill(inp, T + steps, max_seq, trace=tr)
@@ -91,12 +98,13 @@ def test_bf16_mid_block_parity(B, T, steps):
     assert torch.isnan(kc[:, :, n:]).all() and torch.isnan(vc[:, :, n:]).all()
 
 
-@pytest.mark.parametrize("B,T,steps", [(2, 300, 3), (1, 64, 2)])
-def test_bf16_decode_bit_identical_to_prefill(B, T, steps):
+@pytest.mark.parametrize("dims,B,T,steps", [(MID, 2, 300, 3), (MID, 1, 64, 2), (WIDE, 1, 250, 3), (MHA, 2, 130, 2)],
+                         ids=["mid-2x300", "mid-1x64", "wide-1x250", "mha-2x130"])
+def test_bf16_decode_bit_identical_to_prefill(dims, B, T, steps):
     """Decode rows (weight-streaming projections, split-KV attention) equal the
     prefill rows (token-tiled projections, in-CTA attention fold) bit for bit."""
     max_seq = T + steps + 5
-    inp = workloads.make_block_inputs(MID, B, T + steps, max_seq=max_seq)
+    inp = workloads.make_block_inputs(dims, B, T + steps, max_seq=max_seq)
     y_mix, kc_mix, vc_mix, blk, ddb = _prefill_then_decode(inp, T, steps, max_seq)
     dev = torch.device("cuda:0")
     kc = inp.k_cache.to(dev)
