@@ -214,48 +214,6 @@ __device__ __forceinline__ void softmax_row(uint32_t s_taddr, int jmax, float sc
     l_out = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), lq[2]), lq[3]);
 }
 
-// Four-lanes-per-row form (decode): rows 0..7 of the chunk, lane L works on row
-// L / 4, keys 32 (L % 4) .. +31.  srow: this warp's 8 x 128 fp32 staging area.
-// Every lane returns its row's m and l.
-__device__ __forceinline__ void softmax_rows8(uint32_t s_taddr, float* srow, int jmax_of_row, float scale_log2,
-                                              uint8_t* p_base, uint32_t p_sub_stride, float& m_out, float& l_out) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-        float sv[32];
-        ptx::tmem_ld<32>(s_taddr + cb * 32, sv);
-        ptx::tmem_wait_ld();
-        if (lane < 8)
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                *reinterpret_cast<float4*>(srow + lane * 128 + cb * 32 + 4 * q4) =
-                    make_float4(sv[4 * q4], sv[4 * q4 + 1], sv[4 * q4 + 2], sv[4 * q4 + 3]);
-    }
-    __syncwarp();
-    const int r = lane >> 2, q = lane & 3;
-    float sv[32];
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-        const float4 v = *reinterpret_cast<const float4*>(srow + r * 128 + q * 32 + 4 * q4);
-        sv[4 * q4] = v.x; sv[4 * q4 + 1] = v.y; sv[4 * q4 + 2] = v.z; sv[4 * q4 + 3] = v.w;
-    }
-    const int jmax = __shfl_sync(0xffffffffu, jmax_of_row, r);
-    float m = quarter_max_raw(sv, q * 32, jmax);
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m = __fmul_rn(m, scale_log2);
-    uint32_t packed[16];
-    float lq;
-    softmax_quarter(sv, q * 32, jmax, scale_log2, m, packed, lq);
-    store_p_quarter(p_base, p_sub_stride, r, q, packed);
-    const float l0 = __shfl_sync(0xffffffffu, lq, r * 4), l1 = __shfl_sync(0xffffffffu, lq, r * 4 + 1);
-    const float l2 = __shfl_sync(0xffffffffu, lq, r * 4 + 2), l3 = __shfl_sync(0xffffffffu, lq, r * 4 + 3);
-    const float l = __fadd_rn(__fadd_rn(__fadd_rn(l0, l1), l2), l3);
-    // hand row r's (m, l) back to lane r
-    m_out = __shfl_sync(0xffffffffu, m, (lane & 7) * 4);
-    l_out = __shfl_sync(0xffffffffu, l, (lane & 7) * 4);
-    __syncwarp();
-}
 
 // Decode attention for groups of more than 8 query heads per KV head (a query
 // tile holds the group's heads, the other rows are zero).  The chunks of one
@@ -753,20 +711,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // Persistent decode attention for groups of n_rep <= 8 query heads.  The work
 // units are (sequence, KV head, chunk); CTA i walks a contiguous range of them.
 // Query and P tiles hold 8 rows; their descriptors use an 8-row-group stride of
-// 0, so the MMA's 128 rows alias those 8 (rows 8..127 repeat rows 0..7 and are
-// ignored).  Two TMEM slots (S and O_c of one unit share a slot's 128 columns)
-// and two softmax warps take alternate units; the MMA thread issues S of unit
-// i+1 before PV of unit i, so the tensor core works while a softmax runs; K/V
-// stream through a three-stage TMA ring.  Warps: 0 and 4 = softmax + partial
-// store for slots 0 and 1 (rows 0..7 are TMEM lanes 0..7, which warps 0 and 4
-// may read), 1 = TMA producer, 2 = TMEM owner + MMA issuer, 3 idle.
-constexpr int kDecThreads = 160;
+// 0, so the MMA's 128 rows repeat rows 0..7: TMEM lane 8g + r holds row r for
+// every g, and all 32 lanes of a warp's lane quarter see the 8 rows.  A softmax
+// warp therefore works on (row r = lane % 8, key quarter g = lane / 8) straight
+// from TMEM.  Three TMEM slots (S and then O_c of one unit share a slot's 128
+// columns) and three softmax warps take units in turn; the MMA thread issues
+// S of unit i before PV of unit i-1.  K and V stream through separate
+// three-stage TMA rings, so K of unit i+3 loads as soon as S(i) has read K(i).
+// Warps: 0..2 = softmax + partial store of slots 0..2, 3 = K producer,
+// 4 = TMEM owner + MMA issuer, 5 = V producer.
+constexpr int kDecSlots = 3;
+constexpr int kDecThreads = 32 * (kDecSlots + 3);
 constexpr int kDecStages = 3;
 constexpr int D_OFF_Q = 0;                              // [slot][half] 1 KB each
-constexpr int D_OFF_P = 4096;                           // [slot][half] 1 KB each
-constexpr int D_OFF_S = 8192;                           // [slot] 8 x 128 fp32 score staging
-constexpr int D_OFF_KV = 16384;                         // [stage] K: 2 sub-tiles, V: 2 sub-tiles
-constexpr int D_OFF_BAR = D_OFF_KV + kDecStages * 4 * kSub;
+constexpr int D_OFF_P = 8192;                           // [slot][half] 1 KB each
+constexpr int D_OFF_K = 16384;                          // [stage] K: 2 sub-tiles
+constexpr int D_OFF_V = D_OFF_K + kDecStages * 2 * kSub;   // [stage] V: 2 sub-tiles
+constexpr int D_OFF_BAR = D_OFF_V + kDecStages * 2 * kSub;
 constexpr int D_SMEM_BYTES = D_OFF_BAR + 256 + 1024;
 
 __device__ __forceinline__ uint64_t sw128_kmajor_desc_rows8(uint32_t smem_addr) {
@@ -785,19 +746,33 @@ __device__ __forceinline__ DecUnit dec_unit(int u, int n_total, int n_kv) {
     return d;
 }
 
+// The 128 columns at taddr, each lane keeping the 32 of its key quarter q.
+__device__ __forceinline__ void tmem_ld_quarter(uint32_t taddr, int q, float (&out)[32]) {
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        float v[32];
+        ptx::tmem_ld<32>(taddr + cb * 32, v);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) out[j] = (cb == q) ? v[j] : out[j];
+    }
+}
+
 __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_constant__ CUtensorMap mK,
                                                                 const __grid_constant__ CUtensorMap mV,
                                                                 const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + D_OFF_BAR);
-    uint64_t* kv_full = bars + 0;             // [3]
-    uint64_t* kv_empty = bars + 3;            // [3]
-    uint64_t* slot_ready = bars + 6;          // [2] query tile filled, previous unit of the slot drained
-    uint64_t* s_full = bars + 8;              // [2]
-    uint64_t* p_full = bars + 10;             // [2]
-    uint64_t* o_full = bars + 12;             // [2]
-    uint32_t* tmem_holder = (uint32_t*)(bars + 14);
+    uint64_t* k_full = bars + 0;                         // [stages]
+    uint64_t* k_empty = bars + kDecStages;               // [stages] S of the unit done
+    uint64_t* v_full = bars + 2 * kDecStages;            // [stages]
+    uint64_t* v_empty = bars + 3 * kDecStages;           // [stages] PV of the unit done
+    uint64_t* slot_ready = bars + 4 * kDecStages;        // [slots] query tile filled, slot's O_c read
+    uint64_t* s_full = slot_ready + kDecSlots;           // [slots]
+    uint64_t* p_full = s_full + kDecSlots;               // [slots]
+    uint64_t* o_full = p_full + kDecSlots;               // [slots]
+    uint32_t* tmem_holder = (uint32_t*)(o_full + kDecSlots);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // The position comes from the host side (set before the step is launched), not
@@ -818,8 +793,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
     int* err = a.err;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kDecStages; ++i) { ptx::mbar_init(&kv_full[i], 1); ptx::mbar_init(&kv_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kDecStages; ++i) {
+            ptx::mbar_init(&k_full[i], 1);
+            ptx::mbar_init(&k_empty[i], 1);
+            ptx::mbar_init(&v_full[i], 1);
+            ptx::mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < kDecSlots; ++i) {
             ptx::mbar_init(&slot_ready[i], 1);
             ptx::mbar_init(&s_full[i], 1);
             ptx::mbar_init(&p_full[i], 1);
@@ -827,8 +807,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
         }
         ptx::fence_mbar_init();
     }
-    if (warp == 2) {
-        ptx::tmem_alloc(tmem_holder, 256);
+    if (warp == kDecSlots + 1) {
+        ptx::tmem_alloc(tmem_holder, 512);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -836,112 +816,155 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 1) {
-        // ------------------------------------------------------------------ TMA producer
+    if (warp == kDecSlots || warp == kDecSlots + 2) {
+        // ------------------------------------------------------------------ TMA producers (K, V)
         if (lane == 0) {
-            ptx::prefetch_tmap(&mK);
-            ptx::prefetch_tmap(&mV);
+            const bool is_k = (warp == kDecSlots);
+            const CUtensorMap* map = is_k ? &mK : &mV;
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
+            uint8_t* ring = sm + (is_k ? D_OFF_K : D_OFF_V);
+            ptx::prefetch_tmap(map);
             bool waited = false;
-            for (int i = 0; i < n_iter; ++i) {
+            int issued = 0;
+            for (int i = 0; i < n_iter; ++i, ++issued) {
                 const int st = i % kDecStages;
-                if (i >= kDecStages && !ptx::mbar_wait(&kv_empty[st], ((i / kDecStages) - 1) & 1, err)) break;
+                if (i >= kDecStages && !ptx::mbar_wait(&empty[st], ((i / kDecStages) - 1) & 1, err)) break;
                 const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
                 if (!waited && d.c == n_total - 1) {   // this chunk holds the row the QKV step writes
                     ptx::griddep_wait();
                     waited = true;
                 }
                 const int row = (d.b * a.n_kv_heads + d.g) * a.kv_seq + d.c * kAttnChunk;
-                uint8_t* kv = sm + D_OFF_KV + st * 4 * kSub;
-                ptx::mbar_arrive_expect_tx(&kv_full[st], 4 * kSub);
-                ptx::tma_load_2d(kv, &mK, &kv_full[st], 0, row);
-                ptx::tma_load_2d(kv + kSub, &mK, &kv_full[st], 64, row);
-                ptx::tma_load_2d(kv + 2 * kSub, &mV, &kv_full[st], 0, row);
-                ptx::tma_load_2d(kv + 3 * kSub, &mV, &kv_full[st], 64, row);
+                uint8_t* dst = ring + st * 2 * kSub;
+                ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
+                ptx::tma_load_2d(dst, map, &full[st], 0, row);
+                ptx::tma_load_2d(dst + kSub, map, &full[st], 64, row);
             }
+            // no copy may still be landing when the CTA exits (it has landed already
+            // unless a wait above gave up)
+            for (int i = max(0, issued - kDecStages); i < issued; ++i)
+                ptx::mbar_wait_drain(&full[i % kDecStages], (i / kDecStages) & 1);
         }
-    } else if (warp == 2) {
+    } else if (warp == kDecSlots + 1) {
         // ------------------------------------------------------------------ MMA issuer: S(i), then PV(i-1)
         if (lane == 0) {
             auto issue_pv = [&](int j) -> bool {
-                const int slot = j & 1, st = j % kDecStages;
-                if (!ptx::mbar_wait(&p_full[slot], (j >> 1) & 1, err)) return false;
+                const int slot = j % kDecSlots, st = j % kDecStages;
+                if (!ptx::mbar_wait(&p_full[slot], (j / kDecSlots) & 1, err)) return false;
                 ptx::tc_fence_after();
                 const uint32_t p_addr = ptx::smem_u32(sm + D_OFF_P + slot * 2048);
-                const uint32_t v_addr = ptx::smem_u32(sm + D_OFF_KV + st * 4 * kSub + 2 * kSub);
+                if (!ptx::mbar_wait(&v_full[st], (j / kDecStages) & 1, err)) return false;
+                const uint32_t v_addr = ptx::smem_u32(sm + D_OFF_V + st * 2 * kSub);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     ptx::umma_bf16(tmem + slot * 128, sw128_kmajor_desc_rows8(p_addr + (ks >> 2) * 1024 + (ks & 3) * 32),
                                    ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
                 ptx::umma_commit(&o_full[slot]);
-                ptx::umma_commit(&kv_empty[st]);
+                ptx::umma_commit(&v_empty[st]);
                 return true;
             };
             bool ok = true;
             for (int i = 0; i < n_iter && ok; ++i) {
-                const int slot = i & 1, st = i % kDecStages;
-                if (!ptx::mbar_wait(&kv_full[st], (i / kDecStages) & 1, err)) { ok = false; break; }
-                if (!ptx::mbar_wait(&slot_ready[slot], (i >> 1) & 1, err)) { ok = false; break; }
+                const int slot = i % kDecSlots, st = i % kDecStages;
+                if (!ptx::mbar_wait(&k_full[st], (i / kDecStages) & 1, err)) { ok = false; break; }
+                if (!ptx::mbar_wait(&slot_ready[slot], (i / kDecSlots) & 1, err)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t q_addr = ptx::smem_u32(sm + D_OFF_Q + slot * 2048);
-                const uint32_t k_addr = ptx::smem_u32(sm + D_OFF_KV + st * 4 * kSub);
+                const uint32_t k_addr = ptx::smem_u32(sm + D_OFF_K + st * 2 * kSub);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     ptx::umma_bf16(tmem + slot * 128, sw128_kmajor_desc_rows8(q_addr + (ks >> 2) * 1024 + (ks & 3) * 32),
                                    ptx::sw128_kmajor_desc(k_addr + (ks >> 2) * kSub + (ks & 3) * 32), IDESC_S,
                                    ks > 0 ? 1u : 0u);
                 ptx::umma_commit(&s_full[slot]);
+                ptx::umma_commit(&k_empty[st]);
                 if (i > 0) ok = issue_pv(i - 1);
             }
             if (ok) issue_pv(n_iter - 1);
         }
-    } else if (warp == 0 || warp == 4) {
+    } else {
         // ------------------------------------------------------------------ softmax + partial store
-        const int slot = warp >> 2;
-        const bool valid = lane < n_rep;
-        const uint32_t taddr = tmem + slot * 128;   // TMEM lanes 0..31 (warp 0 and warp 4)
+        const int slot = warp;
+        const int r = lane & 7, q = lane >> 3;   // row, key quarter (output column quarter for O_c)
+        const bool valid = r < n_rep;
+        // this warp's lane quarter (every quarter holds the 8 rows), the slot's columns
+        const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + slot * 128;
         uint8_t* qs = sm + D_OFF_Q + slot * 2048;
         uint8_t* ps = sm + D_OFF_P + slot * 2048;
-        float* srow = reinterpret_cast<float*>(sm + D_OFF_S + slot * 4096);
         ptx::griddep_wait();   // q comes from the QKV step
         if (threadIdx.x == 0) ptx::griddep_launch_dependents();
         int q_bg = -1;         // (sequence, KV head) whose query rows the slot's tile holds
         bool ok = true;
-        for (int i = slot, k = 0; i < n_iter; i += 2, ++k) {
+        // The slot's query tile for unit i: rows 0..n_rep-1 of (b, g), zero rows up to 8;
+        // lane = row r x 16-byte column blocks 2q, 2q+1 of both halves.  fetch_q loads a
+        // unit's rows into registers early (the loads' latency hides behind the wait
+        // for PV); prepare writes them to the tile once the slot is free.
+        uint4 qreg[4];
+        int qreg_bg = -1;
+        auto fetch_q = [&](int i) {
             const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
-            const int st = i % kDecStages;
+            const int bg = d.b * a.n_kv_heads + d.g;
+            if (bg == q_bg || bg == qreg_bg) return;
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (valid)
+                        v = *reinterpret_cast<const uint4*>(a.q + (size_t)d.b * a.n_heads * 128 +
+                                                            (size_t)(d.g * n_rep + r) * 128 + half * 64 +
+                                                            (q * 2 + cc) * 8);
+                    qreg[half * 2 + cc] = v;
+                }
+            qreg_bg = bg;
+        };
+        auto prepare = [&](int i) {
+            const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
             const int bg = d.b * a.n_kv_heads + d.g;
             if (bg != q_bg) {
-                // query rows 0..n_rep-1 of (b, g), zero rows up to 8
-                if (lane < 8) {
+                fetch_q(i);
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
+                for (int half = 0; half < 2; ++half)
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint4 v = make_uint4(0, 0, 0, 0);
-                            if (valid)
-                                v = *reinterpret_cast<const uint4*>(a.q + (size_t)d.b * a.n_heads * 128 +
-                                                                    (size_t)(d.g * n_rep + lane) * 128 + half * 64 + c * 8);
-                            *reinterpret_cast<uint4*>(qs + half * 1024 + sw_off(lane, c)) = v;
-                        }
-                }
+                    for (int cc = 0; cc < 2; ++cc)
+                        *reinterpret_cast<uint4*>(qs + half * 1024 + sw_off(r, q * 2 + cc)) = qreg[half * 2 + cc];
                 q_bg = bg;
                 ptx::fence_proxy_async_smem();
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&slot_ready[slot]);
+        };
+        if (slot < n_iter) prepare(slot);
+        for (int i = slot, k = 0; i < n_iter; i += kDecSlots, ++k) {
+            const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
+            const int st = i % kDecStages;
             if (ok) ok = ptx::mbar_wait(&s_full[slot], k & 1, err);
             ptx::tc_fence_after();
-            const int jmax = valid ? min(kAttnChunk - 1, pos - d.c * kAttnChunk) : -1;
-            float m, l;
-            softmax_rows8(taddr, srow, jmax, a.scale_log2, ps, 1024, m, l);
+            const int jmax = min(kAttnChunk - 1, pos - d.c * kAttnChunk);   // the same for every row
+            float sv[32];
+            tmem_ld_quarter(taddr, q, sv);
+            float m = quarter_max_raw(sv, q * 32, jmax);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            m = __fmul_rn(m, a.scale_log2);
+            uint32_t packed[16];
+            float lq;
+            softmax_quarter(sv, q * 32, jmax, a.scale_log2, m, packed, lq);
+            store_p_quarter(ps, 1024, r, q, packed);
+            const float l0 = __shfl_sync(0xffffffffu, lq, r), l1 = __shfl_sync(0xffffffffu, lq, r + 8);
+            const float l2 = __shfl_sync(0xffffffffu, lq, r + 16), l3 = __shfl_sync(0xffffffffu, lq, r + 24);
+            const float l = __fadd_rn(__fadd_rn(__fadd_rn(l0, l1), l2), l3);
             ptx::tc_fence_before();
-            // value rows past the position hold anything (NaN included): zero them
+            // value rows past the position hold anything (NaN included): zero them once
+            // the chunk's V has landed
             if (d.c == n_total - 1) {
+                if (ok) ok = ptx::mbar_wait(&v_full[st], (i / kDecStages) & 1, err);
 #pragma unroll
                 for (int r4 = 0; r4 < 4; ++r4) {
                     const int vr = lane + 32 * r4;
                     if (d.c * kAttnChunk + vr > pos) {
-                        uint8_t* vrow = sm + D_OFF_KV + st * 4 * kSub + 2 * kSub + vr * 128;
+                        uint8_t* vrow = sm + D_OFF_V + st * 2 * kSub + vr * 128;
 #pragma unroll
                         for (int c16 = 0; c16 < 8; ++c16) {
                             *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
@@ -953,31 +976,32 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&p_full[slot]);
+            if (i + kDecSlots < n_iter) fetch_q(i + kDecSlots);
             if (ok) ok = ptx::mbar_wait(&o_full[slot], k & 1, err);
             ptx::tc_fence_after();
-            float* dst = a.partial + ((((size_t)d.b * a.n_kv_heads + d.g) * a.n_chunks + d.c) * n_rep + lane) * kPartStride;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                float ov[32];
-                ptx::tmem_ld<32>(taddr + cb * 32, ov);
-                ptx::tmem_wait_ld();
-                if (valid)
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        *reinterpret_cast<float4*>(dst + cb * 32 + 4 * q4) =
-                            make_float4(ov[4 * q4], ov[4 * q4 + 1], ov[4 * q4 + 2], ov[4 * q4 + 3]);
-            }
-            if (valid) {
-                dst[128] = m;
-                dst[129] = l;
-            }
+            float ov[32];
+            tmem_ld_quarter(taddr, q, ov);   // row r, output columns 32q..32q+31
             ptx::tc_fence_before();
+            // the slot is free again: prepare it for this warp's next unit before storing
+            if (i + kDecSlots < n_iter) prepare(i + kDecSlots);
+            if (valid) {
+                float* dst =
+                    a.partial + ((((size_t)d.b * a.n_kv_heads + d.g) * a.n_chunks + d.c) * n_rep + r) * kPartStride;
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    *reinterpret_cast<float4*>(dst + q * 32 + 4 * q4) =
+                        make_float4(ov[4 * q4], ov[4 * q4 + 1], ov[4 * q4 + 2], ov[4 * q4 + 3]);
+                if (q == 0) {
+                    dst[128] = m;
+                    dst[129] = l;
+                }
+            }
         }
     }
     __syncthreads();
-    if (warp == 2) {
+    if (warp == kDecSlots + 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 256);
+        ptx::tmem_dealloc(tmem, 512);
     }
 }
 
