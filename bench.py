@@ -323,6 +323,8 @@ def run_ours(args, rank, world, device):
     }
     if args.extra and rank == 0:
         out["extra"] = extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind)
+        del wts
+        out["extra"]["llama31_70b"] = extra_70b(ddb, device, hbm, bf16_peak, peak_kind)
     return out
 
 
@@ -362,8 +364,9 @@ def run_prefill(args, rank, world, device):
 
 
 def blk_launches_per_decode():
-    # rmsnorm, qkv, attention chunks, attention combine, o, rmsnorm, gate/up, down
-    return 8
+    # rmsnorm_1; qkv projection + its segment reduction; attention chunks + combine;
+    # o projection + reduction fused with rmsnorm_2; gate/up + reduction; down + reduction
+    return 11
 
 
 STAGES = ("rmsnorm_1", "qkv", "attention", "o_proj", "rmsnorm_2", "gate_up", "down")
@@ -446,6 +449,45 @@ def extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind):
         tf = fl / (ms / 1e3) / 1e12
         res[f"prefill_t{T}"] = {"tok_s": round(T / (ms / 1e3), 1), "ms": round(ms, 3), "tflops": round(tf, 1),
                                 "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind}
+    return res
+
+
+def extra_70b(ddb, device, hbm, bf16_peak, peak_kind):
+    """The 70B-shaped block: decode at batch 16 with 8192 cached positions and a
+    4096-token prefill, each timed on its own (fresh seeded weights, N(0, 0.01))."""
+    cfg = workloads.BLOCK_70B
+    dims = cfg["dims"]
+    wts = workloads.make_weights(dims, weight_std=cfg["weight_std"])
+    w = {k: v.to(device) for k, v in wts[0].items()}
+    g = {k: v.to(device) for k, v in wts[1].items()}
+    stream = torch.cuda.current_stream(device)
+    res = {}
+    B, P = cfg["decode_batch"], cfg["cache_len"]
+    inp = workloads.make_block_inputs(dims, B, 1, cache_len=P, max_seq=P + 8, weights=wts)
+    blk = ddb.LlamaBlock(dims, w, g, P + 8)
+    kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+    x = inp.x.to(device)
+    y = torch.empty_like(x)
+    ws = blk.workspace(B, 1)
+    ms = time_region(lambda: blk.decode(x, kv, P, y, ws), 20, 3, stream)
+    assert blk.poll_error() == 0
+    by = decode_step_bytes(dims, B, P)
+    res["decode_b16_pos8192"] = {"tok_s": round(B / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
+                                 "algorithmic_bytes": by, "hbm_frac": round(by / (ms / 1e3) / 1e9 / hbm, 4)}
+    del inp, kv, x, y, ws, blk
+    T = cfg["prefill_tokens"]
+    inp = workloads.make_block_inputs(dims, 1, T, max_seq=T, weights=wts, poison_tail=False)
+    blk = ddb.LlamaBlock(dims, w, g, T)
+    kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+    x = inp.x.to(device)
+    y = torch.empty_like(x)
+    ws = blk.workspace(1, T)
+    ms = time_region(lambda: blk.prefill(x, kv, y, ws), 5, 2, stream)
+    assert blk.poll_error() == 0
+    fl = prefill_flops(dims, 1, T)
+    tf = fl / (ms / 1e3) / 1e12
+    res[f"prefill_t{T}"] = {"tok_s": round(T / (ms / 1e3), 1), "ms": round(ms, 3), "tflops": round(tf, 1),
+                            "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind}
     return res
 
 
