@@ -76,6 +76,39 @@ __device__ __forceinline__ float rms_tree_256(float ss, float* red) {
     return t;
 }
 
+// RMSNorm sum of squares of a row of S * 512 elements, as every kernel computes it
+// when the width is a multiple of 512 (at most 16 slices): the row is cut into
+// slices of 512; in slice c thread t (of 256) holds elements c*512 + t and
+// c*512 + t + 256 -- v[2c] and v[2c+1], the same ownership as i = t + 256 e --
+// and squares them as fma(v1, v1, v0 * v0); each slice is reduced by the tree of
+// rms_tree_256 and the slice sums are added in slice order.  A kernel spread over
+// S CTAs (one slice each) reproduces it with rms_tree_256 per slice.
+__device__ __forceinline__ float rms_slice_sq(float v0, float v1) { return __fmaf_rn(v1, v1, __fmul_rn(v0, v0)); }
+template <int S>
+__device__ __forceinline__ float rms_sumsq_slices(const float* v, float* red /* [S * 8] */) {
+    float p[S];
+#pragma unroll
+    for (int c = 0; c < S; ++c) {
+        p[c] = rms_slice_sq(v[2 * c], v[2 * c + 1]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) p[c] = __fadd_rn(p[c], __shfl_xor_sync(0xffffffffu, p[c], off));
+    }
+    __syncthreads();   // red may still be read from a previous use
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll
+        for (int c = 0; c < S; ++c) red[c * 8 + (threadIdx.x >> 5)] = p[c];
+    __syncthreads();
+    float total = 0.f;
+#pragma unroll
+    for (int c = 0; c < S; ++c) {
+        float t = red[c * 8];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) t = __fadd_rn(t, red[c * 8 + w]);
+        total = (c == 0) ? t : __fadd_rn(total, t);
+    }
+    return total;
+}
+
 // Launch with programmatic stream serialization: the kernel may begin while the
 // previous kernel on the stream drains.  Every kernel of the library calls
 // griddepcontrol.wait before it reads anything an earlier kernel wrote, and lets

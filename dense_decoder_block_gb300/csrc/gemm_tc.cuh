@@ -38,6 +38,7 @@ struct GemmKArgs {
     int M, F, K;
     int n_segs, seg_kb;
     int q_tiles, k_tiles;     // QKV: feature tiles per map (wq, wk); the rest are wv
+    int group;                // token-tiled: token blocks taken per feature tile in a row
     GemmEpi e;
     float* partial;   // weight-streaming: fp32 segment results [seg][acc][M][F]
 };

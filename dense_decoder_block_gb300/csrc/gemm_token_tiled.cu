@@ -1,4 +1,6 @@
 // Token-tiled (prefill) instantiations of the persistent tcgen05 projection kernel.
+#include <algorithm>
+
 #include "gemm_tt.cuh"
 
 namespace llama {
@@ -21,9 +23,14 @@ static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUten
     }
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
-    const int tiles = (p.F / kTileF) * ((p.M + BN - 1) / BN);
+    const int n_blocks = (p.M + BN - 1) / BN;
+    const int tiles = (p.F / kTileF) * n_blocks;
     const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
-    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, a0, a1, a2, mb, ka);
+    // token blocks per group: about 32 MB of activations (a quarter of L2), at least one
+    GemmKArgs k = ka;
+    const long block_bytes = (long)BN * p.K * 2;
+    k.group = (int)std::max(1L, std::min((long)n_blocks, (32L << 20) / block_bytes));
+    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, a0, a1, a2, mb, k);
 }
 
 cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,

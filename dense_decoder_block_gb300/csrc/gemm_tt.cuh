@@ -8,8 +8,10 @@
 // warps (four per TMEM lane quarter, each owning a quarter of the columns) keep
 // the running sums in registers; after a tile's last segment they apply the
 // fused epilogue and store, while the MMAs of the next tile already run.
-// Tiles are taken in groups of up to 8 token blocks per feature tile, so a
-// weight tile is reused from L2 by the CTAs working on the group.
+// Tiles are taken in groups of `group` token blocks per feature tile (chosen on
+// the host so that a group's activations stay well inside L2), so a weight
+// tile is streamed from HBM once per group and reused from L2 by the CTAs
+// working on it.
 //
 // Warp roles (640 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
 // issuer, warps 2-3 idle; warps 4..19 = epilogue, warp w reading TMEM lane
@@ -38,7 +40,6 @@ struct TtCfg {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
     static_assert(2 * ACC_COLS <= 512, "two TMEM buffers");
 };
-constexpr int kTtGroup = 8;   // token blocks per feature tile, consecutively
 
 template <int BN, bool DUAL, int EPI>
 __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
@@ -64,13 +65,14 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
     const int n_tiles = m_tiles * n_blocks;
     int* err = a.e.err;
 
-    // tile t -> (feature tile m, token block n), groups of kTtGroup token blocks
+    // tile t -> (feature tile m, token block n), groups of a.group token blocks
+    const int G = a.group;
     auto tile_mn = [&](int t, int& m, int& n) {
-        const int grp = t / (kTtGroup * m_tiles);
-        const int rem = t - grp * kTtGroup * m_tiles;
-        const int gn = min(kTtGroup, n_blocks - grp * kTtGroup);
+        const int grp = t / (G * m_tiles);
+        const int rem = t - grp * G * m_tiles;
+        const int gn = min(G, n_blocks - grp * G);
         m = rem / gn;
-        n = grp * kTtGroup + (rem - m * gn);
+        n = grp * G + (rem - m * gn);
     };
 
     if (threadIdx.x == 0) {

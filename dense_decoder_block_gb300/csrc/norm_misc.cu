@@ -15,13 +15,15 @@ __device__ __forceinline__ float to_f(float v) { return v; }
 // "Llama 3.1 70B", RMSNorm reference implementation: fp32 mean of squares,
 // eps inside the square root, the scaled row cast to the trunk dtype before the
 // gain multiplies it.  One 256-thread CTA per row; thread t owns elements
-// t, t+256, ... (kept in registers when d/256 is a small power of two); the sum
-// of squares uses rms_tree_256, the tree every RMSNorm of the library uses, so
+// t, t+256, ... (kept in registers when d/256 is a small power of two).  The sum
+// of squares follows the library's one definition for the width (common.cuh:
+// 512-element slices when d is a multiple of 512, else one chain per thread and
+// rms_tree_256), which the decode reduction fused with RMSNorm reproduces, so
 // prefill and decode rows agree bit for bit.
 template <typename T, int EPT>
 __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ x, const T* __restrict__ g,
                                                           T* __restrict__ y, int d, float eps) {
-    __shared__ float red[kNormThreads / 32];
+    __shared__ float red[16 * 8];
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x, tid = threadIdx.x;
@@ -29,13 +31,18 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ 
     T* yr = y + (size_t)row * d;
     if constexpr (EPT > 0) {
         float v[EPT];
-        float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) {
-            v[e] = to_f(xr[tid + kNormThreads * e]);
-            ss = __fmaf_rn(v[e], v[e], ss);
+        for (int e = 0; e < EPT; ++e) v[e] = to_f(xr[tid + kNormThreads * e]);
+        float sumsq;
+        if constexpr (EPT >= 4 && EPT % 2 == 0 && EPT / 2 <= 16) {
+            sumsq = rms_sumsq_slices<EPT / 2>(v, red);   // width a multiple of 512
+        } else {
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) ss = __fmaf_rn(v[e], v[e], ss);
+            sumsq = rms_tree_256(ss, red);
         }
-        const float r = rms_scale(rms_tree_256(ss, red), d, eps);
+        const float r = rms_scale(sumsq, d, eps);
 #pragma unroll
         for (int e = 0; e < EPT; ++e) {
             const int i = tid + kNormThreads * e;

@@ -17,31 +17,43 @@ namespace llama {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 16;   // segments loaded per round trip
 
 __device__ __forceinline__ void griddep() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Ascending sum over segments of 4 consecutive fp32 values at `off`.
-__device__ __forceinline__ float4 seg_sum4(const float* part, size_t seg_stride, int n_segs, size_t off) {
-    float4 s = __ldcg(reinterpret_cast<const float4*>(part + off));
-    for (int s0 = 1; s0 < n_segs; s0 += kBatch) {
-        float4 v[kBatch];
+__device__ __forceinline__ void add4(float4& s, const float4& v) {
+    s.x = __fadd_rn(s.x, v.x);
+    s.y = __fadd_rn(s.y, v.y);
+    s.z = __fadd_rn(s.z, v.z);
+    s.w = __fadd_rn(s.w, v.w);
+}
+
+// Ascending sums over segments of 4 consecutive fp32 values at off (and at off2
+// when PAIR): the loads of a batch of segments are all issued before its adds.
+// The sums start at -0, and -0 + x == x for every fp32 x, so each equals
+// ((s0 + s1) + s2) + ... exactly.
+template <bool PAIR, int NB>
+__device__ __forceinline__ void seg_sum4(const float* part, size_t seg_stride, int n_segs, size_t off, size_t off2,
+                                         float4& s, float4& s2) {
+    s = make_float4(-0.f, -0.f, -0.f, -0.f);
+    s2 = s;
+    for (int s0 = 0; s0 < n_segs; s0 += NB) {   // NB segments loaded per round trip
+        float4 v[NB], w[NB];
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-            if (s0 + i < n_segs) v[i] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)(s0 + i) * seg_stride + off));
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i)
+        for (int i = 0; i < NB; ++i)
             if (s0 + i < n_segs) {
-                s.x = __fadd_rn(s.x, v[i].x);
-                s.y = __fadd_rn(s.y, v[i].y);
-                s.z = __fadd_rn(s.z, v[i].z);
-                s.w = __fadd_rn(s.w, v[i].w);
+                v[i] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)(s0 + i) * seg_stride + off));
+                if (PAIR) w[i] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)(s0 + i) * seg_stride + off2));
+            }
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+            if (s0 + i < n_segs) {
+                add4(s, v[i]);
+                if (PAIR) add4(s2, w[i]);
             }
     }
-    return s;
 }
 
 __device__ __forceinline__ void store4(bf16* dst, float a, float b, float c, float d) {
@@ -60,13 +72,14 @@ __device__ __forceinline__ float4 load4_bf16(const bf16* src) {
     return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
 }
 
-__global__ void __launch_bounds__(kThreads) k_reduce_qkv(const ReduceArgs r) {
+__global__ void __launch_bounds__(kThreads, 3) k_reduce_qkv(const ReduceArgs r) {
     griddep();
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
     if (idx >= r.M * F4) return;
     const int n = idx / F4, f0 = (idx - n * F4) * 4;
-    const float4 s = seg_sum4(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0);
+    float4 s, unused;
+    seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
     const GemmEpi& e = r.e;
     const int tile = f0 / 128, row0 = f0 % 128;
     int kind, head;
@@ -97,19 +110,20 @@ __global__ void __launch_bounds__(kThreads) k_reduce_qkv(const ReduceArgs r) {
     store4(dst, v0, v1, v2, v3);
 }
 
-__global__ void __launch_bounds__(kThreads) k_reduce_resid(const ReduceArgs r) {
+__global__ void __launch_bounds__(kThreads, 4) k_reduce_resid(const ReduceArgs r) {
     griddep();
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
     if (idx >= r.M * F4) return;
     const int n = idx / F4, f0 = (idx - n * F4) * 4;
     const size_t off = (size_t)n * r.F + f0;
-    const float4 s = seg_sum4(r.partial, (size_t)r.M * r.F, r.n_segs, off);
+    float4 s, unused;
+    seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, off, 0, s, unused);
     const float4 x = load4_bf16(r.e.resid + off);
     store4(r.e.out + off, epi_resid(x.x, s.x), epi_resid(x.y, s.y), epi_resid(x.z, s.z), epi_resid(x.w, s.w));
 }
 
-__global__ void __launch_bounds__(kThreads) k_reduce_swiglu(const ReduceArgs r) {
+__global__ void __launch_bounds__(kThreads, 3) k_reduce_swiglu(const ReduceArgs r) {
     griddep();
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
@@ -117,60 +131,72 @@ __global__ void __launch_bounds__(kThreads) k_reduce_swiglu(const ReduceArgs r) 
     const int n = idx / F4, f0 = (idx - n * F4) * 4;
     const size_t off = (size_t)n * r.F + f0;
     const size_t plane = (size_t)r.M * r.F;                  // [seg][gate|up][M][F]
-    const float4 g = seg_sum4(r.partial, 2 * plane, r.n_segs, off);
-    const float4 u = seg_sum4(r.partial, 2 * plane, r.n_segs, plane + off);
+    float4 g, u;
+    seg_sum4<true, 4>(r.partial, 2 * plane, r.n_segs, off, plane + off, g, u);
     store4(r.e.out + off, epi_swiglu(g.x, u.x), epi_swiglu(g.y, u.y), epi_swiglu(g.z, u.z), epi_swiglu(g.w, u.w));
 }
 
-// One CTA per token row: h = resid epilogue, then RMSNorm(h) with the same element
-// ownership (i = tid + 256 e) and tree as the standalone RMSNorm kernel.
-template <int EPT>
+// h = resid epilogue, then RMSNorm(h), one cluster of S CTAs per token row: CTA c
+// holds the row's slice c (elements c*512 + t and c*512 + t + 256 of thread t),
+// computes its slice's sum of squares with rms_tree_256, sends it to every CTA of
+// the cluster through distributed shared memory, and after one cluster barrier
+// each CTA adds the S slice sums in slice order -- the definition k_rmsnorm uses
+// for widths that are multiples of 512.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(const float* local_addr, uint32_t rank, float v) {
+    uint32_t a = (uint32_t)__cvta_generic_to_shared(local_addr), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int S>
 __global__ void __launch_bounds__(kThreads) k_reduce_resid_norm(const ReduceArgs r, const bf16* __restrict__ gain,
                                                                 bf16* __restrict__ hn, float eps) {
     __shared__ float red[8];
+    __shared__ float slice_sum[S];
     griddep();
-    const int n = blockIdx.x, tid = threadIdx.x;
+    const int c = (int)cluster_ctarank(), n = blockIdx.y, tid = threadIdx.x;
     const int d = r.F;
     const size_t plane = (size_t)r.M * r.F;
     const size_t row = (size_t)n * d;
-    constexpr int SB = (64 / EPT) > 0 ? (64 / EPT) : 1;   // segments per load batch
-    float acc[EPT];
-    {
-        float v[EPT];
+    const int i0 = c * 512 + tid, i1 = i0 + 256;
+    float a0 = -0.f, a1 = -0.f;   // -0 + x == x: the sums equal ((s0 + s1) + s2) + ...
+    for (int s0 = 0; s0 < r.n_segs; s0 += 8) {
+        float w0[8], w1[8];
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) acc[e] = __ldcg(r.partial + row + tid + 256 * e);
-        for (int s0 = 1; s0 < r.n_segs; s0 += SB) {
-            float w[SB][EPT];
+        for (int i = 0; i < 8; ++i)
+            if (s0 + i < r.n_segs) {
+                w0[i] = __ldcg(r.partial + (size_t)(s0 + i) * plane + row + i0);
+                w1[i] = __ldcg(r.partial + (size_t)(s0 + i) * plane + row + i1);
+            }
 #pragma unroll
-            for (int i = 0; i < SB; ++i)
-                if (s0 + i < r.n_segs)
-#pragma unroll
-                    for (int e = 0; e < EPT; ++e) w[i][e] = __ldcg(r.partial + (size_t)(s0 + i) * plane + row + tid + 256 * e);
-#pragma unroll
-            for (int i = 0; i < SB; ++i)
-                if (s0 + i < r.n_segs)
-#pragma unroll
-                    for (int e = 0; e < EPT; ++e) acc[e] = __fadd_rn(acc[e], w[i][e]);
-        }
-        (void)v;
+        for (int i = 0; i < 8; ++i)
+            if (s0 + i < r.n_segs) {
+                a0 = __fadd_rn(a0, w0[i]);
+                a1 = __fadd_rn(a1, w1[i]);
+            }
     }
-    float h[EPT];
-    float ss = 0.f;
+    const bf16 hb0 = __float2bfloat16_rn(epi_resid(__bfloat162float(r.e.resid[row + i0]), a0));
+    const bf16 hb1 = __float2bfloat16_rn(epi_resid(__bfloat162float(r.e.resid[row + i1]), a1));
+    r.e.out[row + i0] = hb0;
+    r.e.out[row + i1] = hb1;
+    const float h0 = __bfloat162float(hb0), h1 = __bfloat162float(hb1);
+    const float part = rms_tree_256(rms_slice_sq(h0, h1), red);
+    if (tid < S) st_cluster_f32(&slice_sum[c], (uint32_t)tid, part);   // to every CTA of the cluster
+    cluster_sync();
+    float total = slice_sum[0];
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-        const int i = tid + 256 * e;
-        const bf16 hb = __float2bfloat16_rn(epi_resid(__bfloat162float(r.e.resid[row + i]), acc[e]));
-        r.e.out[row + i] = hb;
-        h[e] = __bfloat162float(hb);
-        ss = __fmaf_rn(h[e], h[e], ss);
-    }
-    const float scale = rms_scale(rms_tree_256(ss, red), d, eps);
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-        const int i = tid + 256 * e;
-        const float xs = bf16_round(__fmul_rn(h[e], scale));
-        hn[row + i] = __float2bfloat16_rn(__fmul_rn(xs, __bfloat162float(gain[i])));
-    }
+    for (int k = 1; k < S; ++k) total = __fadd_rn(total, slice_sum[k]);
+    const float scale = rms_scale(total, d, eps);
+    hn[row + i0] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h0, scale)), __bfloat162float(gain[i0])));
+    hn[row + i1] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h1, scale)), __bfloat162float(gain[i1])));
 }
 
 dim3 grid4(const ReduceArgs& r) { return dim3((unsigned)(((size_t)r.M * (r.F / 4) + kThreads - 1) / kThreads)); }
@@ -188,21 +214,46 @@ cudaError_t launch_reduce(const ReduceArgs& r, int kind, cudaStream_t s) {
     }
 }
 
+// The widths whose k_rmsnorm uses the slice definition (d / 256 in {4, 8, 16, 32}).
 bool reduce_resid_norm_supported(int d) {
-    return d % 256 == 0 && (d / 256 == 1 || d / 256 == 2 || d / 256 == 4 || d / 256 == 8 || d / 256 == 16 ||
-                            d / 256 == 32);
+    return d % 512 == 0 && (d / 512 == 2 || d / 512 == 4 || d / 512 == 8 || d / 512 == 16);
+}
+
+template <int S>
+static cudaError_t launch_resid_norm(const ReduceArgs& r, const void* gain, void* hn, float eps, cudaStream_t s) {
+    auto kern = k_reduce_resid_norm<S>;
+    if (S > 8) {
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, r.M);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, r, (const bf16*)gain, (bf16*)hn, eps);
 }
 
 cudaError_t launch_reduce_resid_norm(const ReduceArgs& r, const void* gain, void* hn, float eps, cudaStream_t s) {
     if (r.M <= 0) return cudaSuccess;
-    const dim3 g(r.M), b(kThreads);
-    switch (r.F / 256) {
-        case 1: return launch_pdl(k_reduce_resid_norm<1>, g, b, 0, s, r, (const bf16*)gain, (bf16*)hn, eps);
-        case 2: return launch_pdl(k_reduce_resid_norm<2>, g, b, 0, s, r, (const bf16*)gain, (bf16*)hn, eps);
-        case 4: return launch_pdl(k_reduce_resid_norm<4>, g, b, 0, s, r, (const bf16*)gain, (bf16*)hn, eps);
-        case 8: return launch_pdl(k_reduce_resid_norm<8>, g, b, 0, s, r, (const bf16*)gain, (bf16*)hn, eps);
-        case 16: return launch_pdl(k_reduce_resid_norm<16>, g, b, 0, s, r, (const bf16*)gain, (bf16*)hn, eps);
-        case 32: return launch_pdl(k_reduce_resid_norm<32>, g, b, 0, s, r, (const bf16*)gain, (bf16*)hn, eps);
+    switch (r.F / 512) {
+        case 2: return launch_resid_norm<2>(r, gain, hn, eps, s);
+        case 4: return launch_resid_norm<4>(r, gain, hn, eps, s);
+        case 8: return launch_resid_norm<8>(r, gain, hn, eps, s);
+        case 16: return launch_resid_norm<16>(r, gain, hn, eps, s);
         default: return cudaErrorInvalidValue;
     }
 }
