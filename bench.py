@@ -363,6 +363,101 @@ def run_prefill(args, rank, world, device):
             "gpu_launches": args.steps * 7}
 
 
+def run_stack(args, rank, world, device):
+    """The 8B-shaped decoder stack: 32 blocks, token embedding, final RMSNorm + LM head
+    + greedy choice; batch 32, a 1024-token prefill, then 256 decode steps that feed
+    each chosen id back (one step = one captured graph replay).  `value` is the
+    decode throughput; the prefill is reported beside it."""
+    import dense_decoder_block_gb300 as ddb
+    from dense_decoder_block_gb300.stack import LlamaStack
+    ddb.lib()
+    cfg = workloads.STACK_8B
+    dims, L, B, T, steps, V = cfg["dims"], cfg["n_layers"], cfg["batch"], cfg["prefill_tokens"], \
+        cfg["decode_steps"], cfg["vocab"]
+    std = cfg["weight_std"]
+    max_seq = T + steps
+
+    def draw(shape, seed):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(seed)
+        return torch.randn(shape, generator=gen, device=device).mul_(std).to(torch.bfloat16)
+
+    shapes = dims.weight_shapes()
+    layers = []
+    for l in range(L):
+        w = {name: draw(shapes[name], 1000 + 16 * l + i) for i, name in enumerate(workloads.WEIGHT_NAMES)}
+        g = {name: torch.ones(dims.d_model, dtype=torch.bfloat16, device=device) for name in workloads.GAIN_NAMES}
+        layers.append((w, g))
+    w_embed = draw((V, dims.d_model), 7)
+    w_out = draw((V, dims.d_model), 8)
+    g_final = torch.ones(dims.d_model, dtype=torch.bfloat16, device=device)
+    st = LlamaStack(dims, layers, w_embed, g_final, w_out, batch=B, max_seq=max_seq, prefill_tokens=T)
+    ids = workloads.make_token_ids(B, T, V, seed=9).to(device)
+    stream = torch.cuda.current_stream(device)
+
+    # prefill: warm-up once, then time a few
+    n_pre = 3
+    pre_ms = time_region(lambda: st.prefill(ids), n_pre, 1, stream)
+    assert st.poll_error() == 0 and int(st.err.item()) == 0
+    pre_flops = L * prefill_flops(dims, B, T) + 2 * B * dims.d_model * V
+
+    # decode: capture one step, replay `steps` times after a fresh prefill
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        st.decode_step(side)                   # warm-up outside the capture
+        torch.cuda.synchronize(device)
+        with torch.cuda.graph(graph, stream=side):
+            st.decode_step(side)
+    torch.cuda.synchronize(device)
+    st.prefill(ids)
+    torch.cuda.synchronize(device)
+    for _ in range(3):                         # warm-up replays, then restart from the prefill
+        graph.replay()
+    st.prefill(ids)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index or 0)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with sampler:
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+    dec_ms = a.elapsed_time(b)
+    assert st.poll_error() == 0 and int(st.err.item()) == 0
+    assert int(st.pos.item()) == T + steps
+    ids_last = st.ids.cpu()
+    assert int(ids_last.min()) >= 0 and int(ids_last.max()) < V
+    # the prefill is a long step (about half a second of tensor-core work): sustained bf16 peak
+    hbm, _, bf16_sustained, peak_kind = peaks()
+    bf16_peak = bf16_sustained if bf16_sustained > 0 else peaks()[1]
+    step_bytes = [L * decode_step_bytes(dims, B, T + k) + 2 * V * dims.d_model + 2 * B * dims.d_model
+                  for k in range(steps)]
+    dec_bytes = sum(step_bytes)
+    tok_s = B * steps / (dec_ms / 1e3)
+    return {"metric": METRIC, "value": round(tok_s * world, 1), "unit": "tok/s", "n_gpus": world,
+            "steps": steps, "warmup": 3, "ms_per_step": round(dec_ms / steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,0.02) weights drawn on the device, uniform token ids)",
+            "config": {"workload": f"Llama-3 8B-shaped stack: {L} blocks + embedding + LM head (V={V}), batch {B}, "
+                                   f"{T}-token prefill then {steps} greedy decode steps",
+                       "layers": L, "batch": B, "prefill_tokens": T, "decode_steps": steps,
+                       "l2": "inputs larger than L2: 15.9 GB of weights per decode step"},
+            "decode": {"tok_s": round(tok_s, 1), "us_per_step": round(dec_ms / steps * 1e3, 1),
+                       "hbm_frac": round(dec_bytes / (dec_ms / 1e3) / 1e9 / hbm, 4),
+                       "algorithmic_bytes_per_step": round(dec_bytes / steps), "peak_gbs": hbm},
+            "prefill": {"ms": round(pre_ms, 2), "tok_s": round(B * T / (pre_ms / 1e3), 1),
+                        "tflops": round(pre_flops / (pre_ms / 1e3) / 1e12, 1),
+                        "frac_of_bf16_peak": round(pre_flops / (pre_ms / 1e3) / 1e12 / bf16_peak, 4),
+                        "peak_tflops": bf16_peak, "peak_kind": peak_kind + " (sustained)"},
+            "clocks": sampler.summary(),
+            "gpu_launches": steps * (2 + L * blk_launches_per_decode() + 3) + (n_pre + 1) * (1 + L * 7 + 3),
+            "launch": "one CUDA graph per decode step (embedding, 32 blocks, head, position update)"}
+
+
 def blk_launches_per_decode():
     # rmsnorm_1; qkv projection + its segment reduction; attention chunks + combine;
     # o projection + reduction fused with rmsnorm_2; gate/up + reduction; down + reduction
@@ -569,8 +664,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("decode", "prefill"), default="decode",
-                    help="decode: the 8B decode block (default); prefill: the 8B causal prefill block at --tokens")
+    ap.add_argument("--workload", choices=("decode", "prefill", "stack"), default="decode",
+                    help="decode: the 8B decode block (default); prefill: the 8B causal prefill block at --tokens; "
+                         "stack: 32 blocks + embedding + LM head, prefill then greedy decode")
     ap.add_argument("--tokens", type=int, default=2048, help="prefill tokens (with --workload prefill)")
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -592,7 +688,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    out = run_ours(args, rank, world, device) if args.workload == "decode" else run_prefill(args, rank, world, device)
+    run = {"decode": run_ours, "prefill": run_prefill, "stack": run_stack}[args.workload]
+    out = run(args, rank, world, device)
     if rank == 0 and args.cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline_line(workloads.LLAMA3_8B)
     if rank == 0:
