@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- epilogue (8 warps)
-        ptx::griddep_wait();   // residuals, partials and tickets come from earlier kernels
+        ptx::griddep_wait();   // residuals come from earlier kernels
         const int ew = warp - 2;
         const int quarter = warp & 3;
         const int half = ew >> 2;

@@ -11,6 +11,7 @@
 //   resid + RMSNorm: h as resid, then hn = RMSNorm(h) with the 256-thread tree
 // All loads of one output are issued before its additions (one round trip).
 #include "internal.h"
+#include "reduce_epi.cuh"
 
 namespace llama {
 
@@ -23,55 +24,6 @@ __device__ __forceinline__ void griddep() {
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ void add4(float4& s, const float4& v) {
-    s.x = __fadd_rn(s.x, v.x);
-    s.y = __fadd_rn(s.y, v.y);
-    s.z = __fadd_rn(s.z, v.z);
-    s.w = __fadd_rn(s.w, v.w);
-}
-
-// Ascending sums over segments of 4 consecutive fp32 values at off (and at off2
-// when PAIR): the loads of a batch of segments are all issued before its adds.
-// The sums start at -0, and -0 + x == x for every fp32 x, so each equals
-// ((s0 + s1) + s2) + ... exactly.
-template <bool PAIR, int NB>
-__device__ __forceinline__ void seg_sum4(const float* part, size_t seg_stride, int n_segs, size_t off, size_t off2,
-                                         float4& s, float4& s2) {
-    s = make_float4(-0.f, -0.f, -0.f, -0.f);
-    s2 = s;
-    for (int s0 = 0; s0 < n_segs; s0 += NB) {   // NB segments loaded per round trip
-        float4 v[NB], w[NB];
-#pragma unroll
-        for (int i = 0; i < NB; ++i)
-            if (s0 + i < n_segs) {
-                v[i] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)(s0 + i) * seg_stride + off));
-                if (PAIR) w[i] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)(s0 + i) * seg_stride + off2));
-            }
-#pragma unroll
-        for (int i = 0; i < NB; ++i)
-            if (s0 + i < n_segs) {
-                add4(s, v[i]);
-                if (PAIR) add4(s2, w[i]);
-            }
-    }
-}
-
-__device__ __forceinline__ void store4(bf16* dst, float a, float b, float c, float d) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(c, d);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dst) = u;
-}
-
-__device__ __forceinline__ float4 load4_bf16(const bf16* src) {
-    const uint2 u = *reinterpret_cast<const uint2*>(src);
-    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
-    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
-    return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
-}
-
 __global__ void __launch_bounds__(kThreads, 3) k_reduce_qkv(const ReduceArgs r) {
     griddep();
     const int F4 = r.F / 4;
@@ -80,34 +32,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_reduce_qkv(const ReduceArgs r) 
     const int n = idx / F4, f0 = (idx - n * F4) * 4;
     float4 s, unused;
     seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
-    const GemmEpi& e = r.e;
-    const int tile = f0 / 128, row0 = f0 % 128;
-    int kind, head;
-    if (tile < e.n_heads) { kind = 0; head = tile; }
-    else if (tile < e.n_heads + e.n_kv_heads) { kind = 1; head = tile - e.n_heads; }
-    else { kind = 2; head = tile - e.n_heads - e.n_kv_heads; }
-    const int T = e.tokens_per_seq;
-    const int b = n / T, t = n - b * T;
-    const int pos = (e.pos_dev ? *e.pos_dev : e.start_pos) + t;
-    if (pos < 0 || pos >= e.max_pos) {
-        record_error(e.err, LLAMA_ERR_POS_RANGE);
-        return;
-    }
-    float v0 = bf16_round(s.x), v1 = bf16_round(s.y), v2 = bf16_round(s.z), v3 = bf16_round(s.w);
-    if (kind < 2) {
-        const int i0 = row0 >> 1;
-        const float c0 = __ldg(e.cos_tab + (size_t)pos * kRopeMaxPairs + i0);
-        const float s0 = __ldg(e.sin_tab + (size_t)pos * kRopeMaxPairs + i0);
-        const float c1 = __ldg(e.cos_tab + (size_t)pos * kRopeMaxPairs + i0 + 1);
-        const float s1 = __ldg(e.sin_tab + (size_t)pos * kRopeMaxPairs + i0 + 1);
-        const float r0 = rope_rotate_elem(v0, v1, c0, s0, false), r1 = rope_rotate_elem(v1, v0, c0, s0, true);
-        const float r2 = rope_rotate_elem(v2, v3, c1, s1, false), r3 = rope_rotate_elem(v3, v2, c1, s1, true);
-        v0 = r0; v1 = r1; v2 = r2; v3 = r3;
-    }
-    bf16* dst;
-    if (kind == 0) dst = e.out + (size_t)n * (e.n_heads * 128) + head * 128 + row0;
-    else dst = ((kind == 1) ? e.kc : e.vc) + (((size_t)b * e.n_kv_heads + head) * e.kv_seq + pos) * 128 + row0;
-    store4(dst, v0, v1, v2, v3);
+    epi4_qkv(r.e, n, f0, s);
 }
 
 __global__ void __launch_bounds__(kThreads, 4) k_reduce_resid(const ReduceArgs r) {
@@ -119,8 +44,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_resid(const ReduceArgs r
     const size_t off = (size_t)n * r.F + f0;
     float4 s, unused;
     seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, off, 0, s, unused);
-    const float4 x = load4_bf16(r.e.resid + off);
-    store4(r.e.out + off, epi_resid(x.x, s.x), epi_resid(x.y, s.y), epi_resid(x.z, s.z), epi_resid(x.w, s.w));
+    epi4_resid(r.e, r.F, n, f0, s);
 }
 
 __global__ void __launch_bounds__(kThreads, 3) k_reduce_swiglu(const ReduceArgs r) {
@@ -133,7 +57,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_reduce_swiglu(const ReduceArgs 
     const size_t plane = (size_t)r.M * r.F;                  // [seg][gate|up][M][F]
     float4 g, u;
     seg_sum4<true, 4>(r.partial, 2 * plane, r.n_segs, off, plane + off, g, u);
-    store4(r.e.out + off, epi_swiglu(g.x, u.x), epi_swiglu(g.y, u.y), epi_swiglu(g.z, u.z), epi_swiglu(g.w, u.w));
+    epi4_swiglu(r.e, r.F, n, f0, g, u);
 }
 
 // h = resid epilogue, then RMSNorm(h), one cluster of S CTAs per token row: CTA c
