@@ -290,15 +290,26 @@ __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     const int n_chunks = pos / kAttnChunk + 1;
     const float* base = a.partial + (((size_t)b * a.n_kv_heads + g) * a.n_chunks * n_rep + r) * part_stride(DH);
     const size_t cstride = (size_t)n_rep * part_stride(DH);
+    // chunk 0 starts the state; chunks 1.. fold in ascending order.  The loads of a
+    // batch of chunks are issued before its folds (one memory round trip per batch).
+    constexpr int kCB = 8;
     float M = base[DH], L = base[DH + 1], O[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) O[e] = base[lane * DPL + e];
-    for (int c = 1; c < n_chunks; ++c) {
-        const float* p = base + c * cstride;
-        float o[DPL];
+    for (int c0 = 1; c0 < n_chunks; c0 += kCB) {
+        float o[kCB][DPL], m[kCB], l[kCB];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) o[e] = p[lane * DPL + e];
-        fold<DPL>(M, L, O, p[DH], p[DH + 1], o);
+        for (int i = 0; i < kCB; ++i)
+            if (c0 + i < n_chunks) {
+                const float* p = base + (size_t)(c0 + i) * cstride;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[i][e] = p[lane * DPL + e];
+                m[i] = p[DH];
+                l[i] = p[DH + 1];
+            }
+#pragma unroll
+        for (int i = 0; i < kCB; ++i)
+            if (c0 + i < n_chunks) fold<DPL>(M, L, O, m[i], l[i], o[i]);
     }
     T* dst = reinterpret_cast<T*>(a.o) + (size_t)b * a.n_heads * DH + (size_t)h * DH + lane * DPL;
     const float inv_l = __frcp_rn(L);
