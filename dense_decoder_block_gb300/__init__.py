@@ -24,7 +24,8 @@ from ._native import (LLAMA_BF16, LLAMA_F32, LLAMA_OK, LLAMA_ERR_INVALID_ARG, LL
 
 __all__ = [
     "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_destroy",
-    "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_decode", "llama_block_decode_devpos",
+    "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
+    "llama_block_decode_devpos",
     "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_embed", "llama_lmhead_workspace_bytes",
     "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
 ]
@@ -94,6 +95,11 @@ def _check(h, rc, what):
 def llama_block_prefill(h, x, batch, tokens, kv: llama_kv_cache, y, ws, ws_bytes, stream=None) -> None:
     _check(h, lib().llama_block_prefill(h, _ptr(x), batch, tokens, C.byref(kv), _ptr(y), _ptr(ws), ws_bytes,
                                         _stream(stream)), "llama_block_prefill")
+
+
+def llama_block_prefill_at(h, x, batch, tokens, start_pos, kv: llama_kv_cache, y, ws, ws_bytes, stream=None) -> None:
+    _check(h, lib().llama_block_prefill_at(h, _ptr(x), batch, tokens, start_pos, C.byref(kv), _ptr(y), _ptr(ws),
+                                           ws_bytes, _stream(stream)), "llama_block_prefill_at")
 
 
 def llama_block_decode(h, x, batch, kv: llama_kv_cache, pos, y, ws, ws_bytes, stream=None) -> None:
@@ -196,6 +202,11 @@ class LlamaBlock:
     def prefill(self, x, kv: KVCache, y, ws, stream=None):
         B, T = x.shape[0], x.shape[1]
         llama_block_prefill(self.h, x, B, T, kv.c, y, ws, ws.numel(), stream)
+
+    def prefill_at(self, x, kv: KVCache, start_pos: int, y, ws, stream=None):
+        """x [B, T, d] holds the tokens at positions start_pos .. start_pos + T - 1."""
+        B, T = x.shape[0], x.shape[1]
+        llama_block_prefill_at(self.h, x, B, T, start_pos, kv.c, y, ws, ws.numel(), stream)
 
     def decode(self, x, kv: KVCache, pos: int, y, ws, stream=None):
         llama_block_decode(self.h, x, x.shape[0], kv.c, pos, y, ws, ws.numel(), stream)

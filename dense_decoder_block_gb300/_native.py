@@ -49,6 +49,9 @@ SIGNATURES = {
     "llama_block_workspace_bytes": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
     "llama_block_prefill": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.POINTER(llama_kv_cache),
                                       C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "llama_block_prefill_at": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                         C.POINTER(llama_kv_cache), C.c_void_p, C.c_void_p, C.c_size_t,
+                                         C.c_void_p]),
     "llama_block_decode": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.POINTER(llama_kv_cache), C.c_int,
                                      C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "llama_block_decode_devpos": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.POINTER(llama_kv_cache),

@@ -462,6 +462,20 @@ extern "C" int llama_block_prefill(llama_block b, const void* x, int batch, int 
     return run_block(b, x, batch, tokens, kv, 0, nullptr, y, ws, ws_bytes, stream, false);
 }
 
+extern "C" int llama_block_prefill_at(llama_block b, const void* x, int batch, int tokens, int start_pos,
+                                      const llama_kv_cache* kv, void* y, void* ws, size_t ws_bytes, void* stream) {
+    if (!b) return LLAMA_ERR_INVALID_ARG;
+    if (batch < 0 || tokens < 0) return fail(b, LLAMA_ERR_INVALID_ARG, "negative batch or tokens");
+    if (start_pos < 0) return fail(b, LLAMA_ERR_POS_RANGE, "negative start position");
+    if (batch == 0 || tokens == 0) return LLAMA_OK;
+    if (!x || !y || !aligned16(x) || !aligned16(y))
+        return fail(b, LLAMA_ERR_INVALID_ARG, "x / y null or not 16-byte aligned");
+    if ((long)start_pos + tokens > b->dims.max_seq) return fail(b, LLAMA_ERR_POS_RANGE, "start_pos + tokens > max_seq");
+    int rc = check_kv(b, kv, batch, start_pos + tokens - 1);
+    if (rc != LLAMA_OK) return rc;
+    return run_block(b, x, batch, tokens, kv, start_pos, nullptr, y, ws, ws_bytes, stream, false);
+}
+
 extern "C" int llama_block_decode(llama_block b, const void* x, int batch, const llama_kv_cache* kv, int pos,
                                   void* y, void* ws, size_t ws_bytes, void* stream) {
     if (!b) return LLAMA_ERR_INVALID_ARG;

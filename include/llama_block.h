@@ -111,6 +111,17 @@ size_t llama_block_workspace_bytes(llama_block blk, int batch, int tokens);
 int llama_block_prefill(llama_block blk, const void* x, int batch, int tokens, const llama_kv_cache* kv, void* y,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Prefill of `tokens` new tokens per sequence at positions start_pos ..
+ * start_pos + tokens - 1 on a cache that already holds the earlier tokens
+ * (prefill in chunks).  kv rows 0 .. start_pos - 1 must hold their keys and
+ * values; rows start_pos .. start_pos + tokens - 1 are written; the query at
+ * position p sees keys 0..p.  llama_block_prefill is this call with
+ * start_pos = 0.  Each row equals, bit for bit, the same row of one prefill of
+ * all start_pos + tokens tokens.  start_pos + tokens must not exceed max_seq
+ * (LLAMA_ERR_POS_RANGE otherwise). */
+int llama_block_prefill_at(llama_block blk, const void* x, int batch, int tokens, int start_pos,
+                           const llama_kv_cache* kv, void* y, void* workspace, size_t workspace_bytes, void* stream);
+
 /* One decode step at position pos for every sequence of the batch.
  *   x [batch, 1, d] in, y [batch, 1, d] out (may alias x).
  *   kv rows 0..pos-1 must hold the cached keys/values; row pos is written;

@@ -208,3 +208,76 @@ def test_rmsnorm_step_matches_oracle():
     # fp32 reduction vs fp64: at most one bf16 ulp apart, almost always equal
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30)
     assert np.mean(got == ref) > 0.99
+
+
+@pytest.mark.parametrize("dims,cuts", [(MID, (0, 100, 229, 240, 300)), (WIDE, (0, 130, 131, 200))],
+                         ids=["mid-4-chunks", "wide-3-chunks"])
+def test_bf16_chunked_prefill_bit_identical_to_one_prefill(dims, cuts):
+    """Prefill in chunks at start positions > 0 (chunks crossing 128-key boundaries;
+    chunks of 11 tokens and of one token, whose 22 and 2 rows take the
+    weight-streaming projections) gives the same rows and cache, bit for bit, as one
+    prefill of all the tokens."""
+    B, T = 2, cuts[-1]
+    max_seq = T + 5
+    inp = workloads.make_block_inputs(dims, B, T, max_seq=max_seq)
+    blk, ddb = gpu_block(inp, max_seq)
+    dev = torch.device("cuda:0")
+    x = inp.x.to(dev)
+    kc_full, vc_full = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    y_full = run_prefill(blk, ddb, x, kc_full, vc_full)
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    kv = ddb.KVCache(kc, vc)
+    ys = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        xc = x[:, a:b].contiguous()
+        yc = torch.empty_like(xc)
+        blk.prefill_at(xc, kv, a, yc, blk.workspace(B, b - a))
+        ys.append(yc)
+    torch.cuda.synchronize()
+    assert blk.poll_error() == 0
+    assert torch.equal(torch.cat(ys, dim=1), y_full)
+    assert torch.equal(kc[:, :, :T], kc_full[:, :, :T]) and torch.equal(vc[:, :, :T], vc_full[:, :, :T])
+    assert torch.isnan(kc[:, :, T:]).all() and torch.isnan(vc[:, :, T:]).all()
+
+
+def test_fp32_chunked_prefill_matches_oracle():
+    """The fp32 workload prefilled in two chunks (16 then 4 tokens at position 16)
+    against the oracle run the same way (block_forward at start_pos 16 on its cache)."""
+    cfg = workloads.TINY_FP32
+    T0, T1 = 16, 20
+    max_seq = 24
+    inp = workloads.make_block_inputs(cfg["dims"], 2, T1, dtype=torch.float32, max_seq=max_seq)
+    blk, ddb = gpu_block(inp, max_seq)
+    dev = torch.device("cuda:0")
+    x = inp.x.to(dev)
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    kv = ddb.KVCache(kc, vc)
+    y0 = torch.empty_like(x[:, :T0])
+    y1 = torch.empty_like(x[:, T0:T1])
+    blk.prefill_at(x[:, :T0].contiguous(), kv, 0, y0, blk.workspace(2, T0))
+    blk.prefill_at(x[:, T0:T1].contiguous(), kv, T0, y1, blk.workspace(2, T1 - T0))
+    torch.cuda.synchronize()
+    assert blk.poll_error() == 0
+    w, g = oracle_weights(inp)
+    kr = np.zeros((2, cfg["dims"].n_kv_heads, max_seq, cfg["dims"].head_dim))
+    vr = np.zeros_like(kr)
+    x64 = workloads.to_numpy64(inp.x)
+    r0 = ob.block_forward(x64[:, :T0], w, g, cfg["dims"], kr, vr, 0, rnd_for(inp.dtype))
+    r1 = ob.block_forward(x64[:, T0:T1], w, g, cfg["dims"], kr, vr, T0, rnd_for(inp.dtype))
+    assert rel_err(workloads.to_numpy64(y0), r0) <= F32_TOL
+    assert rel_err(workloads.to_numpy64(y1), r1) <= F32_TOL
+    assert rel_err(workloads.to_numpy64(kc[:, :, :T1]), kr[:, :, :T1]) <= F32_TOL
+
+
+def test_chunked_prefill_position_range():
+    inp = workloads.make_block_inputs(MID, 1, 8, max_seq=16)
+    blk, ddb = gpu_block(inp, 16)
+    dev = torch.device("cuda:0")
+    x = inp.x.to(dev)
+    kv = ddb.KVCache(inp.k_cache.to(dev), inp.v_cache.to(dev))
+    y = torch.empty_like(x)
+    with pytest.raises(ddb.LlamaError) as ei:
+        blk.prefill_at(x, kv, 9, y, blk.workspace(1, 8))   # 9 + 8 > max_seq 16
+    assert ei.value.code == -3   # LLAMA_ERR_POS_RANGE
+    with pytest.raises(ddb.LlamaError):
+        blk.prefill_at(x, kv, -1, y, blk.workspace(1, 8))
