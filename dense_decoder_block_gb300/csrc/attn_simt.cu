@@ -277,15 +277,32 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
     }
 }
 
+// One chunk partial's DPL values of this lane (16-, 8- or 4-byte loads through L2:
+// the partials were written by another kernel's CTAs).
+template <int DPL>
+__device__ __forceinline__ void ld_part(const float* p, float (&o)[DPL]) {
+    if constexpr (DPL == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+        o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    } else if constexpr (DPL == 2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
+        o[0] = v.x; o[1] = v.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[e] = __ldcg(p + e);
+    }
+}
+
 template <typename T, int DH>
 __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     constexpr int DPL = DH / 32;
+    // The position is set before the step, never by the kernels this one overlaps.
+    const int pos = base_position(a);
     ptx_wait();
     if (threadIdx.x == 0) ptx_launch_dependents();
     const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int g = h / n_rep, r = h % n_rep;
-    const int pos = base_position(a);
     if (pos < 0 || pos >= a.max_pos) return;
     const int n_chunks = pos / kAttnChunk + 1;
     const float* base = a.partial + (((size_t)b * a.n_kv_heads + g) * a.n_chunks * n_rep + r) * part_stride(DH);
@@ -293,23 +310,30 @@ __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     // chunk 0 starts the state; chunks 1.. fold in ascending order.  The loads of a
     // batch of chunks are issued before its folds (one memory round trip per batch).
     constexpr int kCB = 8;
-    float M = base[DH], L = base[DH + 1], O[DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) O[e] = base[lane * DPL + e];
-    for (int c0 = 1; c0 < n_chunks; c0 += kCB) {
+    float M = 0.f, L = 0.f, O[DPL];
+    for (int c0 = 0; c0 < n_chunks; c0 += kCB) {
         float o[kCB][DPL], m[kCB], l[kCB];
 #pragma unroll
         for (int i = 0; i < kCB; ++i)
             if (c0 + i < n_chunks) {
                 const float* p = base + (size_t)(c0 + i) * cstride;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) o[i][e] = p[lane * DPL + e];
-                m[i] = p[DH];
-                l[i] = p[DH + 1];
+                ld_part<DPL>(p + lane * DPL, o[i]);
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(p + DH));
+                m[i] = ml.x;
+                l[i] = ml.y;
             }
 #pragma unroll
-        for (int i = 0; i < kCB; ++i)
-            if (c0 + i < n_chunks) fold<DPL>(M, L, O, m[i], l[i], o[i]);
+        for (int i = 0; i < kCB; ++i) {
+            if (c0 + i >= n_chunks) break;
+            if (c0 + i == 0) {
+                M = m[0];
+                L = l[0];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) O[e] = o[0][e];
+            } else {
+                fold<DPL>(M, L, O, m[i], l[i], o[i]);
+            }
+        }
     }
     T* dst = reinterpret_cast<T*>(a.o) + (size_t)b * a.n_heads * DH + (size_t)h * DH + lane * DPL;
     const float inv_l = __frcp_rn(L);

@@ -24,27 +24,40 @@ __device__ __forceinline__ void griddep() {
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// What a reduction reads before griddepcontrol.wait -- the position, the RoPE
+// tables, gains and the residual input -- is never written by the kernel it
+// overlaps: a kernel of this chain starts only after its predecessor passed its
+// own wait, so everything two or more launches back is complete and visible.
+// The residual of each reduction is produced at least two launches earlier (the
+// block input, or h four launches before the last reduction).
+
 __global__ void __launch_bounds__(kThreads, 3) k_reduce_qkv(const ReduceArgs r) {
-    griddep();
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
-    if (idx >= r.M * F4) return;
-    const int n = idx / F4, f0 = (idx - n * F4) * 4;
+    const bool live = idx < r.M * F4;
+    const int n = live ? idx / F4 : 0, f0 = live ? (idx - n * F4) * 4 : 0;
+    Qkv4 p{};
+    if (live) p = epi4_qkv_prepare(r.e, n, f0);
+    griddep();
+    if (!live) return;
     float4 s, unused;
     seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
-    epi4_qkv(r.e, n, f0, s);
+    epi4_qkv_apply(p, s);
 }
 
 __global__ void __launch_bounds__(kThreads, 4) k_reduce_resid(const ReduceArgs r) {
-    griddep();
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
-    if (idx >= r.M * F4) return;
-    const int n = idx / F4, f0 = (idx - n * F4) * 4;
+    const bool live = idx < r.M * F4;
+    const int n = live ? idx / F4 : 0, f0 = live ? (idx - n * F4) * 4 : 0;
     const size_t off = (size_t)n * r.F + f0;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) x = load4_bf16(r.e.resid + off);
+    griddep();
+    if (!live) return;
     float4 s, unused;
     seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, off, 0, s, unused);
-    epi4_resid(r.e, r.F, n, f0, s);
+    epi4_resid(r.e, r.F, n, f0, x, s);
 }
 
 __global__ void __launch_bounds__(kThreads, 3) k_reduce_swiglu(const ReduceArgs r) {
@@ -85,12 +98,16 @@ __global__ void __launch_bounds__(kThreads) k_reduce_resid_norm(const ReduceArgs
                                                                 bf16* __restrict__ hn, float eps) {
     __shared__ float red[8];
     __shared__ float slice_sum[S];
-    griddep();
     const int c = (int)cluster_ctarank(), n = blockIdx.y, tid = threadIdx.x;
     const int d = r.F;
     const size_t plane = (size_t)r.M * r.F;
     const size_t row = (size_t)n * d;
     const int i0 = c * 512 + tid, i1 = i0 + 256;
+    // the block input and the gains are not written by the kernels this one overlaps
+    const float x0 = __bfloat162float(__ldcg(r.e.resid + row + i0));
+    const float x1 = __bfloat162float(__ldcg(r.e.resid + row + i1));
+    const float g0 = __bfloat162float(gain[i0]), g1 = __bfloat162float(gain[i1]);
+    griddep();
     float a0 = -0.f, a1 = -0.f;   // -0 + x == x: the sums equal ((s0 + s1) + s2) + ...
     for (int s0 = 0; s0 < r.n_segs; s0 += 8) {
         float w0[8], w1[8];
@@ -107,8 +124,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_resid_norm(const ReduceArgs
                 a1 = __fadd_rn(a1, w1[i]);
             }
     }
-    const bf16 hb0 = __float2bfloat16_rn(epi_resid(__bfloat162float(r.e.resid[row + i0]), a0));
-    const bf16 hb1 = __float2bfloat16_rn(epi_resid(__bfloat162float(r.e.resid[row + i1]), a1));
+    const bf16 hb0 = __float2bfloat16_rn(epi_resid(x0, a0));
+    const bf16 hb1 = __float2bfloat16_rn(epi_resid(x1, a1));
     r.e.out[row + i0] = hb0;
     r.e.out[row + i1] = hb1;
     const float h0 = __bfloat162float(hb0), h1 = __bfloat162float(hb1);
@@ -119,8 +136,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_resid_norm(const ReduceArgs
 #pragma unroll
     for (int k = 1; k < S; ++k) total = __fadd_rn(total, slice_sum[k]);
     const float scale = rms_scale(total, d, eps);
-    hn[row + i0] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h0, scale)), __bfloat162float(gain[i0])));
-    hn[row + i1] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h1, scale)), __bfloat162float(gain[i1])));
+    hn[row + i0] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h0, scale)), g0));
+    hn[row + i1] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h1, scale)), g1));
 }
 
 dim3 grid4(const ReduceArgs& r) { return dim3((unsigned)(((size_t)r.M * (r.F / 4) + kThreads - 1) / kThreads)); }

@@ -50,8 +50,10 @@ __device__ __forceinline__ void store4_bf16(bf16* dst, float a, float b, float c
     *reinterpret_cast<uint2*>(dst) = u;
 }
 
+// Through L2 (__ldcg): the values may have been written by an earlier kernel of the
+// step that ran on another SM.
 __device__ __forceinline__ float4 load4_bf16(const bf16* src) {
-    const uint2 u = *reinterpret_cast<const uint2*>(src);
+    const uint2 u = __ldcg(reinterpret_cast<const uint2*>(src));
     const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
     const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
     return make_float4(__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi));
@@ -59,7 +61,17 @@ __device__ __forceinline__ float4 load4_bf16(const bf16* src) {
 
 // QKV: bf16 round, RoPE on q/k pairs, q -> workspace, k/v -> the cache row of the
 // token's position.  f0 = first of the 4 features (a multiple of 4), n = token.
-__device__ __forceinline__ void epi4_qkv(const GemmEpi& e, int n, int f0, float4 s) {
+// The work splits in two: epi4_qkv_prepare reads only what the step's earlier
+// kernels do not write (the position, the RoPE tables) and may run before
+// griddepcontrol.wait; epi4_qkv_apply takes the segment sum.
+struct Qkv4 {
+    bf16* dst;              // null: position out of range (error recorded)
+    float c0, s0, c1, s1;   // rotation of the pairs (f0, f0+1), (f0+2, f0+3); unused for v
+    bool rope;
+};
+
+__device__ __forceinline__ Qkv4 epi4_qkv_prepare(const GemmEpi& e, int n, int f0) {
+    Qkv4 p{};
     const int tile = f0 / 128, row0 = f0 % 128;
     int kind, head;
     if (tile < e.n_heads) { kind = 0; head = tile; }
@@ -70,29 +82,36 @@ __device__ __forceinline__ void epi4_qkv(const GemmEpi& e, int n, int f0, float4
     const int pos = (e.pos_dev ? *e.pos_dev : e.start_pos) + t;
     if (pos < 0 || pos >= e.max_pos) {
         record_error(e.err, LLAMA_ERR_POS_RANGE);
-        return;
+        p.dst = nullptr;
+        return p;
     }
-    float v0 = bf16_round(s.x), v1 = bf16_round(s.y), v2 = bf16_round(s.z), v3 = bf16_round(s.w);
-    if (kind < 2) {
+    p.rope = kind < 2;
+    if (p.rope) {
         const int i0 = row0 >> 1;
-        const float c0 = __ldg(e.cos_tab + (size_t)pos * kRopeMaxPairs + i0);
-        const float s0 = __ldg(e.sin_tab + (size_t)pos * kRopeMaxPairs + i0);
-        const float c1 = __ldg(e.cos_tab + (size_t)pos * kRopeMaxPairs + i0 + 1);
-        const float s1 = __ldg(e.sin_tab + (size_t)pos * kRopeMaxPairs + i0 + 1);
-        const float r0 = rope_rotate_elem(v0, v1, c0, s0, false), r1 = rope_rotate_elem(v1, v0, c0, s0, true);
-        const float r2 = rope_rotate_elem(v2, v3, c1, s1, false), r3 = rope_rotate_elem(v3, v2, c1, s1, true);
-        v0 = r0; v1 = r1; v2 = r2; v3 = r3;
+        p.c0 = __ldg(e.cos_tab + (size_t)pos * kRopeMaxPairs + i0);
+        p.s0 = __ldg(e.sin_tab + (size_t)pos * kRopeMaxPairs + i0);
+        p.c1 = __ldg(e.cos_tab + (size_t)pos * kRopeMaxPairs + i0 + 1);
+        p.s1 = __ldg(e.sin_tab + (size_t)pos * kRopeMaxPairs + i0 + 1);
     }
-    bf16* dst;
-    if (kind == 0) dst = e.out + (size_t)n * (e.n_heads * 128) + head * 128 + row0;
-    else dst = ((kind == 1) ? e.kc : e.vc) + (((size_t)b * e.n_kv_heads + head) * e.kv_seq + pos) * 128 + row0;
-    store4_bf16(dst, v0, v1, v2, v3);
+    if (kind == 0) p.dst = e.out + (size_t)n * (e.n_heads * 128) + head * 128 + row0;
+    else p.dst = ((kind == 1) ? e.kc : e.vc) + (((size_t)b * e.n_kv_heads + head) * e.kv_seq + pos) * 128 + row0;
+    return p;
 }
 
-// y = bf16(x + bf16(sum)), [M, F] row-major
-__device__ __forceinline__ void epi4_resid(const GemmEpi& e, int F, int n, int f0, float4 s) {
+__device__ __forceinline__ void epi4_qkv_apply(const Qkv4& p, float4 s) {
+    if (p.dst == nullptr) return;
+    float v0 = bf16_round(s.x), v1 = bf16_round(s.y), v2 = bf16_round(s.z), v3 = bf16_round(s.w);
+    if (p.rope) {
+        const float r0 = rope_rotate_elem(v0, v1, p.c0, p.s0, false), r1 = rope_rotate_elem(v1, v0, p.c0, p.s0, true);
+        const float r2 = rope_rotate_elem(v2, v3, p.c1, p.s1, false), r3 = rope_rotate_elem(v3, v2, p.c1, p.s1, true);
+        v0 = r0; v1 = r1; v2 = r2; v3 = r3;
+    }
+    store4_bf16(p.dst, v0, v1, v2, v3);
+}
+
+// y = bf16(x + bf16(sum)), [M, F] row-major; x (the residual) was loaded by the caller
+__device__ __forceinline__ void epi4_resid(const GemmEpi& e, int F, int n, int f0, float4 x, float4 s) {
     const size_t off = (size_t)n * F + f0;
-    const float4 x = load4_bf16(e.resid + off);
     store4_bf16(e.out + off, epi_resid(x.x, s.x), epi_resid(x.y, s.y), epi_resid(x.z, s.z), epi_resid(x.w, s.w));
 }
 
