@@ -17,6 +17,7 @@
 // neither scored nor loaded.
 #include <cfloat>
 
+#include "attn_fold.cuh"
 #include "internal.h"
 
 namespace llama {
@@ -126,18 +127,6 @@ __device__ __forceinline__ void chunk_partial(const float* q, const T* Ks, const
     }
     m_out = mx;
     l_out = l;
-}
-
-// Fold the partial (m, l, o) of the next chunk into the running state (M, L, O).
-template <int DPL>
-__device__ __forceinline__ void fold(float& M, float& L, float (&O)[DPL], float m, float l, const float (&o)[DPL]) {
-    const float Mn = fmaxf(M, m);
-    const float a = exp2f(__fsub_rn(M, Mn));
-    const float b = exp2f(__fsub_rn(m, Mn));
-    L = __fmaf_rn(L, a, __fmul_rn(l, b));
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) O[e] = __fmaf_rn(O[e], a, __fmul_rn(o[e], b));
-    M = Mn;
 }
 
 struct AttnK {
@@ -277,25 +266,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
     }
 }
 
-// One chunk partial's DPL values of this lane (16-, 8- or 4-byte loads through L2:
-// the partials were written by another kernel's CTAs).
-template <int DPL>
-__device__ __forceinline__ void ld_part(const float* p, float (&o)[DPL]) {
-    if constexpr (DPL == 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
-        o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-    } else if constexpr (DPL == 2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
-        o[0] = v.x; o[1] = v.y;
-    } else {
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[e] = __ldcg(p + e);
-    }
-}
-
 template <typename T, int DH>
 __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
-    constexpr int DPL = DH / 32;
     // The position is set before the step, never by the kernels this one overlaps.
     const int pos = base_position(a);
     ptx_wait();
@@ -304,41 +276,9 @@ __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int g = h / n_rep, r = h % n_rep;
     if (pos < 0 || pos >= a.max_pos) return;
-    const int n_chunks = pos / kAttnChunk + 1;
     const float* base = a.partial + (((size_t)b * a.n_kv_heads + g) * a.n_chunks * n_rep + r) * part_stride(DH);
-    const size_t cstride = (size_t)n_rep * part_stride(DH);
-    // chunk 0 starts the state; chunks 1.. fold in ascending order.  The loads of a
-    // batch of chunks are issued before its folds (one memory round trip per batch).
-    constexpr int kCB = 8;
-    float M = 0.f, L = 0.f, O[DPL];
-    for (int c0 = 0; c0 < n_chunks; c0 += kCB) {
-        float o[kCB][DPL], m[kCB], l[kCB];
-#pragma unroll
-        for (int i = 0; i < kCB; ++i)
-            if (c0 + i < n_chunks) {
-                const float* p = base + (size_t)(c0 + i) * cstride;
-                ld_part<DPL>(p + lane * DPL, o[i]);
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(p + DH));
-                m[i] = ml.x;
-                l[i] = ml.y;
-            }
-#pragma unroll
-        for (int i = 0; i < kCB; ++i) {
-            if (c0 + i >= n_chunks) break;
-            if (c0 + i == 0) {
-                M = m[0];
-                L = l[0];
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) O[e] = o[0][e];
-            } else {
-                fold<DPL>(M, L, O, m[i], l[i], o[i]);
-            }
-        }
-    }
-    T* dst = reinterpret_cast<T*>(a.o) + (size_t)b * a.n_heads * DH + (size_t)h * DH + lane * DPL;
-    const float inv_l = __frcp_rn(L);
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) from_f(dst + e, __fmul_rn(O[e], inv_l));
+    T* dst = reinterpret_cast<T*>(a.o) + (size_t)b * a.n_heads * DH + (size_t)h * DH;
+    fold_row<T, DH>(base, (size_t)n_rep * part_stride(DH), pos / kAttnChunk + 1, lane, dst);
 }
 
 template <typename T, int DH>

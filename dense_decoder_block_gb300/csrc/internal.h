@@ -97,7 +97,7 @@ struct AttnArgs {
     const int* pos_dev = nullptr;
     int max_pos = 0;
     int dtype = LLAMA_BF16;
-    float* partial = nullptr;           // decode: [B, Hkv, n_chunks, n_rep, head_dim + 2]
+    float* partial = nullptr;           // decode: [B, Hkv, n_chunks, n_rep, head_dim + 4]
     int n_chunks = 0;                   // decode: chunk slots per (b, kv head)
     int* err = nullptr;
 };
