@@ -714,20 +714,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // 0, so the MMA's 128 rows repeat rows 0..7: TMEM lane 8g + r holds row r for
 // every g, and all 32 lanes of a warp's lane quarter see the 8 rows.  A softmax
 // warp therefore works on (row r = lane % 8, key quarter g = lane / 8) straight
-// from TMEM.  Three TMEM slots (S and then O_c of one unit share a slot's 128
-// columns) and three softmax warps take units in turn; the MMA thread issues
-// S of unit i before PV of unit i-1.  K and V stream through separate
-// three-stage TMA rings, so K of unit i+3 loads as soon as S(i) has read K(i).
-// Warps: 0..2 = softmax + partial store of slots 0..2, 3 = K producer,
-// 4 = TMEM owner + MMA issuer, 5 = V producer.
-constexpr int kDecSlots = 3;
+// from TMEM.  Four TMEM slots (S and then O_c of one unit share a slot's 128
+// columns) and four softmax warps take units in turn; the MMA thread issues
+// S of unit i before PV of unit i-1.  K and V stream through separate TMA
+// rings: K is released as soon as S has read it (two stages), V only after PV,
+// which follows the unit's softmax (four stages, one per slot).
+// Warps: 0..3 = softmax + partial store of slots 0..3, 4 = K producer,
+// 5 = TMEM owner + MMA issuer, 6 = V producer.
+constexpr int kDecSlots = 4;
 constexpr int kDecThreads = 32 * (kDecSlots + 3);
-constexpr int kDecStages = 3;
+constexpr int kDecStagesK = 2;   // K is released as soon as S has read it
+constexpr int kDecStagesV = 4;   // V is held until PV, after the softmax of its unit
 constexpr int D_OFF_Q = 0;                              // [slot][half] 1 KB each
 constexpr int D_OFF_P = 8192;                           // [slot][half] 1 KB each
 constexpr int D_OFF_K = 16384;                          // [stage] K: 2 sub-tiles
-constexpr int D_OFF_V = D_OFF_K + kDecStages * 2 * kSub;   // [stage] V: 2 sub-tiles
-constexpr int D_OFF_BAR = D_OFF_V + kDecStages * 2 * kSub;
+constexpr int D_OFF_V = D_OFF_K + kDecStagesK * 2 * kSub;   // [stage] V: 2 sub-tiles
+constexpr int D_OFF_BAR = D_OFF_V + kDecStagesV * 2 * kSub;
+static_assert(kDecSlots * 2048 <= D_OFF_P && D_OFF_P + kDecSlots * 2048 <= D_OFF_K, "query / P tiles");
+static_assert(kDecSlots * 128 <= 512, "TMEM columns");
 constexpr int D_SMEM_BYTES = D_OFF_BAR + 256 + 1024;
 
 __device__ __forceinline__ uint64_t sw128_kmajor_desc_rows8(uint32_t smem_addr) {
@@ -765,10 +769,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + D_OFF_BAR);
     uint64_t* k_full = bars + 0;                         // [stages]
-    uint64_t* k_empty = bars + kDecStages;               // [stages] S of the unit done
-    uint64_t* v_full = bars + 2 * kDecStages;            // [stages]
-    uint64_t* v_empty = bars + 3 * kDecStages;           // [stages] PV of the unit done
-    uint64_t* slot_ready = bars + 4 * kDecStages;        // [slots] query tile filled, slot's O_c read
+    uint64_t* k_empty = bars + kDecStagesK;              // [K stages] S of the unit done
+    uint64_t* v_full = bars + 2 * kDecStagesK;           // [V stages]
+    uint64_t* v_empty = v_full + kDecStagesV;            // [V stages] PV of the unit done
+    uint64_t* slot_ready = v_empty + kDecStagesV;        // [slots] query tile filled, slot's O_c read
     uint64_t* s_full = slot_ready + kDecSlots;           // [slots]
     uint64_t* p_full = s_full + kDecSlots;               // [slots]
     uint64_t* o_full = p_full + kDecSlots;               // [slots]
@@ -793,9 +797,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
     int* err = a.err;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kDecStages; ++i) {
+        for (int i = 0; i < kDecStagesK; ++i) {
             ptx::mbar_init(&k_full[i], 1);
             ptx::mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < kDecStagesV; ++i) {
             ptx::mbar_init(&v_full[i], 1);
             ptx::mbar_init(&v_empty[i], 1);
         }
@@ -824,12 +830,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             uint64_t* full = is_k ? k_full : v_full;
             uint64_t* empty = is_k ? k_empty : v_empty;
             uint8_t* ring = sm + (is_k ? D_OFF_K : D_OFF_V);
+            const int n_st = is_k ? kDecStagesK : kDecStagesV;
             ptx::prefetch_tmap(map);
             bool waited = false;
             int issued = 0;
             for (int i = 0; i < n_iter; ++i, ++issued) {
-                const int st = i % kDecStages;
-                if (i >= kDecStages && !ptx::mbar_wait(&empty[st], ((i / kDecStages) - 1) & 1, err)) break;
+                const int st = i % n_st;
+                if (i >= n_st && !ptx::mbar_wait(&empty[st], ((i / n_st) - 1) & 1, err)) break;
                 const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
                 if (!waited && d.c == n_total - 1) {   // this chunk holds the row the QKV step writes
                     ptx::griddep_wait();
@@ -843,18 +850,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             }
             // no copy may still be landing when the CTA exits (it has landed already
             // unless a wait above gave up)
-            for (int i = max(0, issued - kDecStages); i < issued; ++i)
-                ptx::mbar_wait_drain(&full[i % kDecStages], (i / kDecStages) & 1);
+            for (int i = max(0, issued - n_st); i < issued; ++i)
+                ptx::mbar_wait_drain(&full[i % n_st], (i / n_st) & 1);
         }
     } else if (warp == kDecSlots + 1) {
         // ------------------------------------------------------------------ MMA issuer: S(i), then PV(i-1)
         if (lane == 0) {
             auto issue_pv = [&](int j) -> bool {
-                const int slot = j % kDecSlots, st = j % kDecStages;
+                const int slot = j % kDecSlots, st = j % kDecStagesV;
                 if (!ptx::mbar_wait(&p_full[slot], (j / kDecSlots) & 1, err)) return false;
                 ptx::tc_fence_after();
                 const uint32_t p_addr = ptx::smem_u32(sm + D_OFF_P + slot * 2048);
-                if (!ptx::mbar_wait(&v_full[st], (j / kDecStages) & 1, err)) return false;
+                if (!ptx::mbar_wait(&v_full[st], (j / kDecStagesV) & 1, err)) return false;
                 const uint32_t v_addr = ptx::smem_u32(sm + D_OFF_V + st * 2 * kSub);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
@@ -866,8 +873,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             };
             bool ok = true;
             for (int i = 0; i < n_iter && ok; ++i) {
-                const int slot = i % kDecSlots, st = i % kDecStages;
-                if (!ptx::mbar_wait(&k_full[st], (i / kDecStages) & 1, err)) { ok = false; break; }
+                const int slot = i % kDecSlots, st = i % kDecStagesK;
+                if (!ptx::mbar_wait(&k_full[st], (i / kDecStagesK) & 1, err)) { ok = false; break; }
                 if (!ptx::mbar_wait(&slot_ready[slot], (i / kDecSlots) & 1, err)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t q_addr = ptx::smem_u32(sm + D_OFF_Q + slot * 2048);
@@ -938,7 +945,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
         if (slot < n_iter) prepare(slot);
         for (int i = slot, k = 0; i < n_iter; i += kDecSlots, ++k) {
             const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
-            const int st = i % kDecStages;
+            const int st = i % kDecStagesV;   // the unit's V stage
             if (ok) ok = ptx::mbar_wait(&s_full[slot], k & 1, err);
             ptx::tc_fence_after();
             const int jmax = min(kAttnChunk - 1, pos - d.c * kAttnChunk);   // the same for every row
@@ -959,7 +966,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             // value rows past the position hold anything (NaN included): zero them once
             // the chunk's V has landed
             if (d.c == n_total - 1) {
-                if (ok) ok = ptx::mbar_wait(&v_full[st], (i / kDecStages) & 1, err);
+                if (ok) ok = ptx::mbar_wait(&v_full[st], (i / kDecStagesV) & 1, err);
 #pragma unroll
                 for (int r4 = 0; r4 < 4; ++r4) {
                     const int vr = lane + 32 * r4;
