@@ -714,17 +714,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // 0, so the MMA's 128 rows repeat rows 0..7: TMEM lane 8g + r holds row r for
 // every g, and all 32 lanes of a warp's lane quarter see the 8 rows.  A softmax
 // warp therefore works on (row r = lane % 8, key quarter g = lane / 8) straight
-// from TMEM.  Four TMEM slots (S and then O_c of one unit share a slot's 128
-// columns) and four softmax warps take units in turn; the MMA thread issues
-// S of unit i before PV of unit i-1.  K and V stream through separate TMA
-// rings: K is released as soon as S has read it (two stages), V only after PV,
-// which follows the unit's softmax (four stages, one per slot).
-// Warps: 0..3 = softmax + partial store of slots 0..3, 4 = K producer,
-// 5 = TMEM owner + MMA issuer, 6 = V producer.
-constexpr int kDecSlots = 4;
+// from TMEM.  Three TMEM slots (S and then O_c of one unit share a slot's 128
+// columns) and three softmax warps take units in turn; the MMA thread issues
+// S of unit i before PV of unit i-1.  K and V stream through separate
+// three-stage TMA rings: K is released as soon as S has read it, V after PV,
+// which follows the unit's softmax.  (Four slots with a 2-stage K ring and a
+// 4-stage V ring, in the same shared memory, measured no faster.)
+// Warps: 0..2 = softmax + partial store of slots 0..2, 3 = K producer,
+// 4 = TMEM owner + MMA issuer, 5 = V producer.
+constexpr int kDecSlots = 3;
 constexpr int kDecThreads = 32 * (kDecSlots + 3);
-constexpr int kDecStagesK = 2;   // K is released as soon as S has read it
-constexpr int kDecStagesV = 4;   // V is held until PV, after the softmax of its unit
+constexpr int kDecStagesK = 3;   // K is released as soon as S has read it
+constexpr int kDecStagesV = 3;   // V is held until PV, after the softmax of its unit
 constexpr int D_OFF_Q = 0;                              // [slot][half] 1 KB each
 constexpr int D_OFF_P = 8192;                           // [slot][half] 1 KB each
 constexpr int D_OFF_K = 16384;                          // [stage] K: 2 sub-tiles
