@@ -708,6 +708,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 }
 
 // ----------------------------------------------------------------------------- decode
+// One TMA copy of a whole 128-key chunk of K or V: the cache viewed as
+// [2 halves of 64 columns][rows][64] (strides 128 B and 256 B), box [2][128][64],
+// lands as the two 16 KB sub-tiles [half][row][64] the MMA reads.
+__device__ __forceinline__ void tma_load_chunk(void* dst, const CUtensorMap* map, uint64_t* bar, int row) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(ptx::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_u32(bar)), "r"(0), "r"(row), "r"(0)
+        : "memory");
+}
+
 // Persistent decode attention for groups of n_rep <= 8 query heads.  The work
 // units are (sequence, KV head, chunk); CTA i walks a contiguous range of them.
 // Query and P tiles hold 8 rows; their descriptors use an 8-row-group stride of
@@ -846,8 +857,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
                 const int row = (d.b * a.n_kv_heads + d.g) * a.kv_seq + d.c * kAttnChunk;
                 uint8_t* dst = ring + st * 2 * kSub;
                 ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
-                ptx::tma_load_2d(dst, map, &full[st], 0, row);
-                ptx::tma_load_2d(dst + kSub, map, &full[st], 64, row);
+                tma_load_chunk(dst, map, &full[st], row);
             }
             // no copy may still be landing when the CTA exits (it has landed already
             // unless a wait above gave up)
@@ -1013,7 +1023,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
     }
 }
 
-bool make_tmap_q3d(CUtensorMap* map, const void* q, int n_heads, int tokens, int n_rep, int tq) {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* p = nullptr;
@@ -1021,9 +1031,28 @@ bool make_tmap_q3d(CUtensorMap* map, const void* q, int n_heads, int tokens, int
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
                 cudaSuccess ||
             qr != cudaDriverEntryPointSuccess)
-            return false;
+            return nullptr;
         fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
+    return fn;
+}
+
+// K or V cache [rows][128] bf16 as [2][rows][64] (see tma_load_chunk).
+bool make_tmap_kv_chunk(CUtensorMap* map, const void* base, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, rows, 2};
+    cuuint64_t strides[2] = {128 * 2, 64 * 2};
+    cuuint32_t box[3] = {64, 128, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_q3d(CUtensorMap* map, const void* q, int n_heads, int tokens, int n_rep, int tq) {
+    auto fn = encode_fn();
+    if (!fn) return false;
     cuuint64_t dims[3] = {128, (cuuint64_t)n_heads, (cuuint64_t)tokens};
     cuuint64_t strides[2] = {128 * 2, (cuuint64_t)n_heads * 128 * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)n_rep, (cuuint32_t)tq};
@@ -1097,6 +1126,9 @@ cudaError_t launch_attention_tc_decode(const AttnArgs& a, int chunks_per_cta, cu
         return cudaErrorInvalidValue;
     const int n_rep = a.n_heads / a.n_kv_heads;
     if (n_rep <= 8) {
+        // one copy per 128-key chunk of K or V
+        if (!make_tmap_kv_chunk(&mk, a.kc, cache_rows) || !make_tmap_kv_chunk(&mv, a.vc, cache_rows))
+            return cudaErrorInvalidValue;
         // persistent: one CTA per SM (units assigned on the device from the position)
         static const int n_sm = device_sm_count();
         const long max_units = (long)a.batch * a.n_kv_heads * a.n_chunks;
