@@ -711,11 +711,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // One TMA copy of a whole 128-key chunk of K or V: the cache viewed as
 // [2 halves of 64 columns][rows][64] (strides 128 B and 256 B), box [2][128][64],
 // lands as the two 16 KB sub-tiles [half][row][64] the MMA reads.
-__device__ __forceinline__ void tma_load_chunk(void* dst, const CUtensorMap* map, uint64_t* bar, int row) {
+// The cache is read once per step: evict-first, so that streaming it does not
+// push out of L2 the small buffers the step's kernels hand to one another (the
+// chunk partials, activations, segment results).  Measured 2.4 us faster per
+// 8B batch-32 decode step than the default policy.
+__device__ __forceinline__ void tma_load_chunk(void* dst, const CUtensorMap* map, uint64_t* bar, int row,
+                                               uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(ptx::smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_u32(bar)), "r"(0), "r"(row), "r"(0)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(ptx::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(ptx::smem_u32(bar)), "r"(0), "r"(row), "r"(0), "l"(policy)
         : "memory");
 }
 
@@ -844,6 +849,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             uint8_t* ring = sm + (is_k ? D_OFF_K : D_OFF_V);
             const int n_st = is_k ? kDecStagesK : kDecStagesV;
             ptx::prefetch_tmap(map);
+            const uint64_t pol = ptx::policy_evict_first();
             bool waited = false;
             int issued = 0;
             for (int i = 0; i < n_iter; ++i, ++issued) {
@@ -857,7 +863,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
                 const int row = (d.b * a.n_kv_heads + d.g) * a.kv_seq + d.c * kAttnChunk;
                 uint8_t* dst = ring + st * 2 * kSub;
                 ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
-                tma_load_chunk(dst, map, &full[st], row);
+                tma_load_chunk(dst, map, &full[st], row, pol);
             }
             // no copy may still be landing when the CTA exits (it has landed already
             // unless a wait above gave up)
