@@ -93,4 +93,85 @@ __device__ __forceinline__ void epi_store(const GemmKArgs& a, int tile, int row,
     }
 }
 
+// The fused epilogue of CPT consecutive columns (tokens n0 .. n0 + CPT - 1) of one
+// accumulator row (feature row `row` of tile `tile`); columns >= M are skipped.
+// What the epilogue reads -- the position, the RoPE factors, the residual -- is
+// loaded for a chunk of columns before that chunk's stores: the outputs may
+// alias the inputs as far as the compiler knows, so a load per column after the
+// previous column's store costs one memory round trip per column.  Per element
+// the arithmetic is epi_store's.
+template <int EPI, int CPT>
+__device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int row, int n0, const float (&acc)[CPT],
+                                               const float (&acc_up)[CPT]) {
+    const GemmEpi& e = a.e;
+    const int f = tile * kTileF + row;
+    if constexpr (EPI == EPI_QKV) {
+        constexpr int CH = CPT < 4 ? CPT : 4;
+        int kind, head;
+        if (tile < a.q_tiles) { kind = 0; head = tile; }
+        else if (tile < a.q_tiles + a.k_tiles) { kind = 1; head = tile - a.q_tiles; }
+        else { kind = 2; head = tile - a.q_tiles - a.k_tiles; }
+        const int T = e.tokens_per_seq;
+        const int base = e.pos_dev ? *e.pos_dev : e.start_pos;
+        const int i = row >> 1;
+#pragma unroll
+        for (int c0 = 0; c0 < CPT; c0 += CH) {
+            float cs[CH], sn[CH];
+            if (kind < 2) {
+#pragma unroll
+                for (int j = 0; j < CH; ++j) {
+                    const int n = n0 + c0 + j;
+                    const int pos = base + (n - (n / T) * T);
+                    const int pc = (pos >= 0 && pos < e.max_pos) ? pos : 0;
+                    cs[j] = __ldg(e.cos_tab + (size_t)pc * kRopeMaxPairs + i);
+                    sn[j] = __ldg(e.sin_tab + (size_t)pc * kRopeMaxPairs + i);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const int n = n0 + c0 + j;
+                const int b = n / T, t = n - b * T;
+                const int pos = base + t;
+                const bool pos_ok = (pos >= 0) && (pos < e.max_pos);
+                float v = bf16_round(acc[c0 + j]);
+                if (kind < 2) {
+                    const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+                    v = rope_rotate_elem(v, other, cs[j], sn[j], (row & 1) != 0);
+                }
+                if (n >= a.M) continue;
+                if (!pos_ok) {
+                    record_error(e.err, LLAMA_ERR_POS_RANGE);
+                    continue;
+                }
+                const bf16 r = __float2bfloat16_rn(v);
+                if (kind == 0) {
+                    e.out[(size_t)n * (e.n_heads * 128) + head * 128 + row] = r;
+                } else {
+                    bf16* dst = (kind == 1) ? e.kc : e.vc;
+                    dst[(((size_t)b * e.n_kv_heads + head) * e.kv_seq + pos) * 128 + row] = r;
+                }
+            }
+        }
+    } else if constexpr (EPI == EPI_RESID) {
+        constexpr int CH = CPT < 8 ? CPT : 8;
+#pragma unroll
+        for (int c0 = 0; c0 < CPT; c0 += CH) {
+            float x[CH];
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const int n = n0 + c0 + j;
+                x[j] = n < a.M ? __bfloat162float(e.resid[(size_t)n * a.F + f]) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const int n = n0 + c0 + j;
+                if (n < a.M) e.out[(size_t)n * a.F + f] = __float2bfloat16_rn(epi_resid(x[j], acc[c0 + j]));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) epi_store<EPI>(a, tile, row, n0 + j, acc[j], acc_up[j], n0 + j < a.M);
+    }
+}
+
 }  // namespace llama

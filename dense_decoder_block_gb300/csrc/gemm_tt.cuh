@@ -220,14 +220,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
             }
-            if (ok) {
-                const int ncol0 = n * BN + cg * CPT;
-#pragma unroll
-                for (int j = 0; j < CPT; ++j) {
-                    const int col = ncol0 + j;
-                    epi_store<EPI>(a, m, row, col, acc[0][j], acc[NACC - 1][j], col < a.M);
-                }
-            }
+            if (ok) epi_store_cols<EPI, CPT>(a, m, row, n * BN + cg * CPT, acc[0], acc[NACC - 1]);
         }
     }
 

@@ -196,13 +196,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 continue;
             }
-            if (ok) {
-#pragma unroll
-                for (int j = 0; j < CPT; ++j) {
-                    const int n = ncol0 + j;
-                    epi_store<EPI>(a, tile, row, n, acc[0][j], acc[NACC - 1][j], n < a.M);
-                }
-            }
+            if (ok) epi_store_cols<EPI, CPT>(a, tile, row, ncol0, acc[0], acc[NACC - 1]);
         }
     }
 
