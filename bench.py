@@ -360,7 +360,7 @@ def run_prefill(args, rank, world, device):
             "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
             "stage_tflops": {k: round(v / (stage_ms[k] / 1e3) / 1e12, 1)
                              for k, v in prefill_stage_flops(dims, 1, T).items()},
-            "gpu_launches": args.steps * 7}
+            "gpu_launches": args.steps * blk_launches_per_prefill()}
 
 
 def run_stack(args, rank, world, device):
@@ -454,8 +454,14 @@ def run_stack(args, rank, world, device):
                         "frac_of_bf16_peak": round(pre_flops / (pre_ms / 1e3) / 1e12 / bf16_peak, 4),
                         "peak_tflops": bf16_peak, "peak_kind": peak_kind + " (sustained)"},
             "clocks": sampler.summary(),
-            "gpu_launches": steps * (2 + L * blk_launches_per_decode() + 3) + (n_pre + 1) * (1 + L * 7 + 3),
+            "gpu_launches": steps * (2 + L * blk_launches_per_decode() + 3) + (n_pre + 1) * (1 + L * blk_launches_per_prefill() + 3),
             "launch": "one CUDA graph per decode step (embedding, 32 blocks, head, position update)"}
+
+
+def blk_launches_per_prefill():
+    # rmsnorm_1; qkv projection + in-place RoPE; attention; o projection; rmsnorm_2;
+    # gate/up; down (token-tiled projections apply their epilogues themselves)
+    return 8
 
 
 def blk_launches_per_decode():

@@ -243,7 +243,15 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         eq.sin_tab = b->sin_tab;
         eq.err = b->err_dev;
         const GemmProblem pq = problem_qkv(b, M, w.xn);
+        // The token-tiled (prefill) QKV stores q and k unrotated and a vectorised
+        // kernel rotates them in place: the per-column table loads of a fused RoPE
+        // kept that projection's epilogue warps behind its MMAs.
+        eq.rope_later = pick_gemm_path(pq, PATH_AUTO) == PATH_TOKEN_TILED;
         LLAMA_TRY(launch_gemm(pq, eq, PATH_AUTO, w.gemm_partial, s), "qkv");
+        if (eq.rope_later)
+            LLAMA_TRY(launch_rope_inplace(w.q, kv->k, M, T, d.n_heads, d.n_kv_heads, kv->max_seq, start_pos, pos_dev,
+                                          max_pos, b->cos_tab, b->sin_tab, b->err_dev, s),
+                      "qkv_rope");
         if (gemm_needs_reduce(pq, PATH_AUTO)) LLAMA_TRY(reduce(pq, eq, EPI_QKV), "qkv_reduce");
         // 3. attention (tensor cores when the group size divides 128; one choice per handle)
         mark();

@@ -114,10 +114,11 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
         const int T = e.tokens_per_seq;
         const int base = e.pos_dev ? *e.pos_dev : e.start_pos;
         const int i = row >> 1;
+        const bool rope = kind < 2 && !e.rope_later;   // warp-uniform
 #pragma unroll
         for (int c0 = 0; c0 < CPT; c0 += CH) {
             float cs[CH], sn[CH];
-            if (kind < 2) {
+            if (rope) {
 #pragma unroll
                 for (int j = 0; j < CH; ++j) {
                     const int n = n0 + c0 + j;
@@ -134,7 +135,7 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
                 const int pos = base + t;
                 const bool pos_ok = (pos >= 0) && (pos < e.max_pos);
                 float v = bf16_round(acc[c0 + j]);
-                if (kind < 2) {
+                if (rope) {
                     const float other = __shfl_xor_sync(0xffffffffu, v, 1);
                     v = rope_rotate_elem(v, other, cs[j], sn[j], (row & 1) != 0);
                 }

@@ -30,6 +30,7 @@ struct GemmEpi {
     int max_pos = 0;                                // positions must be < max_pos
     const float* cos_tab = nullptr;                 // [max_pos, 64]
     const float* sin_tab = nullptr;
+    bool rope_later = false;                        // QKV: store q, k unrotated (launch_rope_inplace follows)
     int* err = nullptr;
 };
 
@@ -110,6 +111,13 @@ cudaError_t launch_attention_combine(const AttnArgs& a, cudaStream_t s);
 bool attention_tc_supported(int n_heads, int n_kv_heads, int head_dim);
 cudaError_t launch_attention_tc_prefill(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attention_tc_decode(const AttnArgs& a, int chunks_per_cta, cudaStream_t s);
+
+// RoPE in place on the bf16 q rows [M, n_heads * 128] and on the cache rows of
+// the M tokens (token n = (b, t) at position base + t, base = *pos_dev or
+// start_pos): what the QKV epilogue does when it stores q and k unrotated.
+cudaError_t launch_rope_inplace(void* q, void* kc, int M, int T, int n_heads, int n_kv_heads, int kv_seq,
+                                int start_pos, const int* pos_dev, int max_pos, const float* cos_tab,
+                                const float* sin_tab, int* err, cudaStream_t s);
 
 // fp32 SIMT block pieces
 cudaError_t launch_linear_f32(const float* x, const float* w, const float* w2, const float* resid, float* y, int M,

@@ -148,6 +148,46 @@ __global__ void k_rope_append_f32(const float* __restrict__ qr, const float* __r
     }
 }
 
+// RoPE in place on bf16 rows of 128 (q rows, then the cache rows of k): one
+// thread per 8 elements (4 pairs) -- a 16-byte load, rope_rotate_elem on the bf16
+// values (the inputs the fused epilogue rotates), a 16-byte store.
+__global__ void __launch_bounds__(256) k_rope_inplace(bf16* __restrict__ q, bf16* __restrict__ kc, int M, int T,
+                                                      int n_heads, int n_kv_heads, int kv_seq, int start_pos,
+                                                      const int* pos_dev, int max_pos,
+                                                      const float* __restrict__ cos_tab,
+                                                      const float* __restrict__ sin_tab, int* err) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int per_tok = (n_heads + n_kv_heads) * 16;   // 16 eight-element groups per 128-wide row
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)M * per_tok) return;
+    const int n = (int)(idx / per_tok), r = (int)(idx - (long long)n * per_tok);
+    const int head = r >> 4, g8 = r & 15;
+    const int b = n / T, t = n - b * T;
+    const int pos = (pos_dev ? *pos_dev : start_pos) + t;
+    if (pos < 0 || pos >= max_pos) {
+        record_error(err, LLAMA_ERR_POS_RANGE);
+        return;
+    }
+    bf16* row = head < n_heads ? q + (size_t)n * n_heads * 128 + (size_t)head * 128
+                               : kc + (((size_t)b * n_kv_heads + (head - n_heads)) * kv_seq + pos) * 128;
+    uint4* p = reinterpret_cast<uint4*>(row + g8 * 8);
+    uint4 u = *p;
+    const float4 c = *reinterpret_cast<const float4*>(cos_tab + (size_t)pos * kRopeMaxPairs + g8 * 4);
+    const float4 sn = *reinterpret_cast<const float4*>(sin_tab + (size_t)pos * kRopeMaxPairs + g8 * 4);
+    const float cv[4] = {c.x, c.y, c.z, c.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+        const float a0 = __low2float(pr), a1 = __high2float(pr);
+        const __nv_bfloat162 o = __floats2bfloat162_rn(rope_rotate_elem(a0, a1, cv[k], sv[k], false),
+                                                       rope_rotate_elem(a1, a0, cv[k], sv[k], true));
+        w[k] = *reinterpret_cast<const uint32_t*>(&o);
+    }
+    *p = u;
+}
+
 template <typename T>
 __global__ void k_embed(const int32_t* __restrict__ ids, const T* __restrict__ w, T* __restrict__ x, int vocab,
                         int d, int32_t* err) {
@@ -214,6 +254,16 @@ cudaError_t launch_rope_append_f32(const float* qkv_q, const float* qkv_k, const
     k_rope_append_f32<<<M, 256, 0, s>>>(qkv_q, qkv_k, qkv_v, q_out, kc, vc, T, n_heads, n_kv_heads, head_dim, kv_seq,
                                         start_pos, pos_dev, max_pos, cos_tab, sin_tab, err);
     return cudaGetLastError();
+}
+
+cudaError_t launch_rope_inplace(void* q, void* kc, int M, int T, int n_heads, int n_kv_heads, int kv_seq,
+                                int start_pos, const int* pos_dev, int max_pos, const float* cos_tab,
+                                const float* sin_tab, int* err, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    const long long threads = (long long)M * (n_heads + n_kv_heads) * 16;
+    const dim3 grid((unsigned)((threads + 255) / 256));
+    return launch_pdl(k_rope_inplace, grid, dim3(256), 0, s, (bf16*)q, (bf16*)kc, M, T, n_heads, n_kv_heads,
+                      kv_seq, start_pos, pos_dev, max_pos, cos_tab, sin_tab, err);
 }
 
 cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, int d, void* x, int32_t* err,
