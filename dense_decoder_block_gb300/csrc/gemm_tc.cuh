@@ -105,6 +105,7 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
                                                const float (&acc_up)[CPT]) {
     const GemmEpi& e = a.e;
     const int f = tile * kTileF + row;
+    const int n_valid = a.M - n0;   // columns j < n_valid are tokens of the call
     if constexpr (EPI == EPI_QKV) {
         constexpr int CH = CPT < 4 ? CPT : 4;
         int kind, head;
@@ -115,23 +116,47 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
         const int base = e.pos_dev ? *e.pos_dev : e.start_pos;
         const int i = row >> 1;
         const bool rope = kind < 2 && !e.rope_later;   // warp-uniform
+        // token n0 + j = (sequence b, index t), advanced column by column
+        int b = n0 / T, t = n0 - b * T;
+        const size_t q_stride = (size_t)e.n_heads * 128;
+        bf16* qp = e.out + (size_t)n0 * q_stride + head * 128 + row;   // kind 0
+        bf16* cp = ((kind == 1) ? e.kc : e.vc) + (size_t)head * e.kv_seq * 128 + row;   // kinds 1, 2
+        const size_t seq_stride = (size_t)e.n_kv_heads * e.kv_seq * 128;
+        if (!rope && base >= 0 && base + T <= e.max_pos) {
+            // Every position of the call is valid and nothing is rotated here: short
+            // straight-line stores (bf16(bf16_round(x)) == bf16(x)).  The general
+            // loop below would keep a large unrolled body in the instruction cache.
+            if (kind == 0) {
+#pragma unroll
+                for (int j = 0; j < CPT; ++j)
+                    if (j < n_valid) qp[(size_t)j * q_stride] = __float2bfloat16_rn(acc[j]);
+            } else {
+                bf16* dst = cp + (size_t)b * seq_stride + (size_t)(base + t) * 128;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    if (j < n_valid) *dst = __float2bfloat16_rn(acc[j]);
+                    dst += 128;
+                    if (++t == T) { t = 0; ++b; dst = cp + (size_t)b * seq_stride + (size_t)base * 128; }
+                }
+            }
+            return;
+        }
 #pragma unroll
         for (int c0 = 0; c0 < CPT; c0 += CH) {
             float cs[CH], sn[CH];
             if (rope) {
+                int bb = b, tt = t;
 #pragma unroll
                 for (int j = 0; j < CH; ++j) {
-                    const int n = n0 + c0 + j;
-                    const int pos = base + (n - (n / T) * T);
+                    const int pos = base + tt;
                     const int pc = (pos >= 0 && pos < e.max_pos) ? pos : 0;
                     cs[j] = __ldg(e.cos_tab + (size_t)pc * kRopeMaxPairs + i);
                     sn[j] = __ldg(e.sin_tab + (size_t)pc * kRopeMaxPairs + i);
+                    if (++tt == T) { tt = 0; ++bb; }
                 }
             }
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
-                const int n = n0 + c0 + j;
-                const int b = n / T, t = n - b * T;
                 const int pos = base + t;
                 const bool pos_ok = (pos >= 0) && (pos < e.max_pos);
                 float v = bf16_round(acc[c0 + j]);
@@ -139,35 +164,31 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
                     const float other = __shfl_xor_sync(0xffffffffu, v, 1);
                     v = rope_rotate_elem(v, other, cs[j], sn[j], (row & 1) != 0);
                 }
-                if (n >= a.M) continue;
-                if (!pos_ok) {
-                    record_error(e.err, LLAMA_ERR_POS_RANGE);
-                    continue;
+                if (c0 + j < n_valid) {
+                    if (!pos_ok) {
+                        record_error(e.err, LLAMA_ERR_POS_RANGE);
+                    } else {
+                        const bf16 r = __float2bfloat16_rn(v);
+                        if (kind == 0) qp[(size_t)(c0 + j) * q_stride] = r;
+                        else cp[(size_t)b * seq_stride + (size_t)pos * 128] = r;
+                    }
                 }
-                const bf16 r = __float2bfloat16_rn(v);
-                if (kind == 0) {
-                    e.out[(size_t)n * (e.n_heads * 128) + head * 128 + row] = r;
-                } else {
-                    bf16* dst = (kind == 1) ? e.kc : e.vc;
-                    dst[(((size_t)b * e.n_kv_heads + head) * e.kv_seq + pos) * 128 + row] = r;
-                }
+                if (++t == T) { t = 0; ++b; }
             }
         }
     } else if constexpr (EPI == EPI_RESID) {
         constexpr int CH = CPT < 8 ? CPT : 8;
+        const size_t F = a.F;
+        const bf16* rp = e.resid + (size_t)n0 * F + f;
+        bf16* op = e.out + (size_t)n0 * F + f;
 #pragma unroll
         for (int c0 = 0; c0 < CPT; c0 += CH) {
             float x[CH];
 #pragma unroll
-            for (int j = 0; j < CH; ++j) {
-                const int n = n0 + c0 + j;
-                x[j] = n < a.M ? __bfloat162float(e.resid[(size_t)n * a.F + f]) : 0.f;
-            }
+            for (int j = 0; j < CH; ++j) x[j] = c0 + j < n_valid ? __bfloat162float(rp[(c0 + j) * F]) : 0.f;
 #pragma unroll
-            for (int j = 0; j < CH; ++j) {
-                const int n = n0 + c0 + j;
-                if (n < a.M) e.out[(size_t)n * a.F + f] = __float2bfloat16_rn(epi_resid(x[j], acc[c0 + j]));
-            }
+            for (int j = 0; j < CH; ++j)
+                if (c0 + j < n_valid) op[(c0 + j) * F] = __float2bfloat16_rn(epi_resid(x[j], acc[c0 + j]));
         }
     } else {
 #pragma unroll
