@@ -33,24 +33,42 @@ static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUten
     return launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, a0, a1, a2, mb, k);
 }
 
+template <int BN>
+static cudaError_t dispatch_tt(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
+                               const CUtensorMap& a1, const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
+    switch (ka.e.kind) {
+        case EPI_QKV: return run_tt<BN, false, EPI_QKV>(p, ka, a0, a1, a2, x, s);
+        case EPI_RESID: return run_tt<BN, false, EPI_RESID>(p, ka, a0, a1, a2, x, s);
+        case EPI_PLAIN: return run_tt<BN, false, EPI_PLAIN>(p, ka, a0, a1, a2, x, s);
+        case EPI_LOGITS: return run_tt<BN, false, EPI_LOGITS>(p, ka, a0, a1, a2, x, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Token-block width of a single-accumulator projection: 256 (the higher
+// arithmetic intensity per loaded byte) unless 128-token tiles give a clearly
+// shorter schedule -- waves of tiles over the SMs times the tile's MMA length,
+// at least 20% shorter -- as when 256-token tiles would leave SMs idle (few
+// tokens); a few percent of span does not pay for the lower intensity (QKV at
+// 8192 tokens measured 1001 TFLOP/s at 128 against 1226 at 256).  The
+// per-element result does not depend on the width.
+static int tt_width(const GemmProblem& p) {
+    const long n_sm = device_sm_count();
+    const long ft = p.F / kTileF;
+    auto span = [&](long bn) {
+        const long tiles = ft * ((p.M + bn - 1) / bn);
+        return ((tiles + n_sm - 1) / n_sm) * bn;
+    };
+    return 5 * span(128) <= 4 * span(256) ? 128 : 256;
+}
+
 cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
                                const CUtensorMap& a1, const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
     if (p.dual) {
         if (ka.e.kind != EPI_SWIGLU) return cudaErrorInvalidValue;
         return run_tt<128, true, EPI_SWIGLU>(p, ka, a0, a1, a2, x, s);
     }
-    switch (ka.e.kind) {
-        case EPI_QKV:
-            return run_tt<256, false, EPI_QKV>(p, ka, a0, a1, a2, x, s);
-        case EPI_RESID:
-            return run_tt<256, false, EPI_RESID>(p, ka, a0, a1, a2, x, s);
-        case EPI_PLAIN:
-            return run_tt<256, false, EPI_PLAIN>(p, ka, a0, a1, a2, x, s);
-        case EPI_LOGITS:
-            return run_tt<256, false, EPI_LOGITS>(p, ka, a0, a1, a2, x, s);
-        default:
-            return cudaErrorInvalidValue;
-    }
+    return tt_width(p) == 128 ? dispatch_tt<128>(p, ka, a0, a1, a2, x, s) : dispatch_tt<256>(p, ka, a0, a1, a2, x, s);
 }
 
 }  // namespace llama
