@@ -462,10 +462,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
 
-    const int g = blockIdx.y, b = blockIdx.z;
+    // blockIdx.x = (sequence, KV head), blockIdx.y = query tile from the last: CTAs are
+    // dispatched in linear order, so every group's longest tiles go first
+    const int g = blockIdx.x % a.n_kv_heads, b = blockIdx.x / a.n_kv_heads;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int base = a.pos_dev ? *a.pos_dev : a.start_pos;
-    const int t0 = (gridDim.x - 1 - blockIdx.x) * a.tq;   // longest tiles first
+    const int t0 = (gridDim.y - 1 - blockIdx.y) * a.tq;
     const int t_last = min(t0 + a.tq, a.tokens) - 1;
     if (base < 0 || base + t_last >= a.max_pos) {
         if (threadIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
@@ -1117,7 +1119,9 @@ cudaError_t launch_attention_tc_prefill(const AttnArgs& a, cudaStream_t s) {
         if (r != cudaSuccess) return r;
         attr = true;
     }
-    dim3 grid((a.tokens + k.tq - 1) / k.tq, a.n_kv_heads, a.batch);
+    const int n_tiles = (a.tokens + k.tq - 1) / k.tq;
+    if (n_tiles > 65535) return cudaErrorInvalidValue;
+    dim3 grid(a.n_kv_heads * a.batch, n_tiles);
     return launch_pdl(k_attn_pf, grid, dim3(kPfThreads), PF_SMEM_BYTES, s, mq, mk, mv, k);
 }
 
