@@ -117,14 +117,36 @@ __device__ __forceinline__ float quarter_max_raw(const float* sv, int j0, int jm
     return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
-// Thread-per-row form for the prefill kernel, with compact code (its rolled
-// loops keep the instruction stream small enough for the instruction cache
-// while several warps run it).  Pass 1 takes the max of the raw scores; pass 2
-// walks 8-key groups of all four quarters at once, so the four quarter sums are
-// independent chains (each still adds its keys in key order).  A hidden key is
-// set to -inf before the exponential, which gives exactly p = 0.
-__device__ __forceinline__ void softmax_row_regs(uint32_t s_taddr, int jmax, float scale_log2, uint8_t* p_base,
-                                                 uint32_t p_sub_stride, int prow, float& m_out, float& l_out) {
+
+// Eight 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// D += A . B with A (M = 128 rows x K = 16, bf16 pairs packed in 8 columns, row =
+// lane) read from tensor memory and B from shared memory.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Prefill softmax of one query row (thread = row) straight from its S row in
+// TMEM, in the canonical order: max over the visible keys of the raw scores,
+// then p = bf16(2^(s c - m)) with hidden keys at -inf, l = ((L0 + L1) + L2) + L3
+// over the key quarters, each summed in ascending key order.  Keys are taken in
+// ascending blocks of 16 (block c in quarter c / 2), and block c's 16
+// probabilities, packed as bf16 pairs, overwrite columns 8c .. 8c+7 of the S row
+// -- columns whose scores (keys 8c .. 8c+7, block c / 2) were read already.  P
+// then occupies columns 0..63, the A operand of PV (no shared-memory round trip).
+__device__ __forceinline__ void softmax_row_tmem(uint32_t s_taddr, int jmax, float scale_log2, float& m_out,
+                                                 float& l_out) {
     const bool full = __all_sync(0xffffffffu, jmax >= kAttnChunk - 1);
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
@@ -145,33 +167,29 @@ __device__ __forceinline__ void softmax_row_regs(uint32_t s_taddr, int jmax, flo
     const float m_use = (jmax >= 0) ? m : 0.f;   // a row with no visible key: every p is 0
     float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-    for (int g = 0; g < 4; ++g) {   // keys 8g..8g+7 of every quarter
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ptx::tmem_ld<8>(s_taddr + q * 32 + g * 8, v + q * 8);
+    for (int c = 0; c < 8; ++c) {   // keys 16c .. 16c+15
+        float v[16];
+        ptx::tmem_ld<16>(s_taddr + c * 16, v);
         ptx::tmem_wait_ld();
         if (!full) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    if (q * 32 + g * 8 + t > jmax) v[q * 8 + t] = -INFINITY;
+            for (int t = 0; t < 16; ++t)
+                if (c * 16 + t > jmax) v[t] = -INFINITY;
         }
+        uint32_t packed[8];
+        float lc = lq[c >> 1];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t packed[4];
-#pragma unroll
-            for (int t = 0; t < 8; t += 2) {
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(softmax_p(v[q * 8 + t], scale_log2, m_use),
-                                                                softmax_p(v[q * 8 + t + 1], scale_log2, m_use));
-                lq[q] = __fadd_rn(lq[q], __low2float(pb));
-                lq[q] = __fadd_rn(lq[q], __high2float(pb));
-                packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-            }
-            *reinterpret_cast<uint4*>(p_base + (q >> 1) * p_sub_stride + sw_off(prow, (q & 1) * 4 + g)) =
-                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        for (int t = 0; t < 16; t += 2) {
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(softmax_p(v[t], scale_log2, m_use),
+                                                            softmax_p(v[t + 1], scale_log2, m_use));
+            lc = __fadd_rn(lc, __low2float(pb));
+            lc = __fadd_rn(lc, __high2float(pb));
+            packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
         }
+        lq[c >> 1] = lc;
+        tmem_st8(s_taddr + c * 8, packed);
     }
+    ptx::tmem_wait_st();
     m_out = m;
     l_out = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), lq[2]), lq[3]);
 }
@@ -435,10 +453,12 @@ static_assert(kPfRegsNeeded <= 128 * kPfThreads, "register split exceeds the lau
 constexpr int PF_OFF_Q = 0;                          // Q: 2 sub-tiles
 constexpr int PF_OFF_K = 2 * kSub;                   // [stage] K: 2 sub-tiles
 constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
-constexpr int PF_OFF_P = PF_OFF_V + 4 * kSub;        // [parity] P: 2 sub-tiles
-constexpr int PF_OFF_BAR = PF_OFF_P + 4 * kSub;
+constexpr int PF_OFF_BAR = PF_OFF_V + 4 * kSub;
 constexpr int PF_SMEM_BYTES = PF_OFF_BAR + 256 + 1024;
 constexpr int PF_TM_S = 0, PF_TM_OC = 256;   // S[parity] at 0 / 128, O_c[parity] at 256 / 384
+// In S[parity], the softmax leaves P (bf16 pairs) in columns 0..63 and the row's
+// (m, l) in columns 64, 65.
+constexpr int PF_TM_ML = 64;
 static_assert(PF_SMEM_BYTES <= 232448, "shared memory per CTA");
 
 __global__ void __launch_bounds__(kPfThreads, 1)
@@ -571,14 +591,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (i >= 2 && !ptx::mbar_wait(&oc_free[k], ((i >> 1) & 1) ^ 1, err)) break;
                     if (!ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err)) break;
                     ptx::tc_fence_after();
-                    const uint32_t p_addr = ptx::smem_u32(sm + PF_OFF_P + k * 2 * kSub);
                     const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + k * 2 * kSub);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t aoff = (ks >> 2) * kSub + (ks & 3) * 32;
-                        ptx::umma_bf16(tmem + PF_TM_OC + k * 128, ptx::sw128_kmajor_desc(p_addr + aoff),
-                                       ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < 8; ++ks)   // P of keys 16ks.. in TMEM columns 8ks..
+                        umma_bf16_ts(tmem + PF_TM_OC + k * 128, tmem + PF_TM_S + k * 128 + ks * 8,
+                                     ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
                     ptx::umma_commit(&oc_full[k]);
                     ptx::umma_commit(&v_empty[k]);
                     if (i + 2 < n_iter) ok = issue_s(i + 2);
@@ -596,7 +613,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool valid = (t_local < a.tq) && (t0 + t_local < a.tokens);
         const int pos_r = base + t0 + t_local;
         const uint32_t s_addr = tmem + lane_addr + PF_TM_S + k * 128;
-        uint8_t* p_base = sm + PF_OFF_P + k * 2 * kSub;
         bool ok = true;
         for (int i = k; i < n_iter; i += 2) {
             // s_full(i) also means PV(i - 2) -- issued before S(i) -- is done with P[k]
@@ -604,8 +620,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ptx::tc_fence_after();
             const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
             float m, l;
-            softmax_row_regs(s_addr, jmax, a.scale_log2, p_base, kSub, row, m, l);
-            ptx::tmem_st2(s_addr, m, l);
+            softmax_row_tmem(s_addr, jmax, a.scale_log2, m, l);
+            ptx::tmem_st2(s_addr + PF_TM_ML, m, l);
             ptx::tmem_wait_st();
             // value rows past the last visible key of this tile are zeroed (they may hold
             // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
@@ -641,7 +657,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (ok) ok = ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err);
             ptx::tc_fence_after();
             float ml[2];
-            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + k * 128, ml);
+            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + k * 128 + PF_TM_ML, ml);
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
             __syncwarp();
