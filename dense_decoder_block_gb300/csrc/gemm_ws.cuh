@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int n_iter = 0;
             for (int u = blockIdx.x; u < n_units; u += gridDim.x) n_iter += unit_kb1(u) - unit_kb0(u);
             const int n_pre = min(C::STAGES, n_iter);
-            int pre_kb[C::STAGES];
             int stage = 0, it = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -103,18 +102,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
                     ptx::tma_load_2d_hint(dst, mapA, &full[stage], kb * kBlockK, arow, pol_w);
                     if (DUAL) ptx::tma_load_2d_hint(dst + kABytes, &mA1, &full[stage], kb * kBlockK, arow, pol_w);
-                    if (it < n_pre) {
-                        // the weights do not depend on earlier kernels: the first stages stream
-                        // before the wait; the activations are fetched after it
-                        pre_kb[it] = kb;
-                        if (it == n_pre - 1) {
-                            ptx::griddep_wait();
-                            ptx::griddep_launch_dependents();
-                            for (int j = 0; j < n_pre; ++j)
-                                ptx::tma_load_2d(smem + j * C::STAGE_BYTES + NACC * kABytes, &mB, &full[j],
-                                                 pre_kb[j] * kBlockK, 0);
-                        }
-                    } else {
+                    // The weights do not depend on earlier kernels: the first n_pre stages
+                    // stream before the wait.  Their activations are loaded by the MMA thread
+                    // as soon as the wait returns (issuing the weight copies takes this thread
+                    // about 2 us); the stage completes only with this thread's arrival and
+                    // both copies, in whatever order they land.
+                    if (it >= n_pre) {
+                        if (it == n_pre) ptx::griddep_wait();
                         ptx::tma_load_2d(dst + NACC * kABytes, &mB, &full[stage], kb * kBlockK, 0);
                     }
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -127,6 +121,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            // first the activations of the prefetched stages (see the producer)
+            ptx::prefetch_tmap(&mB);
+            ptx::griddep_wait();
+            ptx::griddep_launch_dependents();
+            {
+                int n_iter = 0;
+                for (int u = blockIdx.x; u < n_units; u += gridDim.x) n_iter += unit_kb1(u) - unit_kb0(u);
+                const int n_pre = min(C::STAGES, n_iter);
+                int j = 0;
+                for (int u = blockIdx.x; u < n_units && j < n_pre; u += gridDim.x)
+                    for (int kb = unit_kb0(u); kb < unit_kb1(u) && j < n_pre; ++kb, ++j)
+                        ptx::tma_load_2d(smem + j * C::STAGE_BYTES + NACC * kABytes, &mB, &full[j], kb * kBlockK, 0);
+            }
             int stage = 0, use = 0;
             uint32_t phase = 0;
             bool ok = true;
