@@ -430,12 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   warp 0       TMA: the Q tile once, then K chunks through a two-stage ring
 //   warp 2       TMA: V chunks through a two-stage ring (K(i+2) loads once S(i)
 //                has read K(i); V(i+2) once PV(i) has read V(i))
-//   warp 1       TMEM owner + MMA: PV(i) into O_c[i % 2], then S(i+2) = Q K^T
-//                into the S buffer that chunk i used (S and O_c are both
-//                double-buffered in TMEM)
+//   warp 1       TMEM owner + MMA: PV(i) into O_c[i % 2] with P read from
+//                TMEM, then S(i+2) = Q K^T into the S buffer that chunk i used
+//                (S and O_c are both double-buffered in TMEM)
 //   warps 4-7    softmax of the even chunks, warps 8-11 of the odd chunks
-//                (thread = row); P goes to one of two smem tiles, the row's
-//                (m, l) to the first two columns of the S buffer it read
+//                (thread = row); P (bf16 pairs) overwrites the first 64
+//                columns of the S row it read, the row's (m, l) goes to
+//                columns 64, 65
 //   warps 12-15  fold of every chunk into the running (O, M, L), thread = row,
 //                with the row's O in registers; then o = O * (1 / L)
 // Warp 3 only keeps the roles aligned to warpgroups.  A chunk that is wholly
