@@ -93,6 +93,24 @@ __device__ __forceinline__ void epi_store(const GemmKArgs& a, int tile, int row,
     }
 }
 
+// SwiGLU of CPT consecutive features of one token, u = bf16(bf16(silu(bf16(g))) *
+// bf16(up)) (epi_swiglu), stored as 16-byte runs.
+template <int CPT>
+__device__ __forceinline__ void epi_swiglu_row(bf16* dst, const float (&g)[CPT], const float (&u)[CPT]) {
+    static_assert(CPT % 8 == 0, "16-byte runs");
+#pragma unroll
+    for (int j0 = 0; j0 < CPT; j0 += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(epi_swiglu(g[j0 + 2 * t], u[j0 + 2 * t]),
+                                                           epi_swiglu(g[j0 + 2 * t + 1], u[j0 + 2 * t + 1]));
+            w[t] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        *reinterpret_cast<uint4*>(dst + j0) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // The fused epilogue of CPT consecutive columns (tokens n0 .. n0 + CPT - 1) of one
 // accumulator row (feature row `row` of tile `tile`); columns >= M are skipped.
 // What the epilogue reads -- the position, the RoPE factors, the residual -- is

@@ -48,7 +48,12 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
     using C = TtCfg<BN, DUAL>;
     constexpr int NACC = C::NACC;
     constexpr int CPT = C::CPT;
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, BN);
+    // The gate/up pair runs with the roles swapped: the 128 tokens are the A
+    // operand and the gate and up tiles of the same 128 features, stored one after
+    // the other, one B operand of 256 rows -- one N = 256 MMA per K step instead of
+    // two N = 128 MMAs that each re-read the token tile from shared memory.
+    // Accumulator lane = token, columns 0..127 gate, 128..255 up.
+    constexpr uint32_t IDESC = DUAL ? ptx::idesc_bf16_f32(128, 2 * BN) : ptx::idesc_bf16_f32(128, BN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -167,10 +172,12 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
 #pragma unroll
                             for (int k = 0; k < kBlockK / 16; ++k) {
                                 const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                                const uint64_t bdesc = ptx::sw128_kmajor_desc(sb + 32 * k);
-                                ptx::umma_bf16(d, ptx::sw128_kmajor_desc(sa + 32 * k), bdesc, IDESC, accum);
-                                if (DUAL)
-                                    ptx::umma_bf16(d + BN, ptx::sw128_kmajor_desc(sa + kABytes + 32 * k), bdesc, IDESC, accum);
+                                if (DUAL)   // A = tokens, B = gate rows then up rows
+                                    ptx::umma_bf16(d, ptx::sw128_kmajor_desc(sb + 32 * k), ptx::sw128_kmajor_desc(sa + 32 * k),
+                                                   IDESC, accum);
+                                else        // A = weights, B = tokens
+                                    ptx::umma_bf16(d, ptx::sw128_kmajor_desc(sa + 32 * k), ptx::sw128_kmajor_desc(sb + 32 * k),
+                                                   IDESC, accum);
                             }
                             ptx::umma_commit(&empty[stage]);
                             if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -220,7 +227,15 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
             }
-            if (ok) epi_store_cols<EPI, CPT>(a, m, row, n * BN + cg * CPT, acc[0], acc[NACC - 1]);
+            if (ok) {
+                if constexpr (DUAL) {
+                    // lane = token n * BN + row, columns = features m * 128 + cg * CPT + j
+                    const int tok = n * BN + row;
+                    if (tok < a.M) epi_swiglu_row<CPT>(a.e.out + (size_t)tok * a.F + m * kTileF + cg * CPT, acc[0], acc[1]);
+                } else {
+                    epi_store_cols<EPI, CPT>(a, m, row, n * BN + cg * CPT, acc[0], acc[NACC - 1]);
+                }
+            }
         }
     }
 
