@@ -144,7 +144,8 @@ class ClockSampler:
 def kernel_source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_decoder_block_gb300", "csrc")
-    for f in ("gemm_tc.cuh", "gemm_ws.cuh", "gemm_weight_stream.cu", "ptx.cuh", "common.cuh"):
+    # the kernel and the host code that fixes its schedule (the K-segment choice)
+    for f in ("gemm_tc.cuh", "gemm_ws.cuh", "gemm_weight_stream.cu", "gemm_host.cu", "ptx.cuh", "common.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -280,6 +281,7 @@ def run_ours(args, rank, world, device):
     e2e_value = tokens / (e2e_ms / 1e3)
     assert blk.poll_error() == 0
 
+    n_launch = blk_launches(blk)
     hbm, bf16_peak, _, peak_kind = peaks()
     step_bytes = decode_step_bytes(dims, B, POS)
     gu_bytes = gateup_launch_bytes(dims, B)
@@ -318,7 +320,7 @@ def run_ours(args, rank, world, device):
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 1), "unit": "tok/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": y.numel() * y.element_size()},
-        "gpu_launches": args.steps * blk_launches_per_decode(),
+        "gpu_launches": args.steps * n_launch,
         "launch": "one CUDA graph per step (llama_block_decode_devpos captured once)",
     }
     if args.extra and rank == 0:
@@ -347,6 +349,7 @@ def run_prefill(args, rank, world, device):
     stream = torch.cuda.current_stream(device)
     ms = time_region(lambda: blk.prefill(x, kv, y, ws), args.steps, args.warmup, stream)
     assert blk.poll_error() == 0
+    n_launch = blk_launches(blk)
     stage_ms = stage_profile(blk, lambda st: blk.prefill(x, kv, y, ws, st), device, max(3, args.steps))
     _, bf16_peak, _, peak_kind = peaks()
     fl = prefill_flops(dims, 1, T)
@@ -360,7 +363,7 @@ def run_prefill(args, rank, world, device):
             "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
             "stage_tflops": {k: round(v / (stage_ms[k] / 1e3) / 1e12, 1)
                              for k, v in prefill_stage_flops(dims, 1, T).items()},
-            "gpu_launches": args.steps * blk_launches_per_prefill()}
+            "gpu_launches": args.steps * n_launch}
 
 
 def run_stack(args, rank, world, device):
@@ -398,6 +401,7 @@ def run_stack(args, rank, world, device):
     # prefill: warm-up once, then time a few
     n_pre = 3
     pre_ms = time_region(lambda: st.prefill(ids), n_pre, 1, stream)
+    n_pre_launch = blk_launches(st.blocks[0])
     assert st.poll_error() == 0 and int(st.err.item()) == 0
     pre_flops = L * prefill_flops(dims, B, T) + 2 * B * dims.d_model * V
 
@@ -411,6 +415,7 @@ def run_stack(args, rank, world, device):
         with torch.cuda.graph(graph, stream=side):
             st.decode_step(side)
     torch.cuda.synchronize(device)
+    n_dec = blk_launches(st.blocks[0])
     st.prefill(ids)
     torch.cuda.synchronize(device)
     for _ in range(3):                         # warm-up replays, then restart from the prefill
@@ -454,20 +459,18 @@ def run_stack(args, rank, world, device):
                         "frac_of_bf16_peak": round(pre_flops / (pre_ms / 1e3) / 1e12 / bf16_peak, 4),
                         "peak_tflops": bf16_peak, "peak_kind": peak_kind + " (sustained)"},
             "clocks": sampler.summary(),
-            "gpu_launches": steps * (2 + L * blk_launches_per_decode() + 3) + (n_pre + 1) * (1 + L * blk_launches_per_prefill() + 3),
+            "gpu_launches": steps * (2 + L * n_dec + 3) + (n_pre + 1) * (1 + L * n_pre_launch + 3),
             "launch": "one CUDA graph per decode step (embedding, 32 blocks, head, position update)"}
 
 
-def blk_launches_per_prefill():
-    # rmsnorm_1; qkv projection + in-place RoPE; attention; o projection; rmsnorm_2;
-    # gate/up; down (token-tiled projections apply their epilogues themselves)
-    return 8
-
-
-def blk_launches_per_decode():
-    # rmsnorm_1; qkv projection + its segment reduction; attention chunks + combine;
-    # o projection + reduction fused with rmsnorm_2; gate/up + reduction; down + reduction
-    return 11
+def blk_launches(blk):
+    """Kernels the block's last prefill or decode call enqueued, as the library counted
+    them (8B shapes: prefill 8 -- rmsnorm_1, QKV, RoPE, attention, O, rmsnorm_2,
+    gate/up, down; decode 10 -- rmsnorm_1, QKV + reduction, attention + combine,
+    O + reduction with rmsnorm_2, gate/up in one K-segment, down + reduction)."""
+    n = blk.launch_count()
+    assert n > 0
+    return n
 
 
 STAGES = ("rmsnorm_1", "qkv", "attention", "o_proj", "rmsnorm_2", "gate_up", "down")

@@ -26,7 +26,8 @@ __all__ = [
     "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_destroy",
     "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
     "llama_block_decode_devpos",
-    "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_embed", "llama_lmhead_workspace_bytes",
+    "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_block_launch_count",
+    "llama_embed", "llama_lmhead_workspace_bytes",
     "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
 ]
 
@@ -123,6 +124,11 @@ def llama_block_set_stage_events(h, events) -> None:
         raise LlamaError(rc, "llama_block_set_stage_events")
 
 
+def llama_block_launch_count(h) -> int:
+    """Kernels enqueued by the last successful prefill/decode call on the handle."""
+    return int(lib().llama_block_launch_count(h))
+
+
 def llama_block_poll_error(h, stream=None) -> int:
     return int(lib().llama_block_poll_error(h, _stream(stream)))
 
@@ -216,3 +222,6 @@ class LlamaBlock:
 
     def poll_error(self, stream=None) -> int:
         return llama_block_poll_error(self.h, stream)
+
+    def launch_count(self) -> int:
+        return llama_block_launch_count(self.h)

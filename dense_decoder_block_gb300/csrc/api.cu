@@ -18,6 +18,7 @@ struct llama_block_s {
     float* cos_tab = nullptr;   // [max_seq, 64]
     float* sin_tab = nullptr;
     int* err_dev = nullptr;
+    int last_launches = 0;      // kernels enqueued by the last prefill/decode call
     int device = 0;
     std::string last_error;
     cudaEvent_t stage_events[LLAMA_BLOCK_STAGES + 1] = {};
@@ -174,10 +175,14 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
     w = layout(b, B, T, (uint8_t*)ws, decode);
     const int max_pos = std::min(d.max_seq, kv->max_seq);
     cudaError_t e;
+    // kernels enqueued by this call (each launcher below issues one; decode attention two)
+    int n_launch = 0;
+    b->last_launches = 0;
 #define LLAMA_TRY(call, where)                          \
     do {                                                \
         e = (call);                                     \
         if (e != cudaSuccess) return cuda_fail(b, e, where); \
+        ++n_launch;                                     \
     } while (0)
     int stage = 0;
     cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
@@ -256,11 +261,19 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         // 3. attention (tensor cores when the group size divides 128; one choice per handle)
         mark();
         if (attention_tc_supported(d.n_heads, d.n_kv_heads, d.head_dim)) {
-            if (decode) LLAMA_TRY(launch_attention_tc_decode(at, 0, s), "attention_decode");
-            else LLAMA_TRY(launch_attention_tc_prefill(at, s), "attention_prefill");
+            if (decode) {
+                LLAMA_TRY(launch_attention_tc_decode(at, 0, s), "attention_decode");
+                ++n_launch;   // and its combine
+            } else {
+                LLAMA_TRY(launch_attention_tc_prefill(at, s), "attention_prefill");
+            }
         } else {
-            if (decode) LLAMA_TRY(launch_attention_decode(at, s), "attention_decode");
-            else LLAMA_TRY(launch_attention_prefill(at, s), "attention_prefill");
+            if (decode) {
+                LLAMA_TRY(launch_attention_decode(at, s), "attention_decode");
+                ++n_launch;   // and its combine
+            } else {
+                LLAMA_TRY(launch_attention_prefill(at, s), "attention_prefill");
+            }
         }
         // 4. O projection + residual -> h, 5. RMSNorm_2 -> hn
         mark();
@@ -324,8 +337,12 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
                                          d.head_dim, kv->max_seq, start_pos, pos_dev, max_pos, b->cos_tab,
                                          b->sin_tab, b->err_dev, s),
                   "rope_append");
-        if (decode) LLAMA_TRY(launch_attention_decode(at, s), "attention_decode");
-        else LLAMA_TRY(launch_attention_prefill(at, s), "attention_prefill");
+        if (decode) {
+            LLAMA_TRY(launch_attention_decode(at, s), "attention_decode");
+            ++n_launch;   // and its combine
+        } else {
+            LLAMA_TRY(launch_attention_prefill(at, s), "attention_prefill");
+        }
         LLAMA_TRY(launch_linear_f32((const float*)w.o, (const float*)b->w.wo, nullptr, xf, (float*)w.h, M, d.d_model,
                                     qd, 1, s),
                   "o_proj");
@@ -338,6 +355,7 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
                   "down");
     }
 #undef LLAMA_TRY
+    b->last_launches = n_launch;
     return LLAMA_OK;
 }
 
@@ -539,6 +557,8 @@ extern "C" int llama_block_set_stage_events(llama_block b, void* const* events, 
     b->timing = true;
     return LLAMA_OK;
 }
+
+extern "C" int llama_block_launch_count(llama_block b) { return b ? b->last_launches : 0; }
 
 extern "C" int llama_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype,
                              void* stream) {

@@ -60,6 +60,19 @@ static int n_segments(const GemmProblem& p) {
 }
 
 int choose_seg_kb(int n_tiles, int total_kb, int n_sm) {
+    // The fewest segments whose (tile, segment) units keep at least 70% of the SMs
+    // streaming in a single wave: HBM is saturated well before every SM streams,
+    // and each extra segment costs its fp32 partials and, from two segments on, a
+    // reduction kernel (8B decode: the gate/up pair in one segment on 112 SMs and
+    // the down projection in four on 128 took the step from 120.8 to 116.8 us; two
+    // segments for QKV or three for O, 96 units each, were slower).
+    for (int s = 1; s <= total_kb; ++s) {
+        const int seg = (total_kb + s - 1) / s;
+        const long units = (long)n_tiles * ((total_kb + seg - 1) / seg);
+        if (units > n_sm) break;
+        if (10 * units >= 7L * n_sm) return seg;
+    }
+    // Otherwise the segment length with the shortest schedule of equal units.
     int best = total_kb;
     long best_span = -1;
     for (int s = 1; s <= total_kb; ++s) {

@@ -55,8 +55,9 @@ int gemm_num_segments(const GemmProblem& p);
 // (weight-streaming schedule with more than one K-segment).
 bool gemm_needs_reduce(const GemmProblem& p, int path);
 // K-segment length (in 64-element k-blocks) for a projection of n_tiles feature
-// tiles and total_kb k-blocks: the one that minimises the weight-streaming
-// makespan over n_sm SMs, at least 8 k-blocks per segment.
+// tiles and total_kb k-blocks: the fewest segments whose units fill 70-100% of
+// the n_sm SMs in one wave; failing that, the one that minimises the
+// weight-streaming makespan, at least 8 k-blocks per segment.
 int choose_seg_kb(int n_tiles, int total_kb, int n_sm);
 int device_sm_count();
 

@@ -159,6 +159,12 @@ const char* llama_block_last_error(llama_block blk);
 #define LLAMA_BLOCK_STAGES 7
 int llama_block_set_stage_events(llama_block blk, void* const* events, int n_events);
 
+/* Number of kernels the last successful prefill/decode call on this handle
+ * enqueued (0 before the first call, after a failed call, or for NULL).  It
+ * depends on the shape (the K-segment schedule fixed at create decides which
+ * projections need a reduction kernel) and on the call (decode or prefill). */
+int llama_block_launch_count(llama_block blk);
+
 /* ---------------------------------------------------------------------------
  * Stack head (32-layer generation loop): embedding gather, final RMSNorm,
  * LM head with greedy choice.  bf16 only.

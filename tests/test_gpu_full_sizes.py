@@ -35,6 +35,9 @@ def _decode_case(dims, wts, wts64, B, pos, max_seq):
     y = run_decode(blk, ddb, inp.x.to(dev), kc, vc, pos)
     torch.cuda.synchronize()
     assert blk.poll_error() == 0
+    # kernels per decode step: 8B -- the gate/up pair in one K-segment (epilogue in the
+    # projection), QKV, O and down with a reduction each; 70B -- gate/up in two segments
+    assert blk.launch_count() == (10 if dims is workloads.LLAMA3_8B else 11)
     # rows past pos were NaN and stay NaN; nothing beyond pos was read (y finite)
     if pos + 1 < max_seq:
         assert torch.isnan(kc[:, :, pos + 1:]).all()
@@ -75,6 +78,7 @@ def _prefill_case(dims, wts, wts64, T, B=1):
     y = run_prefill(blk, ddb, inp.x.to(dev), kc, vc)
     torch.cuda.synchronize()
     assert blk.poll_error() == 0
+    assert blk.launch_count() == 8   # token-tiled projections carry their epilogues
     rows = _sample_rows(T)
     kc64 = np.zeros((B, dims.n_kv_heads, max_seq, dims.head_dim))
     vc64 = np.zeros_like(kc64)
