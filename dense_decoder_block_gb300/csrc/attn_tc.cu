@@ -137,63 +137,6 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
-// Prefill softmax of one query row (thread = row) straight from its S row in
-// TMEM, in the canonical order: max over the visible keys of the raw scores,
-// then p = bf16(2^(s c - m)) with hidden keys at -inf, l = ((L0 + L1) + L2) + L3
-// over the key quarters, each summed in ascending key order.  Keys are taken in
-// ascending blocks of 16 (block c in quarter c / 2), and block c's 16
-// probabilities, packed as bf16 pairs, overwrite columns 8c .. 8c+7 of the S row
-// -- columns whose scores (keys 8c .. 8c+7, block c / 2) were read already.  P
-// then occupies columns 0..63, the A operand of PV (no shared-memory round trip).
-__device__ __forceinline__ void softmax_row_tmem(uint32_t s_taddr, int jmax, float scale_log2, float& m_out,
-                                                 float& l_out) {
-    const bool full = __all_sync(0xffffffffu, jmax >= kAttnChunk - 1);
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
-        float v[32];
-        ptx::tmem_ld<32>(s_taddr + cb * 32, v);
-        ptx::tmem_wait_ld();
-        if (full) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (cb * 32 + j <= jmax) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
-        }
-    }
-    const float m = __fmul_rn(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), scale_log2);
-    const float m_use = (jmax >= 0) ? m : 0.f;   // a row with no visible key: every p is 0
-    float lq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-    for (int c = 0; c < 8; ++c) {   // keys 16c .. 16c+15
-        float v[16];
-        ptx::tmem_ld<16>(s_taddr + c * 16, v);
-        ptx::tmem_wait_ld();
-        if (!full) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-                if (c * 16 + t > jmax) v[t] = -INFINITY;
-        }
-        uint32_t packed[8];
-        float lc = lq[c >> 1];
-#pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(softmax_p(v[t], scale_log2, m_use),
-                                                            softmax_p(v[t + 1], scale_log2, m_use));
-            lc = __fadd_rn(lc, __low2float(pb));
-            lc = __fadd_rn(lc, __high2float(pb));
-            packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-        }
-        lq[c >> 1] = lc;
-        tmem_st8(s_taddr + c * 8, packed);
-    }
-    ptx::tmem_wait_st();
-    m_out = m;
-    l_out = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), lq[2]), lq[3]);
-}
-
 // Thread-per-row form (prefill): this thread's S row is at s_taddr in TMEM.
 __device__ __forceinline__ void softmax_row(uint32_t s_taddr, int jmax, float scale_log2, uint8_t* p_base,
                                             uint32_t p_sub_stride, int prow, bool write_p, float& m_out,
@@ -433,10 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   warp 1       TMEM owner + MMA: PV(i) into O_c[i % 2] with P read from
 //                TMEM, then S(i+2) = Q K^T into the S buffer that chunk i used
 //                (S and O_c are both double-buffered in TMEM)
-//   warps 4-7    softmax of the even chunks, warps 8-11 of the odd chunks
-//                (thread = row); P (bf16 pairs) overwrites the first 64
-//                columns of the S row it read, the row's (m, l) goes to
-//                columns 64, 65
+//   warps 4-11   softmax of every chunk, two threads per row: warps 4-7 take
+//                keys 0..63 and warps 8-11 keys 64..127 of the rows of their
+//                TMEM lane quarter, exchanging the row max and two quarter sums
+//                through shared memory; P (bf16 pairs) overwrites the first 64
+//                columns of the S row once both halves hold their scores, the
+//                row's (m, l) goes to columns 64, 65.  (One warpgroup per chunk,
+//                alternating chunks, left each chunk to one warp per scheduler
+//                and the chunk time at that warp's latency.)
 //   warps 12-15  fold of every chunk into the running (O, M, L), thread = row,
 //                with the row's O in registers; then o = O * (1 / L)
 // Warp 3 only keeps the roles aligned to warpgroups.  A chunk that is wholly
@@ -447,7 +394,7 @@ constexpr int kPfThreads = 512;
 // register split (launch: 128 per thread): warpgroup 0 and the softmax give up
 // registers so that each fold thread can hold its row of O (128 floats)
 constexpr int kPfRegsCtrl = 56;
-constexpr int kPfRegsSoftmax = 104;
+constexpr int kPfRegsSoftmax = 112;
 constexpr int kPfRegsFold = 232;
 constexpr int kPfRegsNeeded = 128 * kPfRegsCtrl + 256 * kPfRegsSoftmax + 128 * kPfRegsFold;
 static_assert(kPfRegsNeeded <= 128 * kPfThreads, "register split exceeds the launch allocation");
@@ -455,12 +402,86 @@ constexpr int PF_OFF_Q = 0;                          // Q: 2 sub-tiles
 constexpr int PF_OFF_K = 2 * kSub;                   // [stage] K: 2 sub-tiles
 constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
 constexpr int PF_OFF_BAR = PF_OFF_V + 4 * kSub;
-constexpr int PF_SMEM_BYTES = PF_OFF_BAR + 256 + 1024;
+constexpr int PF_OFF_XCH = PF_OFF_BAR + 256;         // softmax halves' exchange: 4 x 128 floats
+constexpr int PF_SMEM_BYTES = PF_OFF_XCH + 2048 + 1024;
 constexpr int PF_TM_S = 0, PF_TM_OC = 256;   // S[parity] at 0 / 128, O_c[parity] at 256 / 384
 // In S[parity], the softmax leaves P (bf16 pairs) in columns 0..63 and the row's
 // (m, l) in columns 64, 65.
 constexpr int PF_TM_ML = 64;
 static_assert(PF_SMEM_BYTES <= 232448, "shared memory per CTA");
+
+// Barrier of `n` threads (whole warps) on hardware barrier `id` (1..15; 0 is
+// __syncthreads).  Every participating warp must reach it the same number of times.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Prefill softmax of one query row over one 128-key chunk, the keys split over
+// two threads (two warps of the same TMEM lane quarter): half h holds keys
+// 64h .. 64h+63 of the row's S in registers.  It computes exactly the canonical
+// softmax: the row max over the visible keys is the max of the two halves' maxima
+// (exchanged through shared memory; max is exact), p = bf16(2^(s c - m)) with
+// hidden keys at -inf, and l = ((L0 + L1) + L2) + L3 with each quarter sum in
+// ascending key order -- half 0 holds L0, L1, half 1 passes L2, L3 over.  Block c
+// (keys 16c .. 16c+15) of P, packed as bf16 pairs, goes to columns 8c .. 8c+7 of
+// the S row once both halves hold their scores in registers; half 0 writes the
+// row's (m, l) to the ML columns.  `xch` is 4 x 128 floats of shared memory; `bar`
+// the barrier id of this lane quarter.
+__device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int row, int jmax, float scale_log2,
+                                                  float* xch, int bar, float& m_out) {
+    float v[64];
+    ptx::tmem_ld<32>(s_taddr + h * 64, v);
+    ptx::tmem_ld<32>(s_taddr + h * 64 + 32, v + 32);
+    ptx::tmem_wait_ld();
+    const int jl = jmax - h * 64;   // last visible key of this half, local index
+    const bool full = __all_sync(0xffffffffu, jl >= 63);
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (full) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+            if (j <= jl) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+    }
+    xch[h * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    named_bar_sync(bar, 64);   // both halves' maxima written, both S halves read
+    const float m = __fmul_rn(fmaxf(xch[row], xch[128 + row]), scale_log2);
+    const float m_use = (jmax >= 0) ? m : 0.f;   // a row with no visible key: every p is 0
+    float lq[2] = {0.f, 0.f};
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {   // keys 64h + 16cb ..
+        float* vb = v + cb * 16;
+        if (!full) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                if (cb * 16 + t > jl) vb[t] = -INFINITY;
+        }
+        uint32_t packed[8];
+        float lc = lq[cb >> 1];
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(softmax_p(vb[t], scale_log2, m_use),
+                                                            softmax_p(vb[t + 1], scale_log2, m_use));
+            lc = __fadd_rn(lc, __low2float(pb));
+            lc = __fadd_rn(lc, __high2float(pb));
+            packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        lq[cb >> 1] = lc;
+        tmem_st8(s_taddr + (h * 4 + cb) * 8, packed);
+    }
+    if (h == 1) {
+        xch[256 + row] = lq[0];
+        xch[384 + row] = lq[1];
+    }
+    named_bar_sync(bar, 64);   // L2, L3 written; the maxima read
+    if (h == 0) {
+        const float l = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), xch[256 + row]), xch[384 + row]);
+        ptx::tmem_st2(s_taddr + PF_TM_ML, m, l);
+    }
+    ptx::tmem_wait_st();
+    m_out = m;
+}
 
 __global__ void __launch_bounds__(kPfThreads, 1)
     k_attn_pf(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
@@ -506,7 +527,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ptx::mbar_init(&v_full[i], 1);
             ptx::mbar_init(&v_empty[i], 1);
             ptx::mbar_init(&s_full[i], 1);
-            ptx::mbar_init(&p_full[i], 4);
+            ptx::mbar_init(&p_full[i], 8);
             ptx::mbar_init(&s_free[i], 4);
             ptx::mbar_init(&oc_full[i], 1);
             ptx::mbar_init(&oc_free[i], 4);
@@ -604,39 +625,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
         }
     } else if (warp < 12) {
-        // ------------------------------------------------------------------ softmax, thread = row
+        // ------------------------------------------------------------------ softmax, two threads per row
         ptx::setmaxnreg_dec<kPfRegsSoftmax>();
-        const int k = (warp - 4) >> 2;   // chunk parity of this warpgroup
+        const int h = (warp - 4) >> 2;   // key half of this warpgroup
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int t_local = row / n_rep;
         const bool valid = (t_local < a.tq) && (t0 + t_local < a.tokens);
         const int pos_r = base + t0 + t_local;
-        const uint32_t s_addr = tmem + lane_addr + PF_TM_S + k * 128;
+        float* xch = reinterpret_cast<float*>(sm + PF_OFF_XCH);
         bool ok = true;
-        for (int i = k; i < n_iter; i += 2) {
+        for (int i = 0; i < n_iter; ++i) {
+            const int k = i & 1;
             // s_full(i) also means PV(i - 2) -- issued before S(i) -- is done with P[k]
             if (ok) ok = ptx::mbar_wait(&s_full[k], (i >> 1) & 1, err);
             ptx::tc_fence_after();
             const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
-            float m, l;
-            softmax_row_tmem(s_addr, jmax, a.scale_log2, m, l);
-            ptx::tmem_st2(s_addr + PF_TM_ML, m, l);
-            ptx::tmem_wait_st();
-            // value rows past the last visible key of this tile are zeroed (they may hold
-            // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
-            // the chunk's V has landed
-            if (i * kAttnChunk + kAttnChunk - 1 > kv_last && ok) ok = ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err);
-            if (i * kAttnChunk + row > kv_last) {
-                uint8_t* vrow = sm + PF_OFF_V + k * 2 * kSub + row * 128;
+            float m;
+            // both halves reach the two barriers inside on every chunk, whatever `ok` says
+            softmax_half_tmem(tmem + lane_addr + PF_TM_S + k * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, m);
+            if (h == 0) {
+                // value rows past the last visible key of this tile are zeroed (they may hold
+                // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
+                // the chunk's V has landed
+                if (i * kAttnChunk + kAttnChunk - 1 > kv_last && ok)
+                    ok = ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err);
+                if (i * kAttnChunk + row > kv_last) {
+                    uint8_t* vrow = sm + PF_OFF_V + k * 2 * kSub + row * 128;
 #pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16) {
-                    *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(vrow + kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vrow + kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+                    }
                 }
+                ptx::fence_proxy_async_smem();
             }
-            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&p_full[k]);
