@@ -26,7 +26,7 @@ __all__ = [
     "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_destroy",
     "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
     "llama_block_decode_devpos",
-    "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_block_launch_count",
+    "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
     "llama_embed", "llama_lmhead_workspace_bytes",
     "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
 ]
@@ -42,9 +42,29 @@ def lib():
     return _native.load()
 
 
-def _ptr(t: Optional[torch.Tensor]):
+class HostMapped:
+    """A pinned host tensor seen through its device address: passed as x or y of
+    prefill/decode, the kernels read or write the host memory directly."""
+
+    def __init__(self, t: torch.Tensor):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("HostMapped needs a pinned host tensor")
+        if not t.is_contiguous():
+            raise ValueError("HostMapped needs a contiguous tensor")
+        dev = C.c_void_p()
+        rc = lib().llama_device_ptr_of_host(C.c_void_p(t.data_ptr()), C.byref(dev))
+        if rc != LLAMA_OK or not dev.value:
+            raise LlamaError(rc, "llama_device_ptr_of_host: not pinned and mapped")
+        self.t = t
+        self.dev_ptr = dev.value
+        self.shape = t.shape
+
+
+def _ptr(t):
     if t is None:
         return None
+    if isinstance(t, HostMapped):
+        return C.c_void_p(t.dev_ptr)
     if not t.is_cuda:
         raise ValueError("tensors passed to the block library must live on a CUDA device")
     if not t.is_contiguous():

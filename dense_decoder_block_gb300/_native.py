@@ -60,6 +60,7 @@ SIGNATURES = {
     "llama_block_last_error": (C.c_char_p, [C.c_void_p]),
     "llama_block_set_stage_events": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.c_int]),
     "llama_block_launch_count": (C.c_int, [C.c_void_p]),
+    "llama_device_ptr_of_host": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p)]),
     "llama_embed": (C.c_int, [C.c_void_p, C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p,
                               C.c_void_p]),
     "llama_lmhead_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),

@@ -560,6 +560,18 @@ extern "C" int llama_block_set_stage_events(llama_block b, void* const* events, 
 
 extern "C" int llama_block_launch_count(llama_block b) { return b ? b->last_launches : 0; }
 
+extern "C" int llama_device_ptr_of_host(const void* host, void** dev) {
+    if (!host || !dev) return LLAMA_ERR_INVALID_ARG;
+    *dev = nullptr;
+    void* p = nullptr;
+    if (cudaHostGetDevicePointer(&p, const_cast<void*>(host), 0) != cudaSuccess) {
+        cudaGetLastError();   // not pinned and mapped: clear the error, report it
+        return LLAMA_ERR_INVALID_ARG;
+    }
+    *dev = p;
+    return LLAMA_OK;
+}
+
 extern "C" int llama_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype,
                              void* stream) {
     if (rows < 0 || d <= 0) return LLAMA_ERR_INVALID_ARG;

@@ -165,6 +165,15 @@ int llama_block_set_stage_events(llama_block blk, void* const* events, int n_eve
  * projections need a reduction kernel) and on the call (decode or prefill). */
 int llama_block_launch_count(llama_block blk);
 
+/* Device address of pinned host memory (cudaHostAlloc / cudaHostRegister; with
+ * unified addressing every such allocation is mapped).  x and y of prefill and
+ * decode may be given this way: the kernels then read x from and write y to host
+ * memory directly (over NVLink-C2C on a Grace host), with no copy calls around
+ * the block.  Only x and y take host memory: weights, the cache and the
+ * workspace are read by TMA and must be device memory.  *dev = NULL and
+ * LLAMA_ERR_INVALID_ARG if `host` is not pinned and mapped. */
+int llama_device_ptr_of_host(const void* host, void** dev);
+
 /* ---------------------------------------------------------------------------
  * Stack head (32-layer generation loop): embedding gather, final RMSNorm,
  * LM head with greedy choice.  bf16 only.

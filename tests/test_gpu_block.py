@@ -281,3 +281,33 @@ def test_chunked_prefill_position_range():
     assert ei.value.code == -3   # LLAMA_ERR_POS_RANGE
     with pytest.raises(ddb.LlamaError):
         blk.prefill_at(x, kv, -1, y, blk.workspace(1, 8))
+
+
+def test_host_mapped_x_and_y_match_device_buffers():
+    """x read from and y written to pinned host memory by the kernels (through
+    llama_device_ptr_of_host) give the same bits as device buffers, in prefill and
+    decode; unpinned memory is refused."""
+    T, steps, max_seq = 200, 2, 208
+    inp = workloads.make_block_inputs(MID, 2, T + steps, max_seq=max_seq)
+    y_dev, kc_dev, vc_dev, blk, ddb = _prefill_then_decode(inp, T, steps, max_seq)
+    dev = torch.device("cuda:0")
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    kv = ddb.KVCache(kc, vc)
+    outs = []
+    xh = inp.x[:, :T].contiguous().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    blk.prefill(ddb.HostMapped(xh), kv, ddb.HostMapped(yh), blk.workspace(2, T))
+    torch.cuda.synchronize()
+    outs.append(yh.clone())
+    for s in range(steps):
+        xs = inp.x[:, T + s:T + s + 1].contiguous().pin_memory()
+        ys = torch.empty_like(xs).pin_memory()
+        blk.decode(ddb.HostMapped(xs), kv, T + s, ddb.HostMapped(ys), blk.workspace(2, 1))
+        torch.cuda.synchronize()
+        outs.append(ys.clone())
+    assert blk.poll_error() == 0
+    assert torch.equal(torch.cat(outs, dim=1), y_dev.cpu())
+    n = T + steps
+    assert torch.equal(kc[:, :, :n], kc_dev[:, :, :n]) and torch.equal(vc[:, :, :n], vc_dev[:, :, :n])
+    with pytest.raises(ValueError):
+        ddb.HostMapped(torch.empty(4))   # not pinned
