@@ -25,7 +25,7 @@ from ._native import (LLAMA_BF16, LLAMA_F32, LLAMA_OK, LLAMA_ERR_INVALID_ARG, LL
 __all__ = [
     "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_destroy",
     "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
-    "llama_block_decode_devpos",
+    "llama_block_decode_devpos", "llama_block_decode_seqpos",
     "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
     "llama_embed", "llama_lmhead_workspace_bytes",
     "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
@@ -131,6 +131,11 @@ def llama_block_decode(h, x, batch, kv: llama_kv_cache, pos, y, ws, ws_bytes, st
 def llama_block_decode_devpos(h, x, batch, kv: llama_kv_cache, pos_dev, y, ws, ws_bytes, stream=None) -> None:
     _check(h, lib().llama_block_decode_devpos(h, _ptr(x), batch, C.byref(kv), _ptr(pos_dev), _ptr(y), _ptr(ws),
                                               ws_bytes, _stream(stream)), "llama_block_decode_devpos")
+
+
+def llama_block_decode_seqpos(h, x, batch, kv: llama_kv_cache, pos_seq, y, ws, ws_bytes, stream=None) -> None:
+    _check(h, lib().llama_block_decode_seqpos(h, _ptr(x), batch, C.byref(kv), _ptr(pos_seq), _ptr(y), _ptr(ws),
+                                              ws_bytes, _stream(stream)), "llama_block_decode_seqpos")
 
 
 def llama_block_set_stage_events(h, events) -> None:
@@ -239,6 +244,10 @@ class LlamaBlock:
 
     def decode_devpos(self, x, kv: KVCache, pos_dev, y, ws, stream=None):
         llama_block_decode_devpos(self.h, x, x.shape[0], kv.c, pos_dev, y, ws, ws.numel(), stream)
+
+    def decode_seqpos(self, x, kv: KVCache, pos_seq, y, ws, stream=None):
+        """pos_seq: int32 CUDA tensor [batch], sequence b at position pos_seq[b]."""
+        llama_block_decode_seqpos(self.h, x, x.shape[0], kv.c, pos_seq, y, ws, ws.numel(), stream)
 
     def poll_error(self, stream=None) -> int:
         return llama_block_poll_error(self.h, stream)

@@ -56,6 +56,8 @@ SIGNATURES = {
                                      C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "llama_block_decode_devpos": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.POINTER(llama_kv_cache),
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "llama_block_decode_seqpos": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.POINTER(llama_kv_cache),
+                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "llama_block_poll_error": (C.c_int, [C.c_void_p, C.c_void_p]),
     "llama_block_last_error": (C.c_char_p, [C.c_void_p]),
     "llama_block_set_stage_events": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.c_int]),

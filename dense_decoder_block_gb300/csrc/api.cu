@@ -160,7 +160,8 @@ int check_kv(llama_block b, const llama_kv_cache* kv, int batch, int last_pos) {
 // The block's schedule, shared by prefill (T tokens at 0..T-1) and decode
 // (T = 1 at `pos`, or at *pos_dev).
 int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* kv, int start_pos,
-              const int32_t* pos_dev, void* y, void* ws, size_t ws_bytes, void* stream_v, bool decode) {
+              const int32_t* pos_dev, void* y, void* ws, size_t ws_bytes, void* stream_v, bool decode,
+              const int32_t* pos_seq = nullptr) {
     const auto& d = b->dims;
     cudaStream_t s = (cudaStream_t)stream_v;
     const int M = B * T;
@@ -208,6 +209,7 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
     at.kv_seq = kv->max_seq;
     at.start_pos = start_pos;
     at.pos_dev = pos_dev;
+    at.pos_seq = pos_seq;
     at.max_pos = max_pos;
     at.dtype = d.dtype;
     at.partial = w.attn_partial;
@@ -243,6 +245,7 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         eq.tokens_per_seq = T;
         eq.start_pos = start_pos;
         eq.pos_dev = pos_dev;
+        eq.pos_seq = pos_seq;
         eq.max_pos = max_pos;
         eq.cos_tab = b->cos_tab;
         eq.sin_tab = b->sin_tab;
@@ -525,6 +528,27 @@ extern "C" int llama_block_decode_devpos(llama_block b, const void* x, int batch
     int rc = check_kv(b, kv, batch, 0);
     if (rc != LLAMA_OK) return rc;
     return run_block(b, x, batch, 1, kv, 0, pos_dev, y, ws, ws_bytes, stream, true);
+}
+
+extern "C" int llama_block_decode_seqpos(llama_block b, const void* x, int batch, const llama_kv_cache* kv,
+                                         const int32_t* pos_seq, void* y, void* ws, size_t ws_bytes, void* stream) {
+    if (!b) return LLAMA_ERR_INVALID_ARG;
+    if (batch < 0) return fail(b, LLAMA_ERR_INVALID_ARG, "negative batch");
+    if (batch == 0) return LLAMA_OK;
+    if (!x || !y || !pos_seq || !aligned16(x) || !aligned16(y))
+        return fail(b, LLAMA_ERR_INVALID_ARG, "x / y / pos_seq null or x / y not 16-byte aligned");
+    const auto& d = b->dims;
+    // The per-sequence positions reach the QKV reduction (RoPE, cache row), the
+    // weight-streaming decode attention and the combine: bf16, up to 8 query heads per
+    // KV head, a QKV projection with a reduction step (more than one K-segment), at
+    // most 32 sequences (the weight-streaming schedule).
+    if (d.dtype != LLAMA_BF16 || !attention_tc_supported(d.n_heads, d.n_kv_heads, d.head_dim) ||
+        d.n_heads / d.n_kv_heads > 8 || batch > 32 ||
+        !gemm_needs_reduce(problem_qkv(b, batch, nullptr), PATH_AUTO))
+        return fail(b, LLAMA_ERR_UNSUPPORTED_DIMS, "per-sequence positions need the bf16 weight-streaming decode path");
+    int rc = check_kv(b, kv, batch, 0);
+    if (rc != LLAMA_OK) return rc;
+    return run_block(b, x, batch, 1, kv, 0, nullptr, y, ws, ws_bytes, stream, true, pos_seq);
 }
 
 extern "C" int llama_block_poll_error(llama_block b, void* stream) {

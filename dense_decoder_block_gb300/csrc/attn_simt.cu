@@ -136,6 +136,7 @@ struct AttnK {
     const void* vc;
     int batch, tokens, n_heads, n_kv_heads, kv_seq, start_pos, max_pos;
     const int* pos_dev;
+    const int* pos_seq;   // decode combine: sequence b at position pos_seq[b]
     float scale_log2;
     float* partial;
     int n_chunks;
@@ -268,11 +269,11 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
 
 template <typename T, int DH>
 __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
+    const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
     // The position is set before the step, never by the kernels this one overlaps.
-    const int pos = base_position(a);
+    const int pos = a.pos_seq ? a.pos_seq[b] : base_position(a);
     ptx_wait();
     if (threadIdx.x == 0) ptx_launch_dependents();
-    const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int g = h / n_rep, r = h % n_rep;
     if (pos < 0 || pos >= a.max_pos) return;
@@ -300,6 +301,7 @@ AttnK make_k(const AttnArgs& a) {
     k.start_pos = a.start_pos;
     k.max_pos = a.max_pos;
     k.pos_dev = a.pos_dev;
+    k.pos_seq = a.pos_seq;
     k.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a.head_dim));
     k.partial = a.partial;
     k.n_chunks = a.n_chunks;

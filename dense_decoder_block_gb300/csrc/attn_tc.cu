@@ -47,6 +47,7 @@ constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32_bmn(128, 128);
 struct TcArgs {
     int batch, tokens, n_heads, n_kv_heads, kv_seq, start_pos, max_pos;
     const int* pos_dev;
+    const int* pos_seq;  // decode: sequence b at position pos_seq[b] (the k_attn_tc_dec kernel only)
     float scale_log2;
     const bf16* q;       // decode: [B, Hq * 128]
     bf16* o;             // prefill: [B * T, Hq * 128]
@@ -798,15 +799,43 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc_rows8(uint32_t smem_addr) 
     return ptx::sw128_kmajor_desc(smem_addr) & ~(0x3FFFull << 32);   // stride byte offset 0
 }
 
+// Decode units: (sequence b, KV head g, chunk c), c fastest, then g, then b.  With
+// one position for the whole batch every sequence has n_total chunks; with one
+// position per sequence, sequence b has nt(b) = pos_b / 128 + 1 and `pre` (shared
+// memory) holds the prefix sums pre[b] = nt(0) + ... + nt(b - 1).
 struct DecUnit {
     int b, g, c;
+    int nt, pos;   // the sequence's chunk count and position
 };
-__device__ __forceinline__ DecUnit dec_unit(int u, int n_total, int n_kv) {
+struct DecMap {
+    int n_kv, n_total, pos, batch;
+    const int* pre;    // null: one position for the batch
+    const int* spos;   // per-sequence positions (shared memory)
+};
+constexpr int kSeqPosMax = 1024;   // sequences per call with per-sequence positions
+__device__ __forceinline__ DecUnit dec_unit(const DecMap& m, int u) {
     DecUnit d;
-    d.c = u % n_total;
-    const int bg = u / n_total;
-    d.g = bg % n_kv;
-    d.b = bg / n_kv;
+    if (m.pre == nullptr) {
+        d.c = u % m.n_total;
+        const int bg = u / m.n_total;
+        d.g = bg % m.n_kv;
+        d.b = bg / m.n_kv;
+        d.nt = m.n_total;
+        d.pos = m.pos;
+        return d;
+    }
+    int lo = 0, hi = m.batch - 1;   // the last sequence whose units start at or before u
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (m.pre[mid] * m.n_kv <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    d.b = lo;
+    d.nt = m.pre[lo + 1] - m.pre[lo];
+    const int r = u - m.pre[lo] * m.n_kv;
+    d.g = r / d.nt;
+    d.c = r - d.g * d.nt;
+    d.pos = m.spos[lo];
     return d;
 }
 
@@ -843,13 +872,55 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
     // from the kernels this one overlaps; cache rows below it were written by
     // earlier steps.  Only q and the newest cache row need griddepcontrol.wait.
     const int n_rep = a.n_heads / a.n_kv_heads;
-    const int pos = a.pos_dev ? *a.pos_dev : a.start_pos;
-    if (pos < 0 || pos >= a.max_pos) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
-        return;
+    __shared__ int s_pre[kSeqPosMax + 1], s_pos[kSeqPosMax];
+    __shared__ int s_bad;
+    DecMap dm{a.n_kv_heads, 0, 0, a.batch, nullptr, nullptr};
+    int n_units;
+    if (a.pos_seq) {
+        // per-sequence positions: chunk counts and their prefix sums, one warp
+        if (warp == 0) {
+            int run = 0, bad = 0;
+            for (int b0 = 0; b0 < a.batch; b0 += 32) {
+                const int b = b0 + lane;
+                const int p = b < a.batch ? a.pos_seq[b] : 0;
+                const bool in = b < a.batch && p >= 0 && p < a.max_pos;
+                if (b < a.batch && !in) bad = 1;
+                int nt = in ? p / kAttnChunk + 1 : 0;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, nt, off);
+                    if (lane >= off) nt += v;
+                }
+                if (b < a.batch) {
+                    s_pre[b + 1] = run + nt;
+                    s_pos[b] = p;
+                }
+                run += __shfl_sync(0xffffffffu, nt, 31);
+            }
+            bad = __any_sync(0xffffffffu, bad);
+            if (lane == 0) {
+                s_pre[0] = 0;
+                s_bad = bad;
+            }
+        }
+        __syncthreads();
+        if (s_bad) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
+            return;
+        }
+        dm.pre = s_pre;
+        dm.spos = s_pos;
+        n_units = s_pre[a.batch] * a.n_kv_heads;
+    } else {
+        const int pos = a.pos_dev ? *a.pos_dev : a.start_pos;
+        if (pos < 0 || pos >= a.max_pos) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
+            return;
+        }
+        dm.pos = pos;
+        dm.n_total = pos / kAttnChunk + 1;
+        n_units = a.batch * a.n_kv_heads * dm.n_total;
     }
-    const int n_total = pos / kAttnChunk + 1;
-    const int n_units = a.batch * a.n_kv_heads * n_total;
     const int u_begin = (int)(((long)n_units * blockIdx.x) / gridDim.x);
     const int u_end = (int)(((long)n_units * (blockIdx.x + 1)) / gridDim.x);
     const int n_iter = u_end - u_begin;
@@ -898,8 +969,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             for (int i = 0; i < n_iter; ++i, ++issued) {
                 const int st = i % n_st;
                 if (i >= n_st && !ptx::mbar_wait(&empty[st], ((i / n_st) - 1) & 1, err)) break;
-                const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
-                if (!waited && d.c == n_total - 1) {   // this chunk holds the row the QKV step writes
+                const DecUnit d = dec_unit(dm, u_begin + i);
+                if (!waited && d.c == d.nt - 1) {   // this chunk holds the row the QKV step writes
                     ptx::griddep_wait();
                     waited = true;
                 }
@@ -970,7 +1041,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
         uint4 qreg[4];
         int qreg_bg = -1;
         auto fetch_q = [&](int i) {
-            const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
+            const DecUnit d = dec_unit(dm, u_begin + i);
             const int bg = d.b * a.n_kv_heads + d.g;
             if (bg == q_bg || bg == qreg_bg) return;
 #pragma unroll
@@ -987,7 +1058,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             qreg_bg = bg;
         };
         auto prepare = [&](int i) {
-            const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
+            const DecUnit d = dec_unit(dm, u_begin + i);
             const int bg = d.b * a.n_kv_heads + d.g;
             if (bg != q_bg) {
                 fetch_q(i);
@@ -1004,11 +1075,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
         };
         if (slot < n_iter) prepare(slot);
         for (int i = slot, k = 0; i < n_iter; i += kDecSlots, ++k) {
-            const DecUnit d = dec_unit(u_begin + i, n_total, a.n_kv_heads);
+            const DecUnit d = dec_unit(dm, u_begin + i);
             const int st = i % kDecStagesV;   // the unit's V stage
             if (ok) ok = ptx::mbar_wait(&s_full[slot], k & 1, err);
             ptx::tc_fence_after();
-            const int jmax = min(kAttnChunk - 1, pos - d.c * kAttnChunk);   // the same for every row
+            const int jmax = min(kAttnChunk - 1, d.pos - d.c * kAttnChunk);   // the same for every row
             float sv[32];
             tmem_ld_quarter(taddr, q, sv);
             float m = quarter_max_raw(sv, q * 32, jmax);
@@ -1025,12 +1096,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
             ptx::tc_fence_before();
             // value rows past the position hold anything (NaN included): zero them once
             // the chunk's V has landed
-            if (d.c == n_total - 1) {
+            if (d.c == d.nt - 1) {
                 if (ok) ok = ptx::mbar_wait(&v_full[st], (i / kDecStagesV) & 1, err);
 #pragma unroll
                 for (int r4 = 0; r4 < 4; ++r4) {
                     const int vr = lane + 32 * r4;
-                    if (d.c * kAttnChunk + vr > pos) {
+                    if (d.c * kAttnChunk + vr > d.pos) {
                         uint8_t* vrow = sm + D_OFF_V + st * 2 * kSub + vr * 128;
 #pragma unroll
                         for (int c16 = 0; c16 < 8; ++c16) {
@@ -1121,6 +1192,7 @@ TcArgs make_args(const AttnArgs& a) {
     k.start_pos = a.start_pos;
     k.max_pos = a.max_pos;
     k.pos_dev = a.pos_dev;
+    k.pos_seq = a.pos_seq;
     k.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a.head_dim));
     k.q = (const bf16*)a.q;
     k.o = (bf16*)a.o;

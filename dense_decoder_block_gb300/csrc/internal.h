@@ -27,6 +27,7 @@ struct GemmEpi {
     int tokens_per_seq = 1;                         // token n -> (n / T, n % T)
     int start_pos = 0;                              // position of token t = base + t
     const int* pos_dev = nullptr;                   // if set, base = *pos_dev
+    const int* pos_seq = nullptr;                   // decode (T = 1): token n at position pos_seq[n]
     int max_pos = 0;                                // positions must be < max_pos
     const float* cos_tab = nullptr;                 // [max_pos, 64]
     const float* sin_tab = nullptr;
@@ -97,6 +98,7 @@ struct AttnArgs {
     int n_heads = 0, n_kv_heads = 0, head_dim = 0, kv_seq = 0;
     int start_pos = 0;
     const int* pos_dev = nullptr;
+    const int* pos_seq = nullptr;       // decode: sequence b at position pos_seq[b] (device)
     int max_pos = 0;
     int dtype = LLAMA_BF16;
     float* partial = nullptr;           // decode: [B, Hkv, n_chunks, n_rep, head_dim + 4]

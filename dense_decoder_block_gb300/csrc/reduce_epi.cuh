@@ -79,7 +79,7 @@ __device__ __forceinline__ Qkv4 epi4_qkv_prepare(const GemmEpi& e, int n, int f0
     else { kind = 2; head = tile - e.n_heads - e.n_kv_heads; }
     const int T = e.tokens_per_seq;
     const int b = n / T, t = n - b * T;
-    const int pos = (e.pos_dev ? *e.pos_dev : e.start_pos) + t;
+    const int pos = e.pos_seq ? e.pos_seq[b] : (e.pos_dev ? *e.pos_dev : e.start_pos) + t;   // pos_seq: T = 1
     if (pos < 0 || pos >= e.max_pos) {
         record_error(e.err, LLAMA_ERR_POS_RANGE);
         p.dst = nullptr;

@@ -142,6 +142,20 @@ int llama_block_decode_devpos(llama_block blk, const void* x, int batch, const l
                               const int32_t* pos_dev, void* y, void* workspace, size_t workspace_bytes,
                               void* stream);
 
+/* One decode step with a position per sequence: sequence b sits at position
+ * pos_seq[b] (int32, device memory, read by the kernels when they run, so a
+ * captured graph can be replayed as the positions move).  Sequence b reads its
+ * cache rows 0..pos_seq[b] and writes row pos_seq[b]; its result equals, bit for
+ * bit, what llama_block_decode at that position gives for it.  Each value must lie
+ * in [0, max_seq): otherwise the kernels record LLAMA_ERR_POS_RANGE in the error
+ * word, write no cache row and leave y undefined.  Supported for bf16 handles
+ * with at most 8 query heads per KV head, batch <= 32, and a QKV projection with
+ * more than one K-segment (true for the 8B and 70B shapes); otherwise
+ * LLAMA_ERR_UNSUPPORTED_DIMS. */
+int llama_block_decode_seqpos(llama_block blk, const void* x, int batch, const llama_kv_cache* kv,
+                              const int32_t* pos_seq, void* y, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /* Synchronise `stream`, read and clear the handle's device error word.
  * Returns LLAMA_OK or the code a kernel recorded (LLAMA_ERR_DEVICE_TIMEOUT,
  * LLAMA_ERR_POS_RANGE). */

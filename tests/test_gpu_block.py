@@ -311,3 +311,52 @@ def test_host_mapped_x_and_y_match_device_buffers():
     assert torch.equal(kc[:, :, :n], kc_dev[:, :, :n]) and torch.equal(vc[:, :, :n], vc_dev[:, :, :n])
     with pytest.raises(ValueError):
         ddb.HostMapped(torch.empty(4))   # not pinned
+
+
+def test_decode_per_sequence_positions_bit_identical_to_prefill():
+    """One decode step with a position per sequence (chunk counts 1, 1, 2, 2 and 3,
+    positions on both sides of chunk edges): every sequence's output row and new
+    cache row equal the prefill rows at its position bit for bit, cache rows past
+    each position are left alone, and an out-of-range position is reported."""
+    pos = [5, 127, 128, 257, 300]
+    B, T_all = len(pos), max(pos) + 1
+    max_seq = T_all + 4
+    inp = workloads.make_block_inputs(MID, B, T_all, max_seq=max_seq)
+    blk, ddb = gpu_block(inp, max_seq)
+    dev = torch.device("cuda:0")
+    kc_pf, vc_pf = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    x = inp.x.to(dev)
+    y_pf = run_prefill(blk, ddb, x, kc_pf, vc_pf)
+    # caches holding only rows 0..pos[b]-1 of each sequence
+    kc, vc = kc_pf.clone(), vc_pf.clone()
+    for b, p in enumerate(pos):
+        kc[b, :, p:] = float("nan")
+        vc[b, :, p:] = float("nan")
+    x_dec = torch.stack([x[b, p] for b, p in enumerate(pos)]).unsqueeze(1).contiguous()
+    pos_seq = torch.tensor(pos, dtype=torch.int32, device=dev)
+    y = torch.empty_like(x_dec)
+    kv = ddb.KVCache(kc, vc)
+    blk.decode_seqpos(x_dec, kv, pos_seq, y, blk.workspace(B, 1))
+    torch.cuda.synchronize()
+    assert blk.poll_error() == 0
+    for b, p in enumerate(pos):
+        assert torch.equal(y[b, 0], y_pf[b, p]), f"sequence {b} at {p}"
+        assert torch.equal(kc[b, :, p], kc_pf[b, :, p]) and torch.equal(vc[b, :, p], vc_pf[b, :, p])
+        assert torch.isnan(kc[b, :, p + 1:]).all() and torch.isnan(vc[b, :, p + 1:]).all()
+    # a position outside the cache is recorded by the kernels
+    bad = torch.tensor([5, 127, max_seq, 257, 300], dtype=torch.int32, device=dev)
+    blk.decode_seqpos(x_dec, kv, bad, y, blk.workspace(B, 1))
+    assert blk.poll_error() == ddb.LLAMA_ERR_POS_RANGE
+    assert blk.poll_error() == 0
+
+
+def test_decode_per_sequence_positions_unsupported_shape():
+    """The fp32 workload has no per-sequence decode path: refused up front."""
+    inp = workloads.make_block_inputs(workloads.TINY, 2, 4, dtype=torch.float32, max_seq=16)
+    blk, ddb = gpu_block(inp, 16)
+    dev = torch.device("cuda:0")
+    kv = ddb.KVCache(inp.k_cache.to(dev), inp.v_cache.to(dev))
+    x = inp.x[:, :1].contiguous().to(dev)
+    with pytest.raises(ddb.LlamaError):
+        blk.decode_seqpos(x, kv, torch.tensor([1, 2], dtype=torch.int32, device=dev), torch.empty_like(x),
+                          blk.workspace(2, 1))
