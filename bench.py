@@ -66,6 +66,17 @@ def decode_step_bytes(dims, B, pos):
     return from_bytes * (weights + kv_read + kv_write + act)
 
 
+def decode_seqpos_bytes(dims, positions):
+    """decode_step_bytes with a position per sequence: each sequence reads its own
+    pos + 1 cache rows."""
+    d, f = dims.d_model, dims.d_ff
+    q, kv = dims.n_heads * dims.head_dim, dims.n_kv_heads * dims.head_dim
+    B = len(positions)
+    weights = d * (q + 2 * kv) + q * d + 3 * d * f + 2 * d
+    kv_read = sum(2 * dims.n_kv_heads * (p + 1) * dims.head_dim for p in positions)
+    return 2 * (weights + kv_read + 2 * B * kv + 2 * B * d)
+
+
 def gateup_launch_bytes(dims, B):
     """Algorithmic bytes of one gate/up projection launch: both weight matrices once,
     the normalised input read, the SwiGLU output written."""
@@ -567,6 +578,7 @@ def extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind):
         by = decode_step_bytes(dims, B, POS)
         res[f"decode_b{B}"] = {"tok_s": round(B / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
                                "hbm_frac": round(by / (ms / 1e3) / 1e9 / hbm, 4)}
+    res["decode_b32_seqpos"] = extra_seqpos(ddb, dims, wts, device, hbm)
     for T in (512, 2048, 8192):
         inp = workloads.make_block_inputs(dims, 1, T, max_seq=T, weights=wts, poison_tail=False)
         blk = ddb.LlamaBlock(dims, w, g, T)
@@ -581,6 +593,30 @@ def extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind):
         res[f"prefill_t{T}"] = {"tok_s": round(T / (ms / 1e3), 1), "ms": round(ms, 3), "tflops": round(tf, 1),
                                 "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind}
     return res
+
+
+def extra_seqpos(ddb, dims, wts, device, hbm):
+    """Batch 32 with a position per sequence (llama_block_decode_seqpos): positions
+    spread evenly over 500..1500 (mean 1000, the main line's), timed on its own."""
+    B = 32
+    positions = [500 + (b * 1000) // (B - 1) for b in range(B)]
+    w = {k: v.to(device) for k, v in wts[0].items()}
+    g = {k: v.to(device) for k, v in wts[1].items()}
+    stream = torch.cuda.current_stream(device)
+    max_seq = 2048
+    inp = workloads.make_block_inputs(dims, B, 1, cache_len=max(positions), max_seq=max_seq, weights=wts)
+    blk = ddb.LlamaBlock(dims, w, g, max_seq)
+    kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+    x = inp.x.to(device)
+    y = torch.empty_like(x)
+    ws = blk.workspace(B, 1)
+    pos_seq = torch.tensor(positions, dtype=torch.int32, device=device)
+    ms = time_region(lambda: blk.decode_seqpos(x, kv, pos_seq, y, ws), 50, 5, stream)
+    assert blk.poll_error() == 0
+    by = decode_seqpos_bytes(dims, positions)
+    return {"tok_s": round(B / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
+            "hbm_frac": round(by / (ms / 1e3) / 1e9 / hbm, 4), "algorithmic_bytes": by,
+            "positions": f"{positions[0]}..{positions[-1]} (one per sequence, mean {sum(positions) / B:.0f})"}
 
 
 def extra_70b(ddb, device, hbm, bf16_peak, peak_kind):
