@@ -382,9 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //                TMEM lane quarter, exchanging the row max and two quarter sums
 //                through shared memory; P (bf16 pairs) overwrites the first 64
 //                columns of the S row once both halves hold their scores, the
-//                row's (m, l) goes to columns 64, 65.  (One warpgroup per chunk,
-//                alternating chunks, left each chunk to one warp per scheduler
-//                and the chunk time at that warp's latency.)
+//                row's (m, l) goes to columns 64, 65.  (One warpgroup per chunk
+//                on alternate chunks, thread = row, gave the same chunk time: it
+//                is set by the chain softmax -> PV -> fold -> next S, not by one
+//                warp's softmax.)
 //   warps 12-15  fold of every chunk into the running (O, M, L), thread = row,
 //                with the row's O in registers; then o = O * (1 / L)
 // Warp 3 only keeps the roles aligned to warpgroups.  A chunk that is wholly
