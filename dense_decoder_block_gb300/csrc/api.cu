@@ -621,6 +621,7 @@ namespace {
 struct HeadWs {
     void* hn;
     float* logits;
+    int* err;   // set by an expired wait of the projection, reported through ids
     size_t total;
 };
 HeadWs head_layout(int batch, int d_model, int vocab, uint8_t* base, bool own_logits) {
@@ -633,6 +634,7 @@ HeadWs head_layout(int batch, int d_model, int vocab, uint8_t* base, bool own_lo
     };
     w.hn = take((size_t)batch * d_model * 2);
     w.logits = own_logits ? (float*)take((size_t)batch * vocab * sizeof(float)) : nullptr;
+    w.err = (int*)take(sizeof(int));
     w.total = off;
     return w;
 }
@@ -654,6 +656,7 @@ extern "C" int llama_lmhead_argmax(const void* h, int batch, int h_stride, const
     HeadWs w = head_layout(batch, d_model, vocab, (uint8_t*)ws, true);
     float* lg = logits ? logits : w.logits;
     cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemsetAsync(w.err, 0, sizeof(int), s) != cudaSuccess) return LLAMA_ERR_CUDA;
     // final RMSNorm of the selected rows (row stride h_stride), one row at a time is
     // avoided by a strided view: the norm kernel reads rows of length d at stride d,
     // so copy-free only when h_stride == d_model.
@@ -677,8 +680,9 @@ extern "C" int llama_lmhead_argmax(const void* h, int batch, int h_stride, const
     GemmEpi e;
     e.kind = EPI_LOGITS;
     e.out_f32 = lg;
+    e.err = w.err;
     // one K segment per CTA: logits need no prefill counterpart, so each CTA owns whole dot products
     if (launch_gemm_single_segment(p, e, s) != cudaSuccess) return LLAMA_ERR_CUDA;
-    if (launch_argmax_rows(lg, batch, vocab, ids, s) != cudaSuccess) return LLAMA_ERR_CUDA;
+    if (launch_argmax_rows(lg, batch, vocab, ids, w.err, s) != cudaSuccess) return LLAMA_ERR_CUDA;
     return LLAMA_OK;
 }

@@ -23,6 +23,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "internal.h"
@@ -1145,17 +1146,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+    if (!f) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult qr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
                 cudaSuccess ||
             qr != cudaDriverEntryPointSuccess)
             return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        fn.store(f, std::memory_order_release);
     }
-    return fn;
+    return f;
 }
 
 // K or V cache [rows][128] bf16 as [2][rows][64] (see tma_load_chunk).
@@ -1222,17 +1225,15 @@ cudaError_t launch_attention_tc_prefill(const AttnArgs& a, cudaStream_t s) {
     if (!make_tmap_bf16(&mk, a.kc, cache_rows, 128, 128, nullptr) ||
         !make_tmap_bf16(&mv, a.vc, cache_rows, 128, 128, nullptr))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
+    cudaError_t r = kernel_setup_once((const void*)k_attn_pf, [](const void* kern) {
         // the register split inside the kernel must fit the block's launch allocation
         cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, k_attn_pf);
-        if (r != cudaSuccess) return r;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
         if (fa.numRegs * kPfThreads < kPfRegsNeeded) return cudaErrorInvalidConfiguration;
-        r = cudaFuncSetAttribute(k_attn_pf, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES);
-        if (r != cudaSuccess) return r;
-        attr = true;
-    }
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES);
+    });
+    if (r != cudaSuccess) return r;
     const int n_tiles = (a.tokens + k.tq - 1) / k.tq;
     if (n_tiles > 65535) return cudaErrorInvalidValue;
     dim3 grid(a.n_kv_heads * a.batch, n_tiles);
@@ -1254,31 +1255,26 @@ cudaError_t launch_attention_tc_decode(const AttnArgs& a, int chunks_per_cta, cu
         if (!make_tmap_kv_chunk(&mk, a.kc, cache_rows) || !make_tmap_kv_chunk(&mv, a.vc, cache_rows))
             return cudaErrorInvalidValue;
         // persistent: one CTA per SM (units assigned on the device from the position)
-        static const int n_sm = device_sm_count();
+        const int n_sm = device_sm_count();
         const long max_units = (long)a.batch * a.n_kv_heads * a.n_chunks;
-        static bool attr_dec = false;
-        if (!attr_dec) {
-            cudaError_t r = cudaFuncSetAttribute(k_attn_tc_dec, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 D_SMEM_BYTES);
-            if (r != cudaSuccess) return r;
-            attr_dec = true;
-        }
+        cudaError_t r = kernel_setup_once((const void*)k_attn_tc_dec, [](const void* kern) {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, D_SMEM_BYTES);
+        });
+        if (r != cudaSuccess) return r;
         dim3 grid((unsigned)std::min<long>(max_units, n_sm));
-        cudaError_t r = launch_pdl(k_attn_tc_dec, grid, dim3(kDecThreads), D_SMEM_BYTES, s, mk, mv, k);
+        r = launch_pdl(k_attn_tc_dec, grid, dim3(kDecThreads), D_SMEM_BYTES, s, mk, mv, k);
         if (r != cudaSuccess) return r;
         return launch_attention_combine(a, s);
     }
     if (chunks_per_cta <= 0) chunks_per_cta = 2;
     k.chunks_per_cta = chunks_per_cta;
     auto kern = k_attn_tc_wide;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (r != cudaSuccess) return r;
-        attr = true;
-    }
+    cudaError_t r = kernel_setup_once((const void*)kern, [](const void* kf) {
+        return cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (r != cudaSuccess) return r;
     dim3 grid((a.n_chunks + chunks_per_cta - 1) / chunks_per_cta, a.n_kv_heads, a.batch);
-    cudaError_t r = launch_pdl(kern, grid, dim3(kThreads), SMEM_BYTES, s, mk, mv, k);
+    r = launch_pdl(kern, grid, dim3(kThreads), SMEM_BYTES, s, mk, mv, k);
     if (r != cudaSuccess) return r;
     return launch_attention_combine(a, s);
 }

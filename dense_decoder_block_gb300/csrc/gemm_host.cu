@@ -1,7 +1,10 @@
 // Host side of the tcgen05 projection kernel: TMA descriptors, schedule choice, launch.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "gemm_tc.cuh"
 
@@ -89,11 +92,34 @@ int choose_seg_kb(int n_tiles, int total_kb, int n_sm) {
     return best;
 }
 
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::mutex g_setup_lock;
+std::set<std::pair<const void*, int>> g_setup_done;
+}  // namespace
+
 int device_sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached && (n = g_sm_count[dev].load(std::memory_order_relaxed)) > 0) return n;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 148;
+    if (n <= 0) return 148;
+    if (cached) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+cudaError_t kernel_setup_once(const void* kern, cudaError_t (*setup)(const void* kern)) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_setup_lock);
+    const auto key = std::make_pair(kern, dev);
+    if (g_setup_done.count(key)) return cudaSuccess;
+    e = setup(kern);
+    if (e == cudaSuccess) g_setup_done.insert(key);
+    return e;
 }
 
 size_t gemm_partial_bytes(const GemmProblem& p, int path) {

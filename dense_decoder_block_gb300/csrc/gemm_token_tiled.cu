@@ -10,17 +10,15 @@ static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUten
                           const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
     using C = TtCfg<BN, DUAL>;
     auto kern = k_gemm_tt<BN, DUAL, EPI>;
-    static bool attr = false;
-    if (!attr) {
+    cudaError_t r = kernel_setup_once((const void*)kern, [](const void* k) {
         // The register split inside the kernel must fit the block's launch allocation.
         cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, kern);
-        if (r != cudaSuccess) return r;
+        cudaError_t e = cudaFuncGetAttributes(&fa, k);
+        if (e != cudaSuccess) return e;
         if (fa.numRegs * C::THREADS < C::REGS_NEEDED) return cudaErrorInvalidConfiguration;
-        r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (r != cudaSuccess) return r;
-        attr = true;
-    }
+        return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    });
+    if (r != cudaSuccess) return r;
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
     const int n_blocks = (p.M + BN - 1) / BN;

@@ -8,15 +8,13 @@ static cudaError_t run_ws(const GemmProblem& p, const GemmKArgs& ka, const CUten
                           const CUtensorMap& a2, const bf16* x, cudaStream_t s) {
     using C = WsCfg<BN, DUAL>;
     auto kern = k_gemm_ws<BN, DUAL, EPI>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (r != cudaSuccess) return r;
-        attr = true;
-    }
+    cudaError_t r = kernel_setup_once((const void*)kern, [](const void* k) {
+        return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    });
+    if (r != cudaSuccess) return r;
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
-    static const int n_sm = device_sm_count();
+    const int n_sm = device_sm_count();
     const int units = (p.F / kTileF) * ka.n_segs;
     dim3 grid(units < n_sm ? units : n_sm);
     return launch_pdl(kern, grid, dim3(kGemmThreads), C::SMEM_BYTES, s, a0, a1, a2, mb, ka);

@@ -60,7 +60,13 @@ bool gemm_needs_reduce(const GemmProblem& p, int path);
 // the n_sm SMs in one wave; failing that, the one that minimises the
 // weight-streaming makespan, at least 8 k-blocks per segment.
 int choose_seg_kb(int n_tiles, int total_kb, int n_sm);
+// SMs of the current device (looked up once per device).
 int device_sm_count();
+// Runs setup(kern) once per (kernel, device) -- function attributes such as the
+// dynamic shared-memory limit apply to the device that was current when they were
+// set -- under a process-wide lock, so concurrent first calls do not race.  A
+// failed setup is not recorded and runs again on the next call.
+cudaError_t kernel_setup_once(const void* kern, cudaError_t (*setup)(const void* kern));
 
 cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, cudaStream_t s);
 
@@ -133,6 +139,8 @@ cudaError_t launch_rope_append_f32(const float* qkv_q, const float* qkv_k, const
 // stack head
 cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, int d, void* x, int32_t* err,
                          cudaStream_t s);
-cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, cudaStream_t s);
+// ids[r] = argmax of logits row r, or *err when err is set and nonzero.
+cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, const int* err,
+                               cudaStream_t s);
 
 }  // namespace llama

@@ -20,30 +20,45 @@ namespace {
 constexpr int kNoAllocRows = 32;
 constexpr int kNoAllocDim = 8192;
 static __device__ __align__(256) __nv_bfloat16 g_lmhead_rows[kNoAllocRows * kNoAllocDim];
+// Error word of the projection's bounded waits (cleared by every call, reported through ids).
+static __device__ __align__(16) int g_lmhead_err;
 
 constexpr int kMaxDevices = 64;
+struct Scratch {
+    void* rows;
+    int* err;
+};
 std::atomic<void*> g_rows_addr[kMaxDevices];
+std::atomic<int*> g_err_addr[kMaxDevices];
 std::mutex g_setup;
 
-// The array's device address on the current device.  The host-side symbol is a
-// stand-in, not a device address, so it is looked up once per device (with that
-// device current) and cached.
-cudaError_t rows_address(void** out) {
+// The arrays' device addresses on the current device.  The host-side symbols are
+// stand-ins, not device addresses, so they are looked up once per device (with
+// that device current) and cached.
+cudaError_t scratch_address(Scratch* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     void* p = g_rows_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
+    int* q = g_err_addr[dev].load(std::memory_order_acquire);
+    if (!p || !q) {
         std::lock_guard<std::mutex> lock(g_setup);
         p = g_rows_addr[dev].load(std::memory_order_relaxed);
-        if (!p) {
+        q = g_err_addr[dev].load(std::memory_order_relaxed);
+        if (!p || !q) {
             e = cudaGetSymbolAddress(&p, g_lmhead_rows);
             if (e != cudaSuccess) return e;
+            void* qv = nullptr;
+            e = cudaGetSymbolAddress(&qv, g_lmhead_err);
+            if (e != cudaSuccess) return e;
+            q = (int*)qv;
+            g_err_addr[dev].store(q, std::memory_order_release);
             g_rows_addr[dev].store(p, std::memory_order_release);
         }
     }
-    *out = p;
+    out->rows = p;
+    out->err = q;
     return cudaSuccess;
 }
 
@@ -59,9 +74,11 @@ extern "C" int llama_lmhead_argmax_noalloc(const void* h, int batch, int h_strid
     if (batch == 0) return LLAMA_OK;
     if (!h || !g_final || !w_out || !ids || !logits || h_stride < d_model) return LLAMA_ERR_INVALID_ARG;
     if (batch > kNoAllocRows || d_model > kNoAllocDim) return LLAMA_ERR_WORKSPACE;   // beyond the static scratch
-    void* rows = nullptr;
-    if (rows_address(&rows) != cudaSuccess) return LLAMA_ERR_CUDA;
+    Scratch sc{};
+    if (scratch_address(&sc) != cudaSuccess) return LLAMA_ERR_CUDA;
+    void* rows = sc.rows;
     cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemsetAsync(sc.err, 0, sizeof(int), s) != cudaSuccess) return LLAMA_ERR_CUDA;
     if (h_stride == d_model) {
         if (launch_rmsnorm(h, g_final, rows, batch, d_model, eps, LLAMA_BF16, s) != cudaSuccess) return LLAMA_ERR_CUDA;
     } else {
@@ -82,7 +99,8 @@ extern "C" int llama_lmhead_argmax_noalloc(const void* h, int batch, int h_strid
     GemmEpi e;
     e.kind = EPI_LOGITS;
     e.out_f32 = logits;
+    e.err = sc.err;
     if (launch_gemm_single_segment(p, e, s) != cudaSuccess) return LLAMA_ERR_CUDA;
-    if (launch_argmax_rows(logits, batch, vocab, ids, s) != cudaSuccess) return LLAMA_ERR_CUDA;
+    if (launch_argmax_rows(logits, batch, vocab, ids, sc.err, s) != cudaSuccess) return LLAMA_ERR_CUDA;
     return LLAMA_OK;
 }

@@ -201,9 +201,11 @@ __global__ void k_embed(const int32_t* __restrict__ ids, const T* __restrict__ w
     for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
 }
 
-// argmax over one row of fp32 logits; ties go to the lowest index.
+// argmax over one row of fp32 logits; ties go to the lowest index.  If the
+// projection that wrote the logits recorded an error in *err (a bounded wait
+// expired), the row's id is that (negative) code instead.
 __global__ void __launch_bounds__(1024) k_argmax_rows(const float* __restrict__ logits, int vocab,
-                                                      int32_t* __restrict__ ids) {
+                                                      int32_t* __restrict__ ids, const int* __restrict__ err) {
     __shared__ float sv[32];
     __shared__ int si[32];
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -225,7 +227,8 @@ __global__ void __launch_bounds__(1024) k_argmax_rows(const float* __restrict__ 
     if (tid == 0) {
         for (int w = 1; w < (int)(blockDim.x / 32); ++w)
             if (sv[w] > best || (sv[w] == best && si[w] < bi)) { best = sv[w]; bi = si[w]; }
-        ids[row] = (bi == INT32_MAX) ? 0 : bi;
+        const int code = err ? *err : 0;
+        ids[row] = code != 0 ? code : (bi == INT32_MAX) ? 0 : bi;
     }
 }
 
@@ -273,9 +276,10 @@ cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, in
     return cudaGetLastError();
 }
 
-cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, cudaStream_t s) {
+cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, const int* err,
+                               cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    k_argmax_rows<<<rows, 1024, 0, s>>>(logits, vocab, ids);
+    k_argmax_rows<<<rows, 1024, 0, s>>>(logits, vocab, ids, err);
     return cudaGetLastError();
 }
 

@@ -76,7 +76,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // another thread of the grid already reported an error.  The error word is read
 // only once a wait has lasted kErrPollNs: every waiting warp of every CTA polling
 // one global address would keep that address's L2 slice busy and slow all the
-// loads that go through it.
+// loads that go through it.  err may be null: the wait is still bounded, it just
+// has nowhere to record the expiry.
 constexpr uint64_t kErrPollNs = 200000ull;   // 200 us
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -86,9 +87,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
         if (mbar_try_wait(bar, parity)) return true;
         if ((++spins & 63u) == 0) {
             const uint64_t dt = globaltimer() - t0;
-            if (dt > kErrPollNs && (spins & 4095u) == 0 && *((volatile int*)err) != 0) return false;
+            if (err && dt > kErrPollNs && (spins & 4095u) == 0 && *((volatile int*)err) != 0) return false;
             if (dt > kWaitBudgetNs) {
-                atomicCAS(err, 0, -6 /* LLAMA_ERR_DEVICE_TIMEOUT */);
+                if (err) atomicCAS(err, 0, -6 /* LLAMA_ERR_DEVICE_TIMEOUT */);
                 return false;
             }
         }

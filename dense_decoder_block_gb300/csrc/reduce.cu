@@ -164,12 +164,10 @@ template <int S>
 static cudaError_t launch_resid_norm(const ReduceArgs& r, const void* gain, void* hn, float eps, cudaStream_t s) {
     auto kern = k_reduce_resid_norm<S>;
     if (S > 8) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
+        cudaError_t e = kernel_setup_once((const void*)kern, [](const void* k) {
+            return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        });
+        if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, r.M);

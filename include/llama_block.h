@@ -204,7 +204,10 @@ int llama_embed(const int32_t* ids, int n_tokens, const void* w_embed, int vocab
  * lowest index ("How Llama 3.1 Generates the Next Token", Unembedding and
  * Sampling: greedy choice).  h [batch, d_model] (stride h_stride elements
  * between rows), g_final [d_model], w_out [vocab, d_model].  logits, if not
- * NULL, receives [batch, vocab] fp32.  workspace: llama_lmhead_workspace_bytes. */
+ * NULL, receives [batch, vocab] fp32.  workspace: llama_lmhead_workspace_bytes
+ * (it also holds the call's device error word).  Every wait inside the kernels
+ * is bounded; if one expires, ids[b] receives LLAMA_ERR_DEVICE_TIMEOUT (a
+ * negative value, never a token id) for every row and the logits are undefined. */
 size_t llama_lmhead_workspace_bytes(int batch, int d_model, int vocab);
 int llama_lmhead_argmax(const void* h, int batch, int h_stride, const void* g_final, const void* w_out, int vocab,
                         int d_model, float eps, int32_t* ids, float* logits, void* workspace,
@@ -221,7 +224,12 @@ int llama_lmhead_argmax(const void* h, int batch, int h_stride, const void* g_fi
  * array's device address (with that device current) and caches it: make that
  * first call before any stream capture.  Every call shares the one array, which
  * keeps the last call's rows; calls that overlap on the GPU (other streams,
- * other threads) race on it. */
+ * other threads) race on it.  The cached address belongs to the device's
+ * context: after cudaDeviceReset (or a reset of the primary context) the
+ * library must be reloaded before this call is used again.  A device wait that
+ * expires is reported as in llama_lmhead_argmax: ids[b] =
+ * LLAMA_ERR_DEVICE_TIMEOUT (the error word is a second library-owned device
+ * int, cleared by every call). */
 int llama_lmhead_argmax_noalloc(const void* h, int batch, int h_stride, const void* g_final, const void* w_out,
                                 int vocab, int d_model, float eps, int32_t* ids, float* logits, void* stream);
 

@@ -20,7 +20,7 @@ The computation, per sequence b, token t at absolute position p
   8. u = R(R(SiLU(R(hn W1^T))) * R(hn W3^T))                      SwiGLU
   9. y = R(h + R(u W2^T))                                         residual
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * bf16 rounding points as above (the unfused PyTorch order of the snippets);
   * a query at absolute position p sees keys 0..p (its own row included);
   * RoPE angles in float64 (the page's listing uses float32 angles);
