@@ -20,11 +20,12 @@ import torch
 from . import _native
 from ._native import (LLAMA_BF16, LLAMA_F32, LLAMA_OK, LLAMA_ERR_INVALID_ARG, LLAMA_ERR_UNSUPPORTED_DIMS,
                       LLAMA_ERR_POS_RANGE, LLAMA_ERR_WORKSPACE, LLAMA_ERR_CUDA, LLAMA_ERR_DEVICE_TIMEOUT,
-                      llama_block_dims, llama_block_weights, llama_kv_cache)
+                      llama_block_dims, llama_block_weights, llama_kv_cache, llama_rope_scaling)
 
 __all__ = [
-    "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_destroy",
-    "llama_block_workspace_bytes", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
+    "LlamaBlock", "LlamaError", "KVCache", "lib", "llama_block_create", "llama_block_create_scaled",
+    "llama_block_destroy",
+    "llama_block_workspace_bytes", "llama_block_workspace_offsets", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
     "llama_block_decode_devpos", "llama_block_decode_seqpos",
     "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
     "llama_embed", "llama_lmhead_workspace_bytes",
@@ -95,12 +96,34 @@ def llama_block_create(dims: llama_block_dims, weights: llama_block_weights) -> 
     return h
 
 
+def llama_block_create_scaled(dims: llama_block_dims, weights: llama_block_weights,
+                              scaling: Optional[llama_rope_scaling]) -> C.c_void_p:
+    h = C.c_void_p()
+    rc = lib().llama_block_create_scaled(C.byref(dims), C.byref(weights),
+                                         C.byref(scaling) if scaling is not None else None, C.byref(h))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_block_create_scaled")
+    return h
+
+
 def llama_block_destroy(h) -> None:
     lib().llama_block_destroy(h)
 
 
 def llama_block_workspace_bytes(h, batch: int, tokens: int) -> int:
     return int(lib().llama_block_workspace_bytes(h, batch, tokens))
+
+
+INTERMEDIATES = ("xn", "q", "o", "h", "hn", "u")
+
+
+def llama_block_workspace_offsets(h, batch: int, tokens: int):
+    """Byte offsets in the workspace of xn, q, o, h, hn, u for a call of this shape."""
+    arr = (C.c_size_t * _native.LLAMA_BLOCK_INTERMEDIATES)()
+    rc = lib().llama_block_workspace_offsets(h, batch, tokens, arr, _native.LLAMA_BLOCK_INTERMEDIATES)
+    if rc != _native.LLAMA_BLOCK_INTERMEDIATES:
+        raise LlamaError(rc, "llama_block_workspace_offsets")
+    return dict(zip(INTERMEDIATES, (int(v) for v in arr)))
 
 
 def llama_block_last_error(h) -> str:
@@ -215,7 +238,10 @@ class LlamaBlock:
                                        max_seq, dims.eps, dims.rope_theta, _dtype_code(dt))
         names = ("g_attn", "wq", "wk", "wv", "wo", "g_ffn", "w_gate", "w_up", "w_down")
         self.c_w = llama_block_weights(*[_ptr(self._keep[n]) for n in names])
-        self.h = llama_block_create(self.c_dims, self.c_w)
+        sc = getattr(dims, "rope_scaling", None)   # (factor, low, high, original context) or None
+        self.c_scaling = None if sc is None else llama_rope_scaling(float(sc[0]), float(sc[1]), float(sc[2]),
+                                                                    int(sc[3]))
+        self.h = llama_block_create_scaled(self.c_dims, self.c_w, self.c_scaling)
 
     def __del__(self):
         h = getattr(self, "h", None)
@@ -229,6 +255,21 @@ class LlamaBlock:
     def workspace(self, batch: int, tokens: int, device=None) -> torch.Tensor:
         n = self.workspace_bytes(batch, tokens)
         return torch.empty(n, dtype=torch.uint8, device=device or self._keep["wq"].device)
+
+    def intermediates(self, ws: torch.Tensor, batch: int, tokens: int) -> Dict[str, torch.Tensor]:
+        """Views of the workspace `ws` of a finished call (batch, tokens) as the block's
+        intermediates xn, q, o, h, hn, u, each [batch * tokens, width]."""
+        off = llama_block_workspace_offsets(self.h, batch, tokens)
+        d = self.dims
+        dt = self._keep["wq"].dtype
+        es = torch.finfo(dt).bits // 8
+        widths = {"xn": d.d_model, "q": d.q_dim, "o": d.q_dim, "h": d.d_model, "hn": d.d_model, "u": d.d_ff}
+        M = batch * tokens
+        out = {}
+        for name, width in widths.items():
+            nbytes = M * width * es
+            out[name] = ws[off[name]:off[name] + nbytes].view(dt).view(M, width)
+        return out
 
     def prefill(self, x, kv: KVCache, y, ws, stream=None):
         B, T = x.shape[0], x.shape[1]

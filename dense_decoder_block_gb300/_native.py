@@ -16,6 +16,7 @@ LLAMA_ERR_CUDA = -5
 LLAMA_ERR_DEVICE_TIMEOUT = -6
 LLAMA_F32 = 0
 LLAMA_BF16 = 1
+LLAMA_BLOCK_INTERMEDIATES = 6
 
 ERROR_NAMES = {
     LLAMA_ERR_INVALID_ARG: "LLAMA_ERR_INVALID_ARG",
@@ -37,6 +38,11 @@ class llama_block_weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("g_attn", "wq", "wk", "wv", "wo", "g_ffn", "w_gate", "w_up", "w_down")]
 
 
+class llama_rope_scaling(C.Structure):
+    _fields_ = [("factor", C.c_float), ("low_freq_factor", C.c_float), ("high_freq_factor", C.c_float),
+                ("original_max_pos", C.c_int32)]
+
+
 class llama_kv_cache(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("batch", C.c_int32), ("max_seq", C.c_int32)]
 
@@ -45,8 +51,11 @@ class llama_kv_cache(C.Structure):
 SIGNATURES = {
     "llama_block_create": (C.c_int, [C.POINTER(llama_block_dims), C.POINTER(llama_block_weights),
                                      C.POINTER(C.c_void_p)]),
+    "llama_block_create_scaled": (C.c_int, [C.POINTER(llama_block_dims), C.POINTER(llama_block_weights),
+                                            C.POINTER(llama_rope_scaling), C.POINTER(C.c_void_p)]),
     "llama_block_destroy": (None, [C.c_void_p]),
     "llama_block_workspace_bytes": (C.c_size_t, [C.c_void_p, C.c_int, C.c_int]),
+    "llama_block_workspace_offsets": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_size_t), C.c_int]),
     "llama_block_prefill": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.POINTER(llama_kv_cache),
                                       C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "llama_block_prefill_at": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,

@@ -406,13 +406,40 @@ int validate_dims(const llama_block_dims* d, std::string* why) {
 
 // ======================================================================== ABI
 
+namespace {
+// Radians per position of RoPE pair i: theta^(-2i/head_dim), or Llama 3.1's
+// long-context schedule (fast band unchanged, slow band / factor, blend between),
+// in fp64.
+double rope_omega(const llama_block_dims& d, const llama_rope_scaling* sc, int i) {
+    const double omega = std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
+    if (!sc) return omega;
+    const double pi = 3.14159265358979323846;
+    const double wavelength = 2.0 * pi / omega;
+    const double fast_edge = (double)sc->original_max_pos / sc->high_freq_factor;
+    const double slow_edge = (double)sc->original_max_pos / sc->low_freq_factor;
+    if (wavelength < fast_edge) return omega;
+    if (wavelength > slow_edge) return omega / sc->factor;
+    const double s = ((double)sc->original_max_pos / wavelength - sc->low_freq_factor) /
+                     ((double)sc->high_freq_factor - sc->low_freq_factor);
+    return (1.0 - s) * omega / sc->factor + s * omega;
+}
+}  // namespace
+
 extern "C" int llama_block_create(const llama_block_dims* dims, const llama_block_weights* w, llama_block* out) {
+    return llama_block_create_scaled(dims, w, nullptr, out);
+}
+
+extern "C" int llama_block_create_scaled(const llama_block_dims* dims, const llama_block_weights* w,
+                                         const llama_rope_scaling* scaling, llama_block* out) {
     if (!out) return LLAMA_ERR_INVALID_ARG;
     *out = nullptr;
     std::string why;
     int rc = validate_dims(dims, &why);
     if (rc != LLAMA_OK) return rc;
     if (!w) return LLAMA_ERR_INVALID_ARG;
+    if (scaling && !(scaling->factor >= 1.f && scaling->low_freq_factor > 0.f &&
+                     scaling->high_freq_factor > scaling->low_freq_factor && scaling->original_max_pos > 0))
+        return LLAMA_ERR_INVALID_ARG;
     const void* ptrs[9] = {w->g_attn, w->wq, w->wk, w->wv, w->wo, w->g_ffn, w->w_gate, w->w_up, w->w_down};
     for (const void* p : ptrs)
         if (!p || !aligned16(p)) return LLAMA_ERR_INVALID_ARG;
@@ -442,13 +469,14 @@ extern "C" int llama_block_create(const llama_block_dims* dims, const llama_bloc
         b->seg_kb[2] = choose_seg_kb(d.d_ff / 128, d.d_model / 64, n_sm);
         b->seg_kb[3] = choose_seg_kb(d.d_model / 128, d.d_ff / 64, n_sm);
     }
-    // cos/sin of p * theta^(-2i/head_dim), computed in fp64, stored fp32, padded to 64 pairs
+    // cos/sin of p * omega_i, computed in fp64, stored fp32, padded to 64 pairs
     const size_t n = (size_t)d.max_seq * kRopeMaxPairs;
     std::vector<float> hc(n, 1.f), hs(n, 0.f);
+    std::vector<double> omega(d.head_dim / 2);
+    for (int i = 0; i < d.head_dim / 2; ++i) omega[i] = rope_omega(d, scaling, i);
     for (int p = 0; p < d.max_seq; ++p)
         for (int i = 0; i < d.head_dim / 2; ++i) {
-            const double omega = std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
-            const double ang = (double)p * omega;
+            const double ang = (double)p * omega[i];
             hc[(size_t)p * kRopeMaxPairs + i] = (float)std::cos(ang);
             hs[(size_t)p * kRopeMaxPairs + i] = (float)std::sin(ang);
         }
@@ -477,6 +505,15 @@ extern "C" size_t llama_block_workspace_bytes(llama_block b, int batch, int toke
     if (!b || batch <= 0 || tokens <= 0) return 0;
     // decode needs the attention partials; prefill does not
     return layout(b, batch, tokens, nullptr, tokens == 1).total;
+}
+
+extern "C" int llama_block_workspace_offsets(llama_block b, int batch, int tokens, size_t* offsets, int n) {
+    if (!b || batch <= 0 || tokens <= 0 || !offsets || n < LLAMA_BLOCK_INTERMEDIATES) return LLAMA_ERR_INVALID_ARG;
+    uint8_t* const base = (uint8_t*)(uintptr_t)kAlign;   // any aligned base: offsets are base-relative
+    const Ws w = layout(b, batch, tokens, base, tokens == 1);
+    const void* at[LLAMA_BLOCK_INTERMEDIATES] = {w.xn, w.q, w.o, w.h, w.hn, w.u};
+    for (int i = 0; i < LLAMA_BLOCK_INTERMEDIATES; ++i) offsets[i] = (size_t)((const uint8_t*)at[i] - base);
+    return LLAMA_BLOCK_INTERMEDIATES;
 }
 
 extern "C" int llama_block_prefill(llama_block b, const void* x, int batch, int tokens, const llama_kv_cache* kv,

@@ -94,12 +94,54 @@ typedef struct llama_block_s* llama_block;
  * (the table and a 4-byte error word).  On success *out holds the handle. */
 int llama_block_create(const llama_block_dims* dims, const llama_block_weights* w, llama_block* out);
 
+/* Llama 3.1's long-context RoPE schedule ("How Llama 3.1 Generates the Next
+ * Token", Why use different rotation speeds?: the fastest rotations unchanged,
+ * the slowest slowed by a factor, a middle range blended; "Llama 3.1 70B",
+ * highlights: llama3 x8).  Pair i turns omega_i = rope_theta^(-2i/head_dim)
+ * radians per position in the base schedule; with wavelength 2 pi / omega_i:
+ *   wavelength < original_max_pos / high_freq_factor  ->  omega_i (unchanged)
+ *   wavelength > original_max_pos / low_freq_factor   ->  omega_i / factor
+ *   otherwise  (1 - s) omega_i / factor + s omega_i,
+ *              s = (original_max_pos / wavelength - low_freq_factor)
+ *                  / (high_freq_factor - low_freq_factor).
+ * The pages give the factor (8) but not the band edges; Llama 3.1's released
+ * configuration is factor 8, low 1, high 4, original_max_pos 8192.  Requires
+ * factor >= 1, 0 < low_freq_factor < high_freq_factor, original_max_pos > 0. */
+typedef struct {
+    float factor, low_freq_factor, high_freq_factor;
+    int32_t original_max_pos;
+} llama_rope_scaling;
+
+/* llama_block_create with the long-context RoPE schedule above in the handle's
+ * cos/sin table (scaling = NULL: the base schedule, same as
+ * llama_block_create).  Only the table differs; every call on the handle then
+ * rotates q and k with the scaled angles.  LLAMA_ERR_INVALID_ARG for scaling
+ * values outside the ranges above. */
+int llama_block_create_scaled(const llama_block_dims* dims, const llama_block_weights* w,
+                              const llama_rope_scaling* scaling, llama_block* out);
+
 /* Free the handle's table, error word and host state.  NULL is a no-op. */
 void llama_block_destroy(llama_block blk);
 
 /* Bytes of device workspace that prefill (tokens = T) or decode (tokens = 1)
  * needs for batch B.  Returns 0 for invalid arguments. */
 size_t llama_block_workspace_bytes(llama_block blk, int batch, int tokens);
+
+/* Where a call's intermediates sit in its workspace, for inspection after the
+ * call (stage-by-stage checks, callers that reuse a stage's output).  For a
+ * call with this batch and tokens (tokens = 1: decode), offsets[i] receives the
+ * byte offset from the workspace start of
+ *   [0] xn  = RMSNorm_1(x)                    [batch*tokens, d_model]
+ *   [1] q   after RoPE                        [batch*tokens, n_heads*head_dim]
+ *   [2] o   attention output, heads merged    [batch*tokens, n_heads*head_dim]
+ *   [3] h   = x + o Wo^T                      [batch*tokens, d_model]
+ *   [4] hn  = RMSNorm_2(h)                    [batch*tokens, d_model]
+ *   [5] u   = SiLU(hn W_gate^T) * (hn W_up^T) [batch*tokens, d_ff]
+ * row-major, element type dims.dtype ("Llama 3.1 70B", Transformer layer: the
+ * steps of the block in order).  n must be at least LLAMA_BLOCK_INTERMEDIATES.
+ * Returns LLAMA_BLOCK_INTERMEDIATES, or LLAMA_ERR_INVALID_ARG. */
+#define LLAMA_BLOCK_INTERMEDIATES 6
+int llama_block_workspace_offsets(llama_block blk, int batch, int tokens, size_t* offsets, int n);
 
 /* Causal prefill of T tokens per sequence at positions 0..T-1.
  *   x  [batch, T, d]   input residual stream

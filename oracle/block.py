@@ -64,10 +64,47 @@ def rope_frequencies(head_dim: int, theta: float) -> np.ndarray:
     return theta ** (-2.0 * i / head_dim)
 
 
-def rope_angles(positions: Sequence[int], head_dim: int, theta: float) -> np.ndarray:
-    """phi[m, i] = m * omega_i ([Next] "What exactly are we rotating?"), float64."""
+def rope_frequencies_scaled(head_dim: int, theta: float, factor: float, low_freq_factor: float,
+                            high_freq_factor: float, original_context: int) -> np.ndarray:
+    """Llama 3.1's long-context adjustment of the base schedule ([Next] "Why use
+    different rotation speeds?": the fastest rotations stay as they are, the slowest
+    turn ``factor`` times more slowly, a middle range is blended between the two;
+    [70B] highlights: "llama3 x8").
+
+    The pages name the three bands but not their edges.  Reading taken: a pair's
+    band follows from its wavelength 2 pi / omega_i, measured against the original
+    context length: shorter than original_context / high_freq_factor -> unchanged;
+    longer than original_context / low_freq_factor -> omega_i / factor; in between,
+    omega' = (1 - s) omega_i / factor + s omega_i with
+    s = (original_context / wavelength - low_freq_factor) / (high_freq_factor - low_freq_factor),
+    which is 1 at the fast edge and 0 at the slow edge (a linear blend in the
+    number of turns per original context).  Llama 3.1's released configuration is
+    factor 8, low 1, high 4, original context 8192.
+    """
+    omega = rope_frequencies(head_dim, theta)
+    wavelength = 2.0 * math.pi / omega
+    fast_edge = original_context / high_freq_factor
+    slow_edge = original_context / low_freq_factor
+    out = np.empty_like(omega)
+    for i, (w, lam) in enumerate(zip(omega, wavelength)):
+        if lam < fast_edge:
+            out[i] = w
+        elif lam > slow_edge:
+            out[i] = w / factor
+        else:
+            s = (original_context / lam - low_freq_factor) / (high_freq_factor - low_freq_factor)
+            out[i] = (1.0 - s) * w / factor + s * w
+    return out
+
+
+def rope_angles(positions: Sequence[int], head_dim: int, theta: float, scaling=None) -> np.ndarray:
+    """phi[m, i] = m * omega_i ([Next] "What exactly are we rotating?"), float64.
+    ``scaling`` = (factor, low_freq_factor, high_freq_factor, original_context)
+    selects the long-context schedule of ``rope_frequencies_scaled``."""
     pos = np.asarray(positions, dtype=np.float64)
-    return np.outer(pos, rope_frequencies(head_dim, theta))
+    omega = rope_frequencies(head_dim, theta) if scaling is None else \
+        rope_frequencies_scaled(head_dim, theta, *scaling)
+    return np.outer(pos, omega)
 
 
 def rope_rotate(x: np.ndarray, angles: np.ndarray) -> np.ndarray:
@@ -171,7 +208,7 @@ def block_forward(x: np.ndarray, w: Dict[str, np.ndarray], g: Dict[str, np.ndarr
     hq, hkv, dh = dims.n_heads, dims.n_kv_heads, dims.head_dim
     rows = np.arange(T) if out_rows is None else np.asarray(out_rows)
     positions = np.arange(start_pos, start_pos + T)
-    ang = rope_angles(positions, dh, dims.rope_theta)               # [T, dh/2]
+    ang = rope_angles(positions, dh, dims.rope_theta, getattr(dims, "rope_scaling", None))   # [T, dh/2]
     ys = []
     for b in range(B):
         xn = rmsnorm(x[b], g["g_attn"], dims.eps, rnd)
@@ -239,7 +276,7 @@ def stack_forward(x: np.ndarray, layers, g_final, w_out, dims, caches, start_pos
 
 
 __all__ = [
-    "rmsnorm", "rope_frequencies", "rope_angles", "rope_rotate", "causal_gqa_attention",
+    "rmsnorm", "rope_frequencies", "rope_frequencies_scaled", "rope_angles", "rope_rotate", "causal_gqa_attention",
     "silu", "swiglu_hidden", "block_forward", "embed", "lm_head_logits", "greedy",
     "stack_forward", "round_bf16", "identity",
 ]

@@ -8,6 +8,7 @@ import torch
 import workloads
 from oracle import block as ob
 from oracle.bf16 import round_bf16, identity
+from tests.parity_log import record_parity  # noqa: F401  (re-exported for the tests)
 
 BF16_TOL = 2e-2
 F32_TOL = 1e-4
@@ -48,8 +49,8 @@ def check_bf16_output(got: np.ndarray, exact: np.ndarray, tol: float = BF16_TOL,
     beyond = float(np.max(np.maximum(diff - ULPS * bf16_ulp(ref), 0.0))) / rms
     rms_err = float(np.sqrt(np.mean(diff ** 2))) / rms
     frac = float(np.count_nonzero(diff)) / diff.size
-    print(f"[parity] {what}: max|err|/rms = {raw:.3e}, beyond {ULPS} ulps = {beyond:.3e}, rms err = {rms_err:.2e}, "
-          f"differing {100 * frac:.2f}%")
+    record_parity(f"[parity] {what}: max|err|/rms = {raw:.3e}, beyond {ULPS} ulps = {beyond:.3e}, "
+                  f"rms err = {rms_err:.2e}, differing {100 * frac:.2f}%")
     assert beyond <= tol, f"{what}: error beyond {ULPS} bf16 ulps = {beyond:.4e} x rms > {tol}"
     assert rms_err <= tol / 4, f"{what}: rms error {rms_err:.3e} > {tol / 4}"
     return raw, frac

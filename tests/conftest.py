@@ -25,3 +25,13 @@ def has_gpu():
         return torch.cuda.is_available()
     except Exception:  # pragma: no cover
         return False
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Repeat the parity figures the GPU tests printed (raw max|err|/rms of every
+    bf16 comparison, stage-by-stage agreement) at the end of the run."""
+    from tests import parity_log
+    if parity_log.LINES:
+        terminalreporter.section("parity figures")
+        for line in parity_log.LINES:
+            terminalreporter.write_line(line)

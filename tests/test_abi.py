@@ -66,6 +66,7 @@ def test_null_arguments_are_rejected_without_a_gpu(lib_path):
     assert lib.llama_block_decode_seqpos(None, None, 1, None, None, None, None, 0, None) == \
         _native.LLAMA_ERR_INVALID_ARG
     assert lib.llama_block_launch_count(None) == 0
+    assert lib.llama_block_workspace_offsets(None, 1, 1, None, 6) == _native.LLAMA_ERR_INVALID_ARG
     dev = ctypes.c_void_p(1)
     assert lib.llama_device_ptr_of_host(None, ctypes.byref(dev)) == _native.LLAMA_ERR_INVALID_ARG
     assert lib.llama_block_set_stage_events(None, None, 0) == _native.LLAMA_ERR_INVALID_ARG

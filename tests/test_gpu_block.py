@@ -7,6 +7,7 @@ import torch
 
 import workloads
 from oracle import block as ob
+from oracle.bf16 import round_bf16
 from tests.blockrun import (BF16_TOL, F32_TOL, check_bf16_output, gpu_block, oracle_weights, rel_err, rnd_for,
                             run_decode, run_prefill)
 
@@ -238,6 +239,24 @@ def test_bf16_chunked_prefill_bit_identical_to_one_prefill(dims, cuts):
     assert torch.equal(torch.cat(ys, dim=1), y_full)
     assert torch.equal(kc[:, :, :T], kc_full[:, :, :T]) and torch.equal(vc[:, :, :T], vc_full[:, :, :T])
     assert torch.isnan(kc[:, :, T:]).all() and torch.isnan(vc[:, :, T:]).all()
+    # the same chunks through the oracle: block_forward at each start position on its
+    # own cache ("Llama 3 8B · Prepare Q, K, V", decode mode: the new tokens attend to
+    # the cached rows and to themselves)
+    w, g = oracle_weights(inp)
+    kr = np.zeros((B, dims.n_kv_heads, max_seq, dims.head_dim))
+    vr = np.zeros_like(kr)
+    x64 = workloads.to_numpy64(inp.x)
+    exact, k_ex, v_ex = [], [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        tr = {}
+        ob.block_forward(x64[:, a:b], w, g, dims, kr, vr, a, rnd_for(inp.dtype), trace=tr)
+        exact.append(tr["y_exact"])
+        k_ex.append(tr["k_exact"])
+        v_ex.append(tr["v_exact"])
+    check_bf16_output(workloads.to_numpy64(torch.cat(ys, dim=1)), np.concatenate(exact, axis=1),
+                      what="chunked prefill y")
+    check_bf16_output(workloads.to_numpy64(kc[:, :, :T]), np.concatenate(k_ex, axis=2), what="chunked k cache")
+    check_bf16_output(workloads.to_numpy64(vc[:, :, :T]), np.concatenate(v_ex, axis=2), what="chunked v cache")
 
 
 def test_fp32_chunked_prefill_matches_oracle():
@@ -343,6 +362,23 @@ def test_decode_per_sequence_positions_bit_identical_to_prefill():
         assert torch.equal(y[b, 0], y_pf[b, p]), f"sequence {b} at {p}"
         assert torch.equal(kc[b, :, p], kc_pf[b, :, p]) and torch.equal(vc[b, :, p], vc_pf[b, :, p])
         assert torch.isnan(kc[b, :, p + 1:]).all() and torch.isnan(vc[b, :, p + 1:]).all()
+    # against the oracle: each sequence run alone up to its own position, its row p kept
+    w, g = oracle_weights(inp)
+    x64 = workloads.to_numpy64(inp.x)
+    y_ex, k_ex, v_ex = [], [], []
+    for b, p in enumerate(pos):
+        kr = np.zeros((1, MID.n_kv_heads, p + 1, MID.head_dim))
+        vr = np.zeros_like(kr)
+        tr = {}
+        ob.block_forward(x64[b:b + 1, :p + 1], w, g, MID, kr, vr, 0, rnd_for(inp.dtype), out_rows=[p], trace=tr)
+        y_ex.append(tr["y_exact"][0, 0])
+        k_ex.append(tr["k_exact"][0, :, p])
+        v_ex.append(tr["v_exact"][0, :, p])
+    check_bf16_output(workloads.to_numpy64(y[:, 0]), np.stack(y_ex), what="per-sequence decode y")
+    check_bf16_output(workloads.to_numpy64(torch.stack([kc[b, :, p] for b, p in enumerate(pos)])), np.stack(k_ex),
+                      what="per-sequence decode k rows")
+    check_bf16_output(workloads.to_numpy64(torch.stack([vc[b, :, p] for b, p in enumerate(pos)])), np.stack(v_ex),
+                      what="per-sequence decode v rows")
     # a position outside the cache is recorded by the kernels
     bad = torch.tensor([5, 127, max_seq, 257, 300], dtype=torch.int32, device=dev)
     blk.decode_seqpos(x_dec, kv, bad, y, blk.workspace(B, 1))
@@ -360,3 +396,44 @@ def test_decode_per_sequence_positions_unsupported_shape():
     with pytest.raises(ddb.LlamaError):
         blk.decode_seqpos(x, kv, torch.tensor([1, 2], dtype=torch.int32, device=dev), torch.empty_like(x),
                           blk.workspace(2, 1))
+
+
+def test_bf16_scaled_rope_matches_oracle():
+    """Llama 3.1's long-context RoPE schedule (llama_block_create_scaled): a decode step
+    at position 6000 and a 20-token chunk at 6001 on a cache of 6000 rows, against the
+    oracle with the same schedule; the slow pairs move far enough at this range that
+    the unscaled schedule gives a clearly different result."""
+    import dataclasses
+    dims = dataclasses.replace(MID, rope_scaling=workloads.LLAMA31_ROPE_SCALING)
+    P, T, B = 6000, 20, 2
+    max_seq = P + T + 1 + 7
+    inp = workloads.make_block_inputs(dims, B, T + 1, cache_len=P, max_seq=max_seq, random_gains=True)
+    blk, ddb = gpu_block(inp, max_seq)
+    dev = torch.device("cuda:0")
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    kv = ddb.KVCache(kc, vc)
+    x = inp.x.to(dev)
+    y_dec = run_decode(blk, ddb, x[:, :1].contiguous(), kc, vc, P)
+    y_chk = torch.empty_like(x[:, 1:])
+    blk.prefill_at(x[:, 1:].contiguous(), kv, P + 1, y_chk, blk.workspace(B, T))
+    torch.cuda.synchronize()
+    assert blk.poll_error() == 0
+    w, g = oracle_weights(inp)
+    x64 = workloads.to_numpy64(inp.x)
+
+    def oracle(d):
+        kr = workloads.to_numpy64(inp.k_cache).copy()
+        vr = workloads.to_numpy64(inp.v_cache).copy()
+        t0, t1 = {}, {}
+        ob.block_forward(x64[:, :1], w, g, d, kr, vr, P, rnd_for(inp.dtype), trace=t0)
+        ob.block_forward(x64[:, 1:], w, g, d, kr, vr, P + 1, rnd_for(inp.dtype), trace=t1)
+        return (np.concatenate([t0["y_exact"], t1["y_exact"]], axis=1),
+                np.concatenate([t0["k_exact"], t1["k_exact"]], axis=2))
+
+    y_ex, k_ex = oracle(dims)
+    got = workloads.to_numpy64(torch.cat([y_dec, y_chk], dim=1))
+    check_bf16_output(got, y_ex, what="scaled-RoPE y (decode at 6000, chunk at 6001)")
+    check_bf16_output(workloads.to_numpy64(kc[:, :, P:P + T + 1]), k_ex, what="scaled-RoPE k rows")
+    _, k_plain = oracle(MID)
+    k_got = workloads.to_numpy64(kc[:, :, P:P + T + 1])
+    assert rel_err(k_got, round_bf16(k_plain)) > 0.1   # the unscaled schedule is far off

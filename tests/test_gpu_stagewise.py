@@ -1,0 +1,275 @@
+"""Stage-by-stage parity of the bf16 block at the 8B shape.
+
+Each stage of the GPU path is fed to the oracle's matching step with the GPU's
+own bf16 inputs (read back from the workspace through
+llama_block_workspace_offsets), so that a difference cannot come from upstream.
+The block's stages round to bf16 at the points the oracle rounds ("Llama 3.1
+70B": RMSNorm reference implementation, GQA, Residual add, SwiGLU MLP).  The
+GPU accumulates each projection in fp32 on the tensor cores where the oracle
+uses fp64, so a value that lies within that accumulation error of a bf16
+rounding boundary may be rounded to the other neighbour.  For every stage this
+test asserts:
+
+  * the share of elements equal to the oracle's step bit for bit: at least
+    99.9% for a stage with one rounded projection, 99% for the SwiGLU stage
+    (three rounded values feed its output);
+  * every element is explained by that arithmetic: it lies between the bf16
+    neighbours of the lowest and the highest value the stage can take when each
+    projection output is anywhere within its fp32 accumulation bound
+    2^-20 * sqrt(K * sum_k (x_k w_k)^2) of the exact dot product (about forty
+    times the typical fp32 accumulation error), each elementwise fp32 step within
+    a few fp32 ulps (the RMSNorm scale, the fp32 cos/sin table of the rotation,
+    SiLU), and each of the stage's rounding points takes either bf16 neighbour.
+    For h = R(x + R(o Wo^T)), for instance, h must lie in
+    [lo(x + lo(o Wo^T - bound)), hi(x + hi(o Wo^T + bound))].
+
+The attention output is the exception the reading of the softmax weights
+implies: the tensor-core kernels round each weight to bf16 for the PV product
+and the normaliser (the oracle keeps them exact), so o may move by up to
+2^-8 * sum_j P_j |v_j - o| beyond its rounding; that bound is asserted per
+element, and the bit-equal share is printed.
+
+Together these show that the end-to-end differences of the parity tests are
+rounding flips carried through the block, which is what the two-ulp allowance
+of ``check_bf16_output`` stands for.
+"""
+from __future__ import annotations
+
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import block as ob
+from oracle.bf16 import round_bf16, identity
+from tests.blockrun import gpu_block, record_parity
+
+pytestmark = pytest.mark.gpu
+
+DIMS = workloads.LLAMA3_8B
+B, T = 2, 300
+ACC = 2.0 ** -20          # fp32 accumulation bound factor (see the module docstring)
+F32_STEP = 2.0 ** -21     # a few fp32 ulps: elementwise fp32 arithmetic on the GPU
+SILU_MIN_AT = -1.2784645427610738   # SiLU's minimum (z with 1 + e^-z (1 + z) = 0)
+
+
+# ----------------------------------------------------------------------------- bf16 neighbours
+
+def _next_bf16(r: np.ndarray, up: bool) -> np.ndarray:
+    """The bf16 value next to the bf16 value r, towards +inf (up) or -inf."""
+    f = r.astype(np.float32)
+    bits = f.view(np.uint32).astype(np.int64)
+    step = np.int64(1 << 16)
+    away = (f > 0) if up else (f < 0)            # moving away from zero grows the magnitude
+    nb = np.where(away, bits + step, bits - step)
+    zero = f == 0
+    tiny = np.float32(2.0 ** -133) * (1 if up else -1)
+    out = nb.astype(np.uint32).view(np.float32).astype(np.float64)
+    return np.where(zero, tiny, out)
+
+
+def lo_hi(e: np.ndarray):
+    """The two bf16 values bracketing the exact value e (equal when e is one)."""
+    r = round_bf16(e)
+    lo = np.where(r <= e, r, _next_bf16(r, False))
+    hi = np.where(r >= e, r, _next_bf16(r, True))
+    return lo, hi
+
+
+def bf16_span(lo_exact, hi_exact):
+    """Every bf16 value a rounding of a number in [lo_exact, hi_exact] can give."""
+    return lo_hi(lo_exact)[0], lo_hi(hi_exact)[1]
+
+
+def widen(lo, hi, rel):
+    """[lo, hi] grown by rel times its largest magnitude on both sides."""
+    m = np.maximum(np.abs(lo), np.abs(hi)) * rel
+    return lo - m, hi + m
+
+
+def gemm_span(x, w):
+    """Exact x w^T, and the bf16 values its fp32 accumulation can round to."""
+    exact = x @ w.T
+    bound = ACC * np.sqrt(x.shape[-1] * ((x * x) @ (w * w).T))
+    return exact, bf16_span(exact - bound, exact + bound)
+
+
+def corners(f, *spans):
+    """Smallest and largest f over the corners of the boxes (f linear or monotone in each
+    argument over each box)."""
+    vals = [f(*c) for c in itertools.product(*spans)]
+    return np.minimum.reduce(vals), np.maximum.reduce(vals)
+
+
+class Stage:
+    def __init__(self, name: str, got: np.ndarray, primary: np.ndarray):
+        self.name, self.got, self.primary = name, got, primary
+
+    def check(self, lo, hi, min_equal: float = 0.999):
+        eq = float(np.mean(self.got == self.primary))
+        inside = (self.got >= lo) & (self.got <= hi)
+        bad = int(np.count_nonzero(~inside))
+        record_parity(f"[stage] {self.name}: {100 * eq:.3f}% bit-equal to the oracle step, "
+                      f"{bad} of {self.got.size} not explained by rounding flips")
+        assert bad == 0, f"{self.name}: {bad} elements outside what the arithmetic allows"
+        assert eq >= min_equal, f"{self.name}: only {100 * eq:.3f}% bit-equal"
+
+
+def _to64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+# ----------------------------------------------------------------------------- stages
+
+def check_rmsnorm(name, x, g, got):
+    """R(R(x r) g), r computed in fp32 on the GPU."""
+    st = Stage(name, got, ob.rmsnorm(x, g, DIMS.eps, round_bf16))
+    xr = ob.rmsnorm(x, np.ones_like(g), DIMS.eps, identity)       # x * r, exact
+    a_lo, a_hi = bf16_span(*widen(xr, xr, F32_STEP))
+    st.check(*bf16_span(*corners(lambda a: a * g, (a_lo, a_hi))))
+
+
+def check_projection(name, x, w, got):
+    """R(x W^T)."""
+    exact, span = gemm_span(x, w)
+    Stage(name, got, round_bf16(exact)).check(*span)
+
+
+def check_rotated(name, x, w, heads, angles, got):
+    """R(rope(R(x W^T))) with the pair rotation in fp32 from an fp32 cos/sin table.
+    got [M, heads, dh]; angles broadcast against [M, heads, dh/2]."""
+    dh = DIMS.head_dim
+    exact, (p_lo, p_hi) = gemm_span(x, w)
+    exact = exact.reshape(-1, heads, dh)
+    p_lo, p_hi = p_lo.reshape(exact.shape), p_hi.reshape(exact.shape)
+    st = Stage(name, got, round_bf16(ob.rope_rotate(round_bf16(exact), angles)))
+    c, s = np.cos(angles), np.sin(angles)
+    a_sp = (p_lo[..., 0::2], p_hi[..., 0::2])
+    b_sp = (p_lo[..., 1::2], p_hi[..., 1::2])
+    mag = np.maximum(np.abs(a_sp[0]), np.abs(a_sp[1])) + np.maximum(np.abs(b_sp[0]), np.abs(b_sp[1]))
+    lo, hi = np.empty_like(exact), np.empty_like(exact)
+    for k, f in ((0, lambda a, b: a * c - b * s), (1, lambda a, b: a * s + b * c)):
+        l, h = corners(f, a_sp, b_sp)
+        l, h = bf16_span(l - 4 * F32_STEP * mag, h + 4 * F32_STEP * mag)
+        lo[..., k::2], hi[..., k::2] = l, h
+    st.check(lo, hi)
+
+
+def check_residual(name, resid, x, w, got):
+    """R(resid + R(x W^T))."""
+    exact, (b_lo, b_hi) = gemm_span(x, w)
+    st = Stage(name, got, round_bf16(resid + round_bf16(exact)))
+    st.check(*bf16_span(*widen(resid + b_lo, resid + b_hi, F32_STEP)))
+
+
+def check_swiglu(name, hn, w_gate, w_up, got):
+    """R(R(SiLU(R(hn W1^T))) R(hn W3^T)); SiLU in fp32 on the GPU."""
+    st = Stage(name, got, ob.swiglu_hidden(hn, w_gate, w_up, round_bf16))
+    _, (g_lo, g_hi) = gemm_span(hn, w_gate)
+    _, up_sp = gemm_span(hn, w_up)
+    s_lo, s_hi = corners(ob.silu, (g_lo, g_hi))
+    dip = (g_lo < SILU_MIN_AT) & (g_hi > SILU_MIN_AT)            # SiLU turns around inside the span
+    s_lo = np.where(dip, ob.silu(np.float64(SILU_MIN_AT)), s_lo)
+    s_sp = bf16_span(*widen(s_lo, s_hi, F32_STEP))
+    st.check(*bf16_span(*corners(lambda a, b: a * b, s_sp, up_sp)), min_equal=0.99)
+
+
+def check_attention(name, q, kc, vc, positions, got):
+    """o_h = R(softmax(q k^T / sqrt(dh)) V) per sequence, from the GPU's q and cache.
+    q [B, M_b, Hq, dh]; kc, vc [B, Hkv, S, dh]; got [B, M_b, Hq*dh]."""
+    hq, hkv, dh = DIMS.n_heads, DIMS.n_kv_heads, DIMS.head_dim
+    n_rep = hq // hkv
+    L = int(max(positions)) + 1
+    exact = np.stack([ob.causal_gqa_attention(q[b].transpose(1, 0, 2), kc[b, :, :L], vc[b, :, :L], positions,
+                                              identity) for b in range(q.shape[0])])
+    # the spread of the values under the softmax weights: rounding each weight to bf16
+    # (relative 2^-9, plus the exponential's own error) moves o by at most 2^-8 times it
+    spread = np.empty_like(exact)
+    keypos = np.arange(L)
+    for b in range(q.shape[0]):
+        for h in range(hq):
+            g = h // n_rep
+            s = (q[b, :, h] @ kc[b, g, :L].T) / np.sqrt(dh)
+            s = np.where(keypos[None, :] > np.asarray(positions)[:, None], -np.inf, s)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            o = exact[b][:, h * dh:(h + 1) * dh]
+            spread[b][:, h * dh:(h + 1) * dh] = np.einsum("tj,tjd->td", p,
+                                                          np.abs(vc[b, g, None, :L] - o[:, None, :]))
+    ref = round_bf16(exact)
+    lo, hi = bf16_span(exact - 2.0 ** -8 * spread, exact + 2.0 ** -8 * spread)
+    eq = float(np.mean(got == ref))
+    bad = int(np.count_nonzero((got < lo) | (got > hi)))
+    record_parity(f"[stage] {name}: {100 * eq:.3f}% bit-equal to the oracle step (softmax weights rounded to "
+                  f"bf16 on the GPU), {bad} of {got.size} beyond the weight-rounding bound")
+    assert bad == 0, f"{name}: {bad} elements beyond the bound"
+    assert eq >= 0.5, f"{name}: only {100 * eq:.2f}% bit-equal"
+
+
+# ----------------------------------------------------------------------------- the test
+
+@pytest.fixture(scope="module")
+def run():
+    """GPU: prefill B x T at the 8B shape, then one decode step at position T.
+    Returns the inputs, the GPU intermediates of both calls and the GPU cache."""
+    max_seq = T + 8
+    inp = workloads.make_block_inputs(DIMS, B, T + 1, max_seq=max_seq, random_gains=True)
+    blk, ddb = gpu_block(inp, max_seq)
+    dev = torch.device("cuda:0")
+    kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
+    kv = ddb.KVCache(kc, vc)
+    x = inp.x.to(dev)
+    ws_p = blk.workspace(B, T)
+    y_p = torch.empty_like(x[:, :T])
+    blk.prefill(x[:, :T].contiguous(), kv, y_p, ws_p)
+    torch.cuda.synchronize()
+    mid_p = {k: _to64(v) for k, v in blk.intermediates(ws_p, B, T).items()}
+    ws_d = blk.workspace(B, 1)
+    y_d = torch.empty_like(x[:, T:T + 1])
+    blk.decode(x[:, T:T + 1].contiguous(), kv, T, y_d, ws_d)
+    torch.cuda.synchronize()
+    assert blk.poll_error() == 0
+    mid_d = {k: _to64(v) for k, v in blk.intermediates(ws_d, B, 1).items()}
+    w = {k: _to64(v) for k, v in inp.weights.items()}
+    g = {k: _to64(v) for k, v in inp.gains.items()}
+    return dict(x=_to64(inp.x), w=w, g=g, pf=mid_p, dec=mid_d, y_p=_to64(y_p), y_d=_to64(y_d),
+                kc=_to64(kc), vc=_to64(vc))
+
+
+@pytest.mark.parametrize("mode", ["prefill", "decode"])
+def test_each_stage_matches_the_oracle_step(run, mode):
+    r = run
+    w, g = r["w"], r["g"]
+    hq, hkv, dh = DIMS.n_heads, DIMS.n_kv_heads, DIMS.head_dim
+    if mode == "prefill":
+        mid, y, tok = r["pf"], r["y_p"].reshape(B * T, -1), list(range(T))
+        x = r["x"][:, :T].reshape(B * T, -1)
+    else:
+        mid, y, tok = r["dec"], r["y_d"].reshape(B, -1), [T]
+        x = r["x"][:, T:T + 1].reshape(B, -1)
+    nt = len(tok)
+    tag = f"{mode} 8B B={B}" + (f" T={T}" if mode == "prefill" else f" pos={T}")
+    # 1. RMSNorm_1
+    check_rmsnorm(f"{tag} xn", x, g["g_attn"], mid["xn"])
+    xn = mid["xn"]
+    ang = ob.rope_angles(tok, dh, DIMS.rope_theta)                     # [nt, dh/2]
+    ang_m = np.tile(ang, (B, 1))[:, None, :]                           # [B*nt, 1, dh/2]
+    # 2-3. projections, RoPE, cache rows
+    check_rotated(f"{tag} q (rotated)", xn, w["wq"], hq, ang_m, mid["q"].reshape(B * nt, hq, dh))
+    k_got = r["kc"][:, :, tok].transpose(0, 2, 1, 3).reshape(B * nt, hkv, dh)
+    check_rotated(f"{tag} k cache rows", xn, w["wk"], hkv, ang_m, k_got)
+    v_got = r["vc"][:, :, tok].transpose(0, 2, 1, 3).reshape(B * nt, hkv * dh)
+    check_projection(f"{tag} v cache rows", xn, w["wv"], v_got)
+    # 4. attention from the GPU's q and cache
+    check_attention(f"{tag} o", mid["q"].reshape(B, nt, hq, dh), r["kc"], r["vc"], tok,
+                    mid["o"].reshape(B, nt, hq * dh))
+    # 5. O projection + residual
+    check_residual(f"{tag} h", x, mid["o"], w["wo"], mid["h"])
+    # 6. RMSNorm_2
+    check_rmsnorm(f"{tag} hn", mid["h"], g["g_ffn"], mid["hn"])
+    # 7. gate/up + SwiGLU
+    check_swiglu(f"{tag} u", mid["hn"], w["w_gate"], w["w_up"], mid["u"])
+    # 8. down + residual
+    check_residual(f"{tag} y", mid["h"], mid["u"], w["w_down"], y)

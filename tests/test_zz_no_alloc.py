@@ -52,6 +52,26 @@ def test_noalloc_lmhead_matches_workspace_version_twice():
         assert torch.equal(ids, ids_ref), f"call {call}"
 
 
+@pytest.mark.parametrize("batch,d,stride,vocab", [(7, 4096, 4096 + 256, 1024), (32, 8192, 8192, 2048)],
+                         ids=["rows-strided", "scratch-full"])
+def test_noalloc_lmhead_strided_rows_and_full_scratch(batch, d, stride, vocab):
+    """Rows read at a stride larger than d_model (one norm launch per row), and the
+    largest shape the scratch holds (32 rows of 8192)."""
+    import dense_decoder_block_gb300 as ddb
+    ddb.lib()
+    dev = torch.device("cuda:0")
+    h, g, w = (t.to(dev) for t in _inputs(batch, d, vocab, 13))
+    hs = torch.zeros(batch, stride, dtype=torch.bfloat16, device=dev)
+    hs[:, :d] = h
+    ids_ref, logits_ref = _run_with_workspace(ddb, h, g, w, batch, d, vocab)
+    ids = torch.full((batch,), -1, dtype=torch.int32, device=dev)
+    logits = torch.full((batch, vocab), float("nan"), dtype=torch.float32, device=dev)
+    ddb.llama_lmhead_argmax_noalloc(hs, batch, stride, g, w, vocab, d, 1e-5, ids, logits)
+    torch.cuda.synchronize()
+    assert torch.equal(logits, logits_ref)
+    assert torch.equal(ids, ids_ref)
+
+
 def test_noalloc_lmhead_rejects_sizes_beyond_its_scratch():
     import dense_decoder_block_gb300 as ddb
     ddb.lib()
@@ -63,4 +83,11 @@ def test_noalloc_lmhead_rejects_sizes_beyond_its_scratch():
     logits = torch.empty(33, 128, dtype=torch.float32, device=dev)
     with pytest.raises(ddb.LlamaError) as e:
         ddb.llama_lmhead_argmax_noalloc(h, 33, 256, g, w, 128, 256, 1e-5, ids, logits)
+    assert e.value.code == ddb.LLAMA_ERR_WORKSPACE
+    # one row wider than the scratch's 8192 columns
+    h = torch.zeros(1, 8320, dtype=torch.bfloat16, device=dev)
+    g = torch.ones(8320, dtype=torch.bfloat16, device=dev)
+    w = torch.zeros(128, 8320, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ddb.LlamaError) as e:
+        ddb.llama_lmhead_argmax_noalloc(h, 1, 8320, g, w, 128, 8320, 1e-5, ids, logits)
     assert e.value.code == ddb.LLAMA_ERR_WORKSPACE

@@ -43,6 +43,9 @@ class BlockDims:
     d_ff: int
     eps: float = 1e-5
     rope_theta: float = 500000.0
+    # None, or Llama 3.1's long-context RoPE schedule as
+    # (factor, low_freq_factor, high_freq_factor, original_context)
+    rope_scaling: Optional[tuple] = None
 
     @property
     def q_dim(self) -> int:
@@ -65,6 +68,8 @@ TINY = BlockDims(256, 4, 2, 64, 768)
 LLAMA3_8B = BlockDims(4096, 32, 8, 128, 14336)
 LLAMA31_70B = BlockDims(8192, 64, 8, 128, 28672)
 VOCAB = 128256
+# Llama 3.1's released RoPE scaling configuration (the pages name the x8 factor only)
+LLAMA31_ROPE_SCALING = (8.0, 1.0, 4.0, 8192)
 
 
 def _randn(gen: torch.Generator, shape, std: float, dtype: torch.dtype) -> torch.Tensor:
