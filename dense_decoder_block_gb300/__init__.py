@@ -29,7 +29,7 @@ __all__ = [
     "llama_block_decode_devpos", "llama_block_decode_seqpos",
     "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
     "llama_embed", "llama_lmhead_workspace_bytes",
-    "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
+    "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_sample", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
 ]
 
 
@@ -214,6 +214,14 @@ def llama_lmhead_argmax_noalloc(h, batch, h_stride, g_final, w_out, vocab, d_mod
                                            C.c_float(eps), _ptr(ids), _ptr(logits), _stream(stream))
     if rc != LLAMA_OK:
         raise LlamaError(rc, "llama_lmhead_argmax_noalloc")
+
+
+def llama_sample(logits, batch, vocab, temperature, top_k, top_p, uniforms, ids, stream=None) -> None:
+    """ids[b] drawn from softmax(logits[b] / temperature) after top-k / top-p, with uniforms[b]."""
+    rc = lib().llama_sample(_ptr(logits), batch, vocab, C.c_float(temperature), int(top_k), C.c_float(top_p),
+                            _ptr(uniforms), _ptr(ids), _stream(stream))
+    if rc != LLAMA_OK:
+        raise LlamaError(rc, "llama_sample")
 
 
 # ----------------------------------------------------------------------------- convenience

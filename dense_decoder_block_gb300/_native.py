@@ -79,6 +79,8 @@ SIGNATURES = {
                                       C.c_float, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "llama_lmhead_argmax_noalloc": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_int,
                                               C.c_int, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "llama_sample": (C.c_int, [C.c_void_p, C.c_int, C.c_int, C.c_float, C.c_int, C.c_float, C.c_void_p,
+                               C.c_void_p, C.c_void_p]),
     "llama_rmsnorm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float, C.c_int,
                                 C.c_void_p]),
 }

@@ -143,4 +143,8 @@ cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, in
 cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, const int* err,
                                cudaStream_t s);
 
+// Next-token sampling: one CTA per row of fp32 logits [batch, vocab].
+cudaError_t launch_sample(const float* logits, int batch, int vocab, float temperature, int top_k, float top_p,
+                          const float* uniforms, int32_t* ids, cudaStream_t s);
+
 }  // namespace llama

@@ -275,6 +275,25 @@ int llama_lmhead_argmax(const void* h, int batch, int h_stride, const void* g_fi
 int llama_lmhead_argmax_noalloc(const void* h, int batch, int h_stride, const void* g_final, const void* w_out,
                                 int vocab, int d_model, float eps, int32_t* ids, float* logits, void* stream);
 
+/* Next-token sampling from fp32 logits [batch, vocab] ("How Llama 3.1
+ * Generates the Next Token", Temperature, Softmax, Top-k and top-p sampling):
+ * divide by the temperature, softmax over the whole vocabulary, keep the top_k
+ * most probable tokens and the smallest set of most probable tokens whose
+ * probability reaches top_p (both restrictions: the smaller set), renormalise,
+ * and draw: with the kept tokens in order of decreasing logit (equal logits by
+ * increasing index), ids[b] is the first token whose cumulative renormalised
+ * probability exceeds uniforms[b] (device fp32 in [0, 1), one per row, supplied
+ * by the caller; values outside are clamped).  temperature = 0 or top_k = 1
+ * gives the greedy choice (first maximum); top_k = 0 means no top-k limit and
+ * top_p = 1 no top-p limit.  Weights e^{(z - max)/T} are computed in fp32 and
+ * summed exactly in 2^-40 fixed point, top_p and the uniforms are taken to 24
+ * bits: the result does not depend on thread scheduling.  Logits must be finite
+ * (-inf allowed, weight zero).  Requires temperature >= 0, top_k >= 0,
+ * 0 < top_p <= 1, 1 <= vocab <= 2^23, batch <= 65535; otherwise
+ * LLAMA_ERR_INVALID_ARG.  No workspace, nothing allocated. */
+int llama_sample(const float* logits, int batch, int vocab, float temperature, int top_k, float top_p,
+                 const float* uniforms, int32_t* ids, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Step-level entry points (the block's individual steps, for unit tests and
  * for callers that compose their own schedule).  Same conventions as above.

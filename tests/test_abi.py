@@ -67,6 +67,11 @@ def test_null_arguments_are_rejected_without_a_gpu(lib_path):
         _native.LLAMA_ERR_INVALID_ARG
     assert lib.llama_block_launch_count(None) == 0
     assert lib.llama_block_workspace_offsets(None, 1, 1, None, 6) == _native.LLAMA_ERR_INVALID_ARG
+    assert lib.llama_sample(None, 1, 10, ctypes.c_float(1.0), 0, ctypes.c_float(1.0), None, None, None) == \
+        _native.LLAMA_ERR_INVALID_ARG
+    assert lib.llama_sample(None, 1, 10, ctypes.c_float(-1.0), 0, ctypes.c_float(1.0), None, None, None) == \
+        _native.LLAMA_ERR_INVALID_ARG
+    assert lib.llama_block_create_scaled(None, None, None, ctypes.byref(h)) == _native.LLAMA_ERR_INVALID_ARG
     dev = ctypes.c_void_p(1)
     assert lib.llama_device_ptr_of_host(None, ctypes.byref(dev)) == _native.LLAMA_ERR_INVALID_ARG
     assert lib.llama_block_set_stage_events(None, None, 0) == _native.LLAMA_ERR_INVALID_ARG

@@ -1,0 +1,129 @@
+"""GPU parity of the sampling head (llama_sample) against the oracle's sampling
+("How Llama 3.1 Generates the Next Token", Temperature, Softmax, Top-k and top-p
+sampling), given the same uniforms, at batch 32 over the 128,256-token
+vocabulary.
+
+The chosen id is an integer decided by floating point: the kernel's weights are
+fp32 exponentials summed exactly in fixed point, the oracle's are fp64.  The ids
+must be equal wherever the uniform, and the top-p threshold, lie farther than
+1e-5 from a cumulative-probability boundary of the oracle's distribution; at a
+boundary closer than that, either neighbouring token is accepted (and counted).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sampling as sm
+from tests.parity_log import record_parity
+
+pytestmark = pytest.mark.gpu
+
+V = 128256
+B = 32
+MARGIN = 1e-5
+
+
+def _logits(batch, vocab, seed, ties=False):
+    gen = torch.Generator().manual_seed(seed)
+    scale = torch.tensor([1.0, 3.0, 6.0, 0.3])[torch.arange(batch) % 4][:, None]
+    z = torch.randn(batch, vocab, generator=gen) * scale
+    if ties:
+        z = torch.round(z * 2) / 2            # many equal logits
+    u = torch.rand(batch, generator=gen)
+    return z, u
+
+
+def _gpu(z, u, temperature, top_k, top_p):
+    import dense_decoder_block_gb300 as ddb
+    ddb.lib()
+    dev = torch.device("cuda:0")
+    zd, ud = z.to(dev), u.to(dev)
+    ids = torch.full((z.shape[0],), -1, dtype=torch.int32, device=dev)
+    ddb.llama_sample(zd, z.shape[0], z.shape[1], temperature, top_k, top_p, ud, ids)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy()
+
+
+def _allowed(z, temperature, top_k, top_p, u):
+    """(the oracle's id, the ids acceptable when a boundary is within MARGIN)."""
+    want = sm.sample_row(z, temperature, top_k, top_p, u)
+    if temperature == 0.0 or top_k == 1:
+        return want, {want}
+    order = sm.descending_order(z)
+    p = sm.softmax_temperature(z, temperature)[order]
+    n = sm.kept_count(p, top_k, top_p)
+    near = set()
+    if top_p < 1.0:
+        cum_p = np.cumsum(p)
+        if abs(cum_p[n - 1] - top_p) < MARGIN or (n >= 2 and abs(cum_p[n - 2] - top_p) < MARGIN):
+            near.update(range(max(0, n - 2), min(len(z), n + 1)))
+    q = np.cumsum(p[:n] / p[:n].sum())
+    j = int(np.searchsorted(q, u, side="right"))
+    lo_edge = q[j - 1] if j >= 1 else 0.0
+    hi_edge = q[j] if j < n else 1.0
+    if abs(u - lo_edge) < MARGIN or abs(hi_edge - u) < MARGIN:
+        near.update(range(max(0, j - 1), min(n, j + 2)))
+    return want, {want} | {int(order[i]) for i in near}
+
+
+CASES = [
+    # temperature, top_k, top_p
+    (1.0, 0, 1.0),      # plain softmax sampling
+    (0.7, 50, 0.9),     # both restrictions
+    (1.0, 0, 0.9),      # top-p only (Meta's 8B reference: temperature then top-p)
+    (1.3, 5, 1.0),      # top-k only
+    (0.6, 0, 0.5),
+    (0.0, 0, 1.0),      # greedy limit
+    (1.0, 1, 0.9),      # top-k = 1 is greedy too
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("ties", [False, True], ids=["distinct", "ties"])
+def test_sample_matches_oracle(case, ties):
+    temperature, top_k, top_p = CASES[case]
+    z, u = _logits(B, V, 40 + case, ties)
+    got = _gpu(z, u, temperature, top_k, top_p)
+    zn = z.double().numpy()
+    exact, near = 0, 0
+    for b in range(B):
+        want, ok = _allowed(zn[b], temperature, top_k, top_p, float(u[b]))
+        assert int(got[b]) in ok, f"row {b}: got {got[b]}, oracle {want}"
+        exact += int(got[b]) == want
+        near += len(ok) > 1
+    record_parity(f"[sample] T={temperature} top_k={top_k} top_p={top_p} ties={ties}: {exact}/{B} ids equal "
+                  f"to the oracle, {near} rows near a boundary")
+    assert exact >= B - near
+
+
+def test_sample_small_vocab_and_argument_checks():
+    import dense_decoder_block_gb300 as ddb
+    z, u = _logits(3, 1000, 7)
+    got = _gpu(z, u, 0.9, 20, 0.8)
+    zn = z.double().numpy()
+    for b in range(3):
+        _, ok = _allowed(zn[b], 0.9, 20, 0.8, float(u[b]))
+        assert int(got[b]) in ok
+    dev = torch.device("cuda:0")
+    ids = torch.empty(3, dtype=torch.int32, device=dev)
+    for bad in ((-1.0, 0, 1.0), (1.0, -1, 1.0), (1.0, 0, 0.0), (1.0, 0, 1.5)):
+        with pytest.raises(ddb.LlamaError):
+            ddb.llama_sample(z.to(dev), 3, 1000, bad[0], bad[1], bad[2], u.to(dev), ids)
+
+
+def test_sample_uniform_sweep_realises_the_distribution():
+    """One row of 1000 logits drawn with 4096 evenly spaced uniforms: the share of
+    draws per token matches the kept, renormalised probabilities."""
+    gen = torch.Generator().manual_seed(9)
+    z = (torch.randn(1, 1000, generator=gen) * 2).repeat(4096, 1)
+    u = (torch.arange(4096, dtype=torch.float32) + 0.5) / 4096
+    got = _gpu(z, u, 1.0, 0, 0.95)
+    zn = z[0].double().numpy()
+    order = sm.descending_order(zn)
+    p = sm.softmax_temperature(zn, 1.0)[order]
+    n = sm.kept_count(p, 0, 0.95)
+    want = np.zeros(1000)
+    want[order[:n]] = p[:n] / p[:n].sum()
+    freq = np.bincount(got, minlength=1000) / 4096
+    assert np.all(freq[order[n:]] == 0)
+    assert np.max(np.abs(freq - want)) <= 1.5 / 4096
