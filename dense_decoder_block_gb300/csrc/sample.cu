@@ -93,7 +93,7 @@ __device__ Sel radix_select(const float* __restrict__ z, int V, float m, float t
             if (r > 0 && ((k ^ prefix) >> (shift + 8)) != 0) continue;
             const uint32_t bin = (k >> shift) & (kBins - 1);
             atomicAdd(&sm.cnt[bin], 1u);
-            if (MODE != SEL_COUNT_GE) atomicAdd(&sm.mass[bin], weight_of(zi, m, t));
+            atomicAdd(&sm.mass[bin], weight_of(zi, m, t));   // the mass above the boundary is needed in every mode
         }
         __syncthreads();
         if (warp == 0) {
