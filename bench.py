@@ -365,6 +365,8 @@ def run_ours(args, rank, world, device):
         out["extra"] = extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind)
         del wts
         out["extra"]["llama31_70b"] = extra_70b(ddb, device, hbm, bf16_peak, peak_kind)
+        st = stack_measurements(device)
+        out["extra"]["stack_8b_32_layers"] = {k: st[k] for k in ("workload", "decode", "prefill", "clocks")}
     return out
 
 
@@ -409,6 +411,22 @@ def run_stack(args, rank, world, device):
     + greedy choice; batch 32, a 1024-token prefill, then 256 decode steps that feed
     each chosen id back (one step = one captured graph replay).  `value` is the
     decode throughput; the prefill is reported beside it."""
+    r = stack_measurements(device)
+    steps, B = r["decode_steps"], r["batch"]
+    return {"metric": METRIC, "value": round(r["decode"]["tok_s"] * world, 1), "unit": "tok/s", "n_gpus": world,
+            "steps": steps, "warmup": 3, "ms_per_step": round(r["decode"]["us_per_step"] / 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,0.02) weights drawn on the device, uniform token ids)",
+            "config": {"workload": r["workload"], "layers": r["layers"], "batch": B,
+                       "prefill_tokens": r["prefill_tokens"], "decode_steps": steps,
+                       "l2": "inputs larger than L2: 15.9 GB of weights per decode step"},
+            "decode": r["decode"], "prefill": r["prefill"], "clocks": r["clocks"],
+            "gpu_launches": r["gpu_launches"],
+            "launch": "one CUDA graph per decode step (embedding, 32 blocks, head, position update)"}
+
+
+def stack_measurements(device):
+    """Config 5 measured: build the stack, time its prefill and its greedy decode steps."""
     import dense_decoder_block_gb300 as ddb
     from dense_decoder_block_gb300.stack import LlamaStack
     ddb.lib()
@@ -481,24 +499,21 @@ def run_stack(args, rank, world, device):
                   for k in range(steps)]
     dec_bytes = sum(step_bytes)
     tok_s = B * steps / (dec_ms / 1e3)
-    return {"metric": METRIC, "value": round(tok_s * world, 1), "unit": "tok/s", "n_gpus": world,
-            "steps": steps, "warmup": 3, "ms_per_step": round(dec_ms / steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,0.02) weights drawn on the device, uniform token ids)",
-            "config": {"workload": f"Llama-3 8B-shaped stack: {L} blocks + embedding + LM head (V={V}), batch {B}, "
-                                   f"{T}-token prefill then {steps} greedy decode steps",
-                       "layers": L, "batch": B, "prefill_tokens": T, "decode_steps": steps,
-                       "l2": "inputs larger than L2: 15.9 GB of weights per decode step"},
-            "decode": {"tok_s": round(tok_s, 1), "us_per_step": round(dec_ms / steps * 1e3, 1),
-                       "hbm_frac": round(dec_bytes / (dec_ms / 1e3) / 1e9 / hbm, 4),
-                       "algorithmic_bytes_per_step": round(dec_bytes / steps), "peak_gbs": hbm},
-            "prefill": {"ms": round(pre_ms, 2), "tok_s": round(B * T / (pre_ms / 1e3), 1),
-                        "tflops": round(pre_flops / (pre_ms / 1e3) / 1e12, 1),
-                        "frac_of_bf16_peak": round(pre_flops / (pre_ms / 1e3) / 1e12 / bf16_peak, 4),
-                        "peak_tflops": bf16_peak, "peak_kind": peak_kind + " (sustained)"},
-            "clocks": sampler.summary(),
-            "gpu_launches": steps * (2 + L * n_dec + 3) + (n_pre + 1) * (1 + L * n_pre_launch + 3),
-            "launch": "one CUDA graph per decode step (embedding, 32 blocks, head, position update)"}
+    res = {"workload": f"Llama-3 8B-shaped stack: {L} blocks + embedding + LM head (V={V}), batch {B}, "
+                       f"{T}-token prefill then {steps} greedy decode steps",
+           "layers": L, "batch": B, "prefill_tokens": T, "decode_steps": steps,
+           "decode": {"tok_s": round(tok_s, 1), "us_per_step": round(dec_ms / steps * 1e3, 1),
+                      "hbm_frac": round(dec_bytes / (dec_ms / 1e3) / 1e9 / hbm, 4),
+                      "algorithmic_bytes_per_step": round(dec_bytes / steps), "peak_gbs": hbm},
+           "prefill": {"ms": round(pre_ms, 2), "tok_s": round(B * T / (pre_ms / 1e3), 1),
+                       "tflops": round(pre_flops / (pre_ms / 1e3) / 1e12, 1),
+                       "frac_of_bf16_peak": round(pre_flops / (pre_ms / 1e3) / 1e12 / bf16_peak, 4),
+                       "peak_tflops": bf16_peak, "peak_kind": peak_kind + " (sustained)"},
+           "clocks": sampler.summary(),
+           "gpu_launches": steps * (2 + L * n_dec + 3) + (n_pre + 1) * (1 + L * n_pre_launch + 3)}
+    del graph, st, layers, w_embed, w_out
+    torch.cuda.empty_cache()
+    return res
 
 
 def blk_launches(blk):
@@ -590,9 +605,31 @@ def extra_measurements(ddb, dims, wts, device, hbm, bf16_peak, peak_kind):
         ms = time_region(lambda: blk.prefill(x, kv, y, ws), steps, 2, stream)
         fl = prefill_flops(dims, 1, T)
         tf = fl / (ms / 1e3) / 1e12
+        # per stage, events between the kernels (a second pass; the step's own time is above)
+        stage_ms = stage_profile(blk, lambda st: blk.prefill(x, kv, y, ws, st), device, steps)
+        st_tf = {k: v / (stage_ms[k] / 1e3) / 1e12 for k, v in prefill_stage_flops(dims, 1, T).items()}
         res[f"prefill_t{T}"] = {"tok_s": round(T / (ms / 1e3), 1), "ms": round(ms, 3), "tflops": round(tf, 1),
-                                "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind}
+                                "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_kind": peak_kind,
+                                "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+                                "stage_tflops": {k: round(v, 1) for k, v in st_tf.items()},
+                                "stage_frac_of_bf16_peak": {k: round(v / bf16_peak, 4) for k, v in st_tf.items()}}
+    res["sample_b32"] = extra_sample(ddb, device, stream)
     return res
+
+
+def extra_sample(ddb, device, stream):
+    """The sampling head (llama_sample) on batch-32 rows of 128,256 fp32 logits:
+    temperature 1 then top-p 0.9 (Meta's 8B reference setting), and top-k 50 with it."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(3)
+    z = torch.randn(32, workloads.VOCAB, generator=gen, device=device) * 3
+    u = torch.rand(32, generator=gen, device=device)
+    ids = torch.empty(32, dtype=torch.int32, device=device)
+    out = {}
+    for name, k, p in (("top_p_0.9", 0, 0.9), ("top_k_50_top_p_0.9", 50, 0.9)):
+        ms = time_region(lambda: ddb.llama_sample(z, 32, workloads.VOCAB, 1.0, k, p, u, ids), 20, 3, stream)
+        out[name] = {"us_per_call": round(ms * 1e3, 2), "logits_mb": round(32 * workloads.VOCAB * 4 / 1e6, 2)}
+    return out
 
 
 def extra_seqpos(ddb, dims, wts, device, hbm):

@@ -12,7 +12,7 @@ KV caches and the scratch buffers, all allocated once.
 from __future__ import annotations
 
 import contextlib
-from typing import Dict, List, Optional, Sequence, Tuple
+from typing import Callable, Dict, List, Optional, Sequence, Tuple
 
 import torch
 
@@ -63,28 +63,41 @@ class LlamaStack:
                             self.dims.d_model, self.dims.eps, self.ids, self.logits, self.head_ws,
                             self.head_ws.numel(), stream)
 
-    def prefill(self, ids: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    def prefill(self, ids: torch.Tensor, stream: Optional[torch.cuda.Stream] = None,
+                on_layer: Optional[Callable[[int, torch.Tensor], None]] = None) -> None:
         """ids [B, T] int32 on the device, positions 0..T-1.  Leaves the logits of the
-        last position in self.logits, the greedy ids in self.ids, and self.pos = T."""
+        last position in self.logits, the greedy ids in self.ids, and self.pos = T.
+        ``on_layer(l, h)``, if given, sees the embedding (l = -1) and each block's
+        output h [B, T, d] as soon as its call is enqueued (for inspection)."""
         B, T = ids.shape
         assert B == self.batch and T <= self.prefill_tokens
         x, y = self._acts(T)
         llama_embed(ids, B * T, self.w_embed, self.vocab, self.dims.d_model, x, self.err, stream)
-        for blk, kv in zip(self.blocks, self.caches):
+        if on_layer:
+            on_layer(-1, x)
+        for l, (blk, kv) in enumerate(zip(self.blocks, self.caches)):
             blk.prefill(x, kv, y, self.ws, stream)
+            if on_layer:
+                on_layer(l, y)
             x, y = y, x
         self._head(x, T, stream)
         with self._on(stream):
             self.pos.fill_(T)
 
-    def decode_step(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+    def decode_step(self, stream: Optional[torch.cuda.Stream] = None,
+                    on_layer: Optional[Callable[[int, torch.Tensor], None]] = None) -> None:
         """One token for every sequence at position self.pos (on the device): embeds
         self.ids, runs the blocks, writes the next ids into self.ids and advances
-        self.pos.  Capturable in a CUDA graph (nothing is read on the host)."""
+        self.pos.  Capturable in a CUDA graph (nothing is read on the host) when
+        ``on_layer`` (as in prefill) is not given."""
         x, y = self._acts(1)
         llama_embed(self.ids, self.batch, self.w_embed, self.vocab, self.dims.d_model, x, self.err, stream)
-        for blk, kv in zip(self.blocks, self.caches):
+        if on_layer:
+            on_layer(-1, x)
+        for l, (blk, kv) in enumerate(zip(self.blocks, self.caches)):
             blk.decode_devpos(x, kv, self.pos, y, self.ws, stream)
+            if on_layer:
+                on_layer(l, y)
             x, y = y, x
         self._head(x, 1, stream)
         with self._on(stream):

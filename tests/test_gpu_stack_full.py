@@ -1,16 +1,29 @@
 """The full 32-layer Llama-3 8B-shaped stack against the oracle at its stated size:
 d = 4096, 32 query / 8 KV heads, d_ff = 14336, 32 blocks, vocabulary 128,256,
 batch 32.  A 32-token prefill, then two teacher-forced decode steps (the given
-next tokens are fed in, so both sides see the same inputs).
+next tokens are fed in, so both sides see the same tokens).
 
 Batch rows are independent, so the oracle runs rows 0 and 31 only.  The weights
 are drawn on the device with a seeded generator (as the benchmark draws them)
-and copied to the host for the oracle one layer at a time.  Checked: the fp32
-logits of the last position after the prefill and after each decode step
-(max |err| / rms(ref) <= 2e-2), the greedy ids wherever the oracle's top-2
-margin exceeds twice the measured error, and that all 32 rows' ids are in
-range.  ("How Llama 3.1 Generates the Next Token": the transformer blocks,
-Unembedding, Sampling; "Llama 3.1 70B": Token embedding, LM head.)
+and copied to the host for the oracle one layer at a time.
+
+A deep stack of random blocks magnifies last-bit differences: one bf16 rounding
+flip in one element after the first of 32 such blocks leaves the oracle's own
+final hidden state about 4e-2 (rms) and 0.15 (max) of its rms away from the
+unperturbed run (measured on the oracle alone, fp64).  No two implementations
+that round one value differently can therefore agree within 2e-2 after 32
+layers, and the comparison is made layer by layer instead ("hidden states
+teacher-forced", like the token teacher forcing): each block of the GPU stack
+is checked against the oracle's block applied to that block's GPU input, at
+every position of the prefill and of both decode steps, with the bound every
+block parity test uses (2e-2 of rms beyond two bf16 ulps); the head is checked
+on the GPU's final hidden state (fp32 logits, max |err| / rms <= 2e-2), and the
+greedy ids wherever the oracle's top-2 margin exceeds twice the error.  The
+free-running difference (the oracle run on its own from the embedding) is
+printed beside them.
+
+("How Llama 3.1 Generates the Next Token": the transformer blocks, Unembedding,
+Sampling; "Llama 3.1 70B": Token embedding, Transformer layer, LM head.)
 """
 import numpy as np
 import pytest
@@ -18,13 +31,14 @@ import torch
 
 import workloads
 from oracle import block as ob
+from tests.blockrun import check_bf16_output
 from tests.parity_log import record_parity
 
 pytestmark = pytest.mark.gpu
 
 LOGIT_TOL = 2e-2
 T, STEPS = 32, 2
-ROWS = (0, 31)
+ROWS = [0, 31]
 
 
 def _draw(shape, seed, std, device):
@@ -33,7 +47,7 @@ def _draw(shape, seed, std, device):
     return torch.randn(shape, generator=gen, device=device).mul_(std).to(torch.bfloat16)
 
 
-def test_full_stack_prefill_and_decode_rows_match_oracle():
+def test_full_stack_layers_and_head_match_oracle():
     import dense_decoder_block_gb300 as ddb
     from dense_decoder_block_gb300.stack import LlamaStack
     ddb.lib()
@@ -53,49 +67,68 @@ def test_full_stack_prefill_and_decode_rows_match_oracle():
     ids = workloads.make_token_ids(B, T + STEPS, V, seed=9)
     ids_dev = ids.to(dev)
 
+    # every block's input and output rows (sequences 0 and 31) at every position
+    hidden = [[] for _ in range(L + 1)]          # hidden[l + 1]: output of block l; hidden[0]: embedding
+
+    def keep(l, h):
+        hidden[l + 1].append(h[ROWS].double().cpu().numpy())
+
     logits_gpu, ids_gpu = [], []
-    st.prefill(ids_dev[:, :T].contiguous())
+    st.prefill(ids_dev[:, :T].contiguous(), on_layer=keep)
     torch.cuda.synchronize()
     assert st.poll_error() == 0 and int(st.err.item()) == 0
     logits_gpu.append(st.logits.double().cpu().numpy())
     ids_gpu.append(st.ids.cpu().numpy())
     for s in range(STEPS):
         st.ids.copy_(ids_dev[:, T + s])          # teacher forcing
-        st.decode_step()
+        st.decode_step(on_layer=keep)
         torch.cuda.synchronize()
         assert st.poll_error() == 0
         logits_gpu.append(st.logits.double().cpu().numpy())
         ids_gpu.append(st.ids.cpu().numpy())
     for got in ids_gpu:
         assert got.min() >= 0 and got.max() < V
-
-    # the oracle on rows 0 and 31: every position 0 .. T + STEPS - 1 in one causal pass
-    rows = list(ROWS)
+    hidden = [np.concatenate(h, axis=1) for h in hidden]   # [2, T + STEPS, d]
     n = T + STEPS
+
     to64 = workloads.to_numpy64
-    h = ob.embed(ids[rows].numpy(), to64(w_embed))
-    for w, g in layers:
+    assert np.array_equal(hidden[0], ob.embed(ids[ROWS].numpy(), to64(w_embed)))
+    free = hidden[0]
+    worst = 0.0
+    for l, (w, g) in enumerate(layers):
         w64 = {k: to64(v) for k, v in w.items()}
         g64 = {k: to64(v) for k, v in g.items()}
-        kc = np.zeros((len(rows), dims.n_kv_heads, n, dims.head_dim))
+        kc = np.zeros((len(ROWS), dims.n_kv_heads, n, dims.head_dim))
         vc = np.zeros_like(kc)
-        h = ob.block_forward(h, w64, g64, dims, kc, vc, 0)
+        tr = {}
+        ob.block_forward(hidden[l], w64, g64, dims, kc, vc, 0, trace=tr)
+        raw, _ = check_bf16_output(hidden[l + 1], tr["y_exact"], what=f"32-layer stack, block {l}")
+        worst = max(worst, raw)
+        kc[:] = 0
+        vc[:] = 0
+        free = ob.block_forward(free, w64, g64, dims, kc, vc, 0)
         del w64
-    w_out64 = to64(w_out)
+    record_parity(f"[parity] 32-layer stack: every block against the oracle on its GPU input, worst raw "
+                  f"max|err|/rms = {worst:.3e}")
+    w_out64, g_f64 = to64(w_out), to64(g_final)
     for k, pos in enumerate(range(T - 1, n)):
-        ref = ob.lm_head_logits(h[:, pos, :], to64(g_final), w_out64, dims.eps)
-        got = logits_gpu[k][rows]
+        what = "prefill" if k == 0 else f"decode step {k - 1}"
+        ref = ob.lm_head_logits(hidden[L][:, pos, :], g_f64, w_out64, dims.eps)
+        got = logits_gpu[k][ROWS]
         rms = float(np.sqrt(np.mean(ref ** 2)))
         err = np.abs(got - ref)
-        what = "prefill" if k == 0 else f"decode step {k - 1}"
-        record_parity(f"[parity] 32-layer stack {what} logits (rows 0, 31): max|err|/rms = {err.max() / rms:.3e}, "
-                      f"rms err / rms = {np.sqrt(np.mean(err ** 2)) / rms:.3e}")
+        record_parity(f"[parity] 32-layer stack head, {what} logits (rows 0, 31) on the GPU's final hidden "
+                      f"state: max|err|/rms = {err.max() / rms:.3e}")
         assert np.all(np.isfinite(got))
         assert err.max() <= LOGIT_TOL * rms
         bound = float(err.max())
-        for r, b in enumerate(rows):
+        for r, b in enumerate(ROWS):
             top = np.argsort(ref[r])[::-1][:2]
             if ref[r][top[0]] - ref[r][top[1]] > 2 * bound:
                 assert int(ids_gpu[k][b]) == int(top[0]), f"{what}: row {b}"
             else:
                 assert ref[r][int(ids_gpu[k][b])] >= ref[r][top[0]] - 2 * bound
+        free_ref = ob.lm_head_logits(free[:, pos, :], g_f64, w_out64, dims.eps)
+        fe = np.abs(got - free_ref)
+        record_parity(f"[parity] 32-layer stack, {what} logits against the free-running oracle: "
+                      f"max|err|/rms = {fe.max() / rms:.3e}, rms err / rms = {np.sqrt(np.mean(fe ** 2)) / rms:.3e}")
