@@ -10,36 +10,46 @@
 // cumulative mass up to a token -- is an exact integer sum whatever order the
 // threads add in: the kept set and the drawn token do not depend on scheduling.
 //
-// The kept set and the draw are found without sorting.  "The first n tokens in
-// order whose mass reaches a target" is found by a radix descent over the
-// logits' order-preserving 32-bit keys: four rounds, each a 256-bin histogram
-// (token count and mass per bin) of the tokens that share the key bits fixed so
-// far, scanned from the highest bin down to the bin where the running count or
-// mass reaches the target.  After the last round the boundary key is exact; the
-// tokens equal to it (a tie group) share one weight, so how many of them the
-// target needs is a division, and the drawn one is found by its rank among them
-// in index order.
+// The kept set and the draw are found without sorting.  "The first token (in
+// order) at which the running count or mass reaches a target" is found in two
+// levels.  Level 0, shared by every search of a row: a 256-bin histogram (token
+// count and mass per bin) over bins of one eighth of (max - z) / T each, i.e.
+// intervals of logits in decreasing order, kept per warp and then summed (the
+// bins follow the distribution, so few threads add to the same bin at once).
+// Scanning it from the top gives the bin that holds the boundary.  Then an exact
+// radix descent over the logits' order-preserving 32-bit keys, restricted to that
+// bin: four rounds, each a 256-bin histogram of the bin's tokens that share the
+// key bits fixed so far, scanned from the highest key down.  The boundary key is
+// then exact; the tokens equal to it (a tie group) share one weight, so how many
+// of them the target needs is a division, and the drawn one is found by its rank
+// among them in index order.
 #include "internal.h"
 
 namespace llama {
 namespace {
 
 constexpr int kSampThreads = 1024;
+constexpr int kWarps = kSampThreads / 32;
 constexpr int kBins = 256;
+constexpr float kBinsPerNat = 8.0f;              // level-0 bins per unit of (max - z) / T
 constexpr float kMassScale = 1099511627776.0f;   // 2^40: fixed-point weight of the largest logit
 
 struct SampSmem {
-    unsigned int cnt[kBins];
+    unsigned int pc[kWarps][kBins];              // level 0, per warp
+    unsigned long long pm[kWarps][kBins];
+    unsigned int cnt0[kBins];                    // level 0, summed
+    unsigned long long mass0[kBins];
+    unsigned int cnt[kBins];                     // key rounds
     unsigned long long mass[kBins];
-    float red_v[32];
-    int red_i[32];
-    unsigned long long red_m[32];
-    unsigned int scan[32];
-    // descent state, written by warp 0
-    unsigned int prefix, above_c, tie_c;
+    float red_v[kWarps];
+    int red_i[kWarps];
+    unsigned int scan[kWarps];
+    // search state, written by warp 0
+    unsigned int prefix, above_c, tie_c, chosen;
     unsigned long long above_m;
     int found;
 };
+constexpr size_t kSampSmem = sizeof(SampSmem);
 
 // Order-preserving key: larger logit -> larger key (-0 counted as +0).
 __device__ __forceinline__ uint32_t order_key(float z) {
@@ -54,6 +64,12 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
 __device__ __forceinline__ unsigned long long weight_of(float z, float m, float t) {
     const float e = expf(__fdiv_rn(__fsub_rn(z, m), t));
     return __float2ull_rn(__fmul_rn(e, kMassScale));
+}
+
+// Level-0 bin of a logit: floor(8 (m - z) / T), at most 255 (monotone in z: a bin
+// is an interval of logits, bin 0 the highest).
+__device__ __forceinline__ int level0_bin(float z, float m, float t) {
+    return (int)fminf(__fmul_rn(__fdiv_rn(__fsub_rn(m, z), t), kBinsPerNat), (float)(kBins - 1));
 }
 
 // ceil or floor of a * b / 2^24 for a <= 2^24, b < 2^57 (the product needs 81 bits).
@@ -72,13 +88,93 @@ struct Sel {
     uint32_t tie_c;              // tokens with exactly this key
 };
 
-// Radix descent: the key of the first token (in order) at which the running count
-// reaches `target` (SEL_COUNT_GE), or the running mass reaches it (SEL_MASS_GE) or
-// exceeds it (SEL_MASS_GT).  The target must be reachable.
+// Warp 0: scan 256 bins in order (bin o for level 0, where bin 0 is the highest;
+// bin 255 - o for key rounds, where the highest key is bin 255) from running
+// totals (above_c0, above_m0) to the first non-empty bin at which the running
+// count reaches `target` (SEL_COUNT_GE) or the running mass reaches it
+// (SEL_MASS_GE) or exceeds it (SEL_MASS_GT).  Writes sm.chosen, sm.above_c,
+// sm.above_m (totals before that bin) and sm.tie_c (its count).  The target must
+// be reachable; otherwise the last non-empty bin is taken.
+template <int MODE, bool ASCENDING>
+__device__ void scan_bins(const unsigned int* cnt, const unsigned long long* mass, uint32_t above_c0,
+                          unsigned long long above_m0, unsigned long long target, SampSmem& sm) {
+    const int lane = threadIdx.x & 31;
+    auto bin_at = [](int o) { return ASCENDING ? o : kBins - 1 - o; };
+    uint32_t c_l = 0;
+    unsigned long long m_l = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int b = bin_at(lane * 8 + j);
+        c_l += cnt[b];
+        m_l += mass[b];
+    }
+    uint32_t c_inc = c_l;
+    unsigned long long m_inc = m_l;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t c_o = __shfl_up_sync(0xffffffffu, c_inc, off);
+        const unsigned long long m_o = __shfl_up_sync(0xffffffffu, m_inc, off);
+        if (lane >= off) {
+            c_inc += c_o;
+            m_inc += m_o;
+        }
+    }
+    const uint32_t c_run = above_c0 + c_inc;
+    const unsigned long long m_run = above_m0 + m_inc;
+    const bool hit = MODE == SEL_COUNT_GE ? c_run >= target : MODE == SEL_MASS_GE ? m_run >= target : m_run > target;
+    const unsigned ballot = __ballot_sync(0xffffffffu, hit && c_l > 0);
+    // the last lane that holds a non-empty bin, for an unreachable target
+    const unsigned nonempty = __ballot_sync(0xffffffffu, c_l > 0);
+    const int first = ballot ? __ffs(ballot) - 1 : (nonempty ? 31 - __clz(nonempty) : 0);
+    if (lane == first) {
+        uint32_t c_acc = above_c0 + c_inc - c_l;
+        unsigned long long m_acc = above_m0 + m_inc - m_l;
+        int chosen = -1, last = -1;
+        uint32_t tie = 0, last_c = 0;
+        unsigned long long last_m = 0;
+        for (int j = 0; j < 8; ++j) {
+            const int b = bin_at(lane * 8 + j);
+            const uint32_t c = cnt[b];
+            const unsigned long long ms = mass[b];
+            if (c == 0) continue;
+            const bool h = MODE == SEL_COUNT_GE ? c_acc + c >= target
+                           : MODE == SEL_MASS_GE ? m_acc + ms >= target
+                                                 : m_acc + ms > target;
+            if (h) {
+                chosen = b;
+                tie = c;
+                break;
+            }
+            last = b;
+            last_c = c;
+            last_m = ms;
+            c_acc += c;
+            m_acc += ms;
+        }
+        if (chosen < 0) {   // unreachable target: stop at the last non-empty bin
+            chosen = last < 0 ? bin_at(lane * 8) : last;
+            tie = last_c;
+            c_acc -= last_c;
+            m_acc -= last_m;
+        }
+        sm.chosen = (unsigned int)chosen;
+        sm.above_c = c_acc;
+        sm.above_m = m_acc;
+        sm.tie_c = tie;
+    }
+}
+
+// The first token in order at which the running count reaches `target`
+// (SEL_COUNT_GE) or the running mass reaches it (SEL_MASS_GE) or exceeds it
+// (SEL_MASS_GT): the level-0 bin from the row's level-0 histogram, then the exact
+// key by a radix descent over that bin's tokens.
 template <int MODE>
-__device__ Sel radix_select(const float* __restrict__ z, int V, float m, float t, unsigned long long target,
-                            SampSmem& sm) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ Sel select_boundary(const float* __restrict__ z, int V, float m, float t, unsigned long long target,
+                               SampSmem& sm) {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (warp == 0) scan_bins<MODE, true>(sm.cnt0, sm.mass0, 0u, 0ull, target, sm);
+    __syncthreads();
+    const int b0 = (int)sm.chosen;
     uint32_t prefix = 0;
     for (int r = 0; r < 4; ++r) {
         const int shift = 24 - 8 * r;
@@ -86,87 +182,22 @@ __device__ Sel radix_select(const float* __restrict__ z, int V, float m, float t
             sm.cnt[i] = 0;
             sm.mass[i] = 0;
         }
+        const uint32_t above_c0 = sm.above_c;
+        const unsigned long long above_m0 = sm.above_m;
         __syncthreads();
         for (int i = tid; i < V; i += blockDim.x) {
             const float zi = z[i];
+            if (level0_bin(zi, m, t) != b0) continue;
             const uint32_t k = order_key(zi);
             if (r > 0 && ((k ^ prefix) >> (shift + 8)) != 0) continue;
             const uint32_t bin = (k >> shift) & (kBins - 1);
             atomicAdd(&sm.cnt[bin], 1u);
-            atomicAdd(&sm.mass[bin], weight_of(zi, m, t));   // the mass above the boundary is needed in every mode
+            atomicAdd(&sm.mass[bin], weight_of(zi, m, t));
         }
         __syncthreads();
-        if (warp == 0) {
-            // lane l owns bins 255 - 8l down to 248 - 8l (highest keys first)
-            const unsigned long long above_m0 = r == 0 ? 0ull : sm.above_m;
-            const uint32_t above_c0 = r == 0 ? 0u : sm.above_c;
-            uint32_t c_l = 0;
-            unsigned long long m_l = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int b = kBins - 1 - (lane * 8 + j);
-                c_l += sm.cnt[b];
-                m_l += sm.mass[b];
-            }
-            // inclusive scan over lanes (lane 0 = highest bins)
-            uint32_t c_inc = c_l;
-            unsigned long long m_inc = m_l;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const uint32_t c_o = __shfl_up_sync(0xffffffffu, c_inc, off);
-                const unsigned long long m_o = __shfl_up_sync(0xffffffffu, m_inc, off);
-                if (lane >= off) {
-                    c_inc += c_o;
-                    m_inc += m_o;
-                }
-            }
-            const uint32_t c_run = above_c0 + c_inc;
-            const unsigned long long m_run = above_m0 + m_inc;
-            const bool hit = MODE == SEL_COUNT_GE ? c_run >= target
-                             : MODE == SEL_MASS_GE ? m_run >= target
-                                                   : m_run > target;
-            const unsigned ballot = __ballot_sync(0xffffffffu, hit);
-            // the target is reachable, so some lane hits; guard anyway (last lane)
-            const int first = ballot ? __ffs(ballot) - 1 : 31;
-            if (lane == first) {
-                uint32_t c_acc = above_c0 + c_inc - c_l;
-                unsigned long long m_acc = above_m0 + m_inc - m_l;
-                int chosen = -1;
-                uint32_t tie = 0;
-                int last_nonempty = -1;
-                for (int j = 0; j < 8; ++j) {
-                    const int b = kBins - 1 - (lane * 8 + j);
-                    const uint32_t c = sm.cnt[b];
-                    const unsigned long long ms = sm.mass[b];
-                    if (c == 0) continue;
-                    last_nonempty = b;
-                    const bool h = MODE == SEL_COUNT_GE ? c_acc + c >= target
-                                   : MODE == SEL_MASS_GE ? m_acc + ms >= target
-                                                         : m_acc + ms > target;
-                    if (h) {
-                        chosen = b;
-                        tie = c;
-                        break;
-                    }
-                    c_acc += c;
-                    m_acc += ms;
-                }
-                if (chosen < 0) {   // unreachable target: stop at the lowest non-empty bin seen
-                    chosen = last_nonempty < 0 ? 0 : last_nonempty;
-                    tie = last_nonempty < 0 ? 0 : sm.cnt[chosen];
-                    if (last_nonempty >= 0) {
-                        c_acc -= tie;
-                        m_acc -= sm.mass[chosen];
-                    }
-                }
-                sm.prefix = prefix | ((uint32_t)chosen << shift);
-                sm.above_c = c_acc;
-                sm.above_m = m_acc;
-                sm.tie_c = tie;
-            }
-        }
+        if (warp == 0) scan_bins<MODE, false>(sm.cnt, sm.mass, above_c0, above_m0, target, sm);
         __syncthreads();
-        prefix = sm.prefix;
+        prefix |= sm.chosen << shift;
     }
     Sel s;
     s.key = prefix;
@@ -181,7 +212,8 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
                                                          int top_k, unsigned int p_q24,
                                                          const float* __restrict__ uniforms,
                                                          int32_t* __restrict__ ids) {
-    __shared__ SampSmem sm;
+    extern __shared__ __align__(16) uint8_t samp_smem_raw[];
+    SampSmem& sm = *reinterpret_cast<SampSmem*>(samp_smem_raw);
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_warps = blockDim.x >> 5;
     const float* z = logits + (size_t)row * V;
@@ -217,22 +249,41 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     }
     __syncthreads();
 
-    // 2. the normaliser: total fixed-point mass
-    unsigned long long zsum = 0;
-    for (int i = tid; i < V; i += blockDim.x) zsum += weight_of(z[i], m, t);
+    // 2. the level-0 histogram (per warp, then summed) and the normaliser Z
+    for (int i = tid; i < kWarps * kBins; i += blockDim.x) {
+        (&sm.pc[0][0])[i] = 0;
+        (&sm.pm[0][0])[i] = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < V; i += blockDim.x) {
+        const float zi = z[i];
+        const int b = level0_bin(zi, m, t);
+        atomicAdd(&sm.pc[warp][b], 1u);
+        atomicAdd(&sm.pm[warp][b], weight_of(zi, m, t));
+    }
+    __syncthreads();
+    for (int b = tid; b < kBins; b += blockDim.x) {
+        unsigned int c = 0;
+        unsigned long long ms = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            c += sm.pc[w][b];
+            ms += sm.pm[w][b];
+        }
+        sm.cnt0[b] = c;
+        sm.mass0[b] = ms;
+    }
+    __syncthreads();
+    unsigned long long Z = 0;   // every warp sums the 256 bins (8 per lane)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
-    if (lane == 0) sm.red_m[warp] = zsum;
-    __syncthreads();
-    unsigned long long Z = 0;
-    for (int w = 0; w < n_warps; ++w) Z += sm.red_m[w];
-    __syncthreads();
+    for (int j = 0; j < 8; ++j) Z += sm.mass0[lane * 8 + j];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, off);
 
     // 3. top-k: the mass of the k first tokens
     uint32_t n_k = (uint32_t)V;
     unsigned long long S_k = Z;
     if (top_k > 0 && top_k < V) {
-        const Sel s = radix_select<SEL_COUNT_GE>(z, V, m, t, (unsigned long long)top_k, sm);
+        const Sel s = select_boundary<SEL_COUNT_GE>(z, V, m, t, (unsigned long long)top_k, sm);
         const unsigned long long w = weight_of(key_logit(s.key), m, t);
         n_k = (uint32_t)top_k;
         S_k = s.above_m + (unsigned long long)(top_k - s.above_c) * w;
@@ -243,7 +294,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     if (p_q24 < (1u << 24)) {
         unsigned long long target = mul_shift24(p_q24, Z, true);
         if (target == 0) target = 1;
-        const Sel s = radix_select<SEL_MASS_GE>(z, V, m, t, target, sm);
+        const Sel s = select_boundary<SEL_MASS_GE>(z, V, m, t, target, sm);
         const unsigned long long w = weight_of(key_logit(s.key), m, t);
         unsigned long long j = w ? (target - s.above_m + w - 1) / w : 1;
         if (j < 1) j = 1;
@@ -259,7 +310,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     unsigned long long u_q24 = (unsigned long long)(u * 16777216.0f);
     if (u_q24 > (1ull << 24) - 1) u_q24 = (1ull << 24) - 1;
     const unsigned long long target = mul_shift24(u_q24, S, false);
-    const Sel s = radix_select<SEL_MASS_GT>(z, V, m, t, target, sm);
+    const Sel s = select_boundary<SEL_MASS_GT>(z, V, m, t, target, sm);
     const unsigned long long w = weight_of(key_logit(s.key), m, t);
     unsigned long long j = w ? (target - s.above_m) / w + 1 : 1;
     if (j > s.tie_c) j = s.tie_c;
@@ -302,8 +353,12 @@ cudaError_t launch_sample(const float* logits, int batch, int vocab, float tempe
     if (batch <= 0) return cudaSuccess;
     const double pq = (double)top_p * 16777216.0;
     const unsigned int p_q24 = top_p >= 1.0f ? (1u << 24) : (unsigned int)(pq + 0.5);
-    return launch_pdl(k_sample, dim3(batch), dim3(kSampThreads), 0, s, logits, vocab, temperature, top_k, p_q24,
-                      uniforms, ids);
+    cudaError_t e = kernel_setup_once((const void*)k_sample, [](const void* k) {
+        return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSampSmem);
+    });
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_sample, dim3(batch), dim3(kSampThreads), kSampSmem, s, logits, vocab, temperature, top_k,
+                      p_q24, uniforms, ids);
 }
 
 }  // namespace llama

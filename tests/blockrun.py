@@ -26,7 +26,8 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(a)) - 7)
 
 
-def check_bf16_output(got: np.ndarray, exact: np.ndarray, tol: float = BF16_TOL, what: str = "y"):
+def check_bf16_output(got: np.ndarray, exact: np.ndarray, tol: float = BF16_TOL, what: str = "y",
+                      assert_: bool = True):
     """Parity of a bf16 output with the oracle.
 
     ref = the oracle's output (its value rounded to bf16 at the same point);
@@ -40,7 +41,8 @@ def check_bf16_output(got: np.ndarray, exact: np.ndarray, tol: float = BF16_TOL,
     carry such a flip, hence ULPS = 2.  Also asserted: the rms error stays
     below tol / 4 of rms (no systematic drift).  Printed: the raw
     max|err|/rms and the share of elements that differ.
-    Returns (raw metric, fraction differing)."""
+    Returns (raw metric, fraction differing, error beyond the ulps, rms error),
+    all relative to rms(ref); ``assert_=False`` only measures."""
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     ref = round_bf16(exact)
     rms = float(np.sqrt(np.mean(ref ** 2)))
@@ -51,9 +53,10 @@ def check_bf16_output(got: np.ndarray, exact: np.ndarray, tol: float = BF16_TOL,
     frac = float(np.count_nonzero(diff)) / diff.size
     record_parity(f"[parity] {what}: max|err|/rms = {raw:.3e}, beyond {ULPS} ulps = {beyond:.3e}, "
                   f"rms err = {rms_err:.2e}, differing {100 * frac:.2f}%")
-    assert beyond <= tol, f"{what}: error beyond {ULPS} bf16 ulps = {beyond:.4e} x rms > {tol}"
-    assert rms_err <= tol / 4, f"{what}: rms error {rms_err:.3e} > {tol / 4}"
-    return raw, frac
+    if assert_:
+        assert beyond <= tol, f"{what}: error beyond {ULPS} bf16 ulps = {beyond:.4e} x rms > {tol}"
+        assert rms_err <= tol / 4, f"{what}: rms error {rms_err:.3e} > {tol / 4}"
+    return raw, frac, beyond, rms_err
 
 
 def rnd_for(dtype):
