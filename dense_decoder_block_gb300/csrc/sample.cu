@@ -10,19 +10,19 @@
 // cumulative mass up to a token -- is an exact integer sum whatever order the
 // threads add in: the kept set and the drawn token do not depend on scheduling.
 //
-// The kept set and the draw are found without sorting.  "The first token (in
-// order) at which the running count or mass reaches a target" is found in two
-// levels.  Level 0, shared by every search of a row: a 256-bin histogram (token
-// count and mass per bin) over bins of one eighth of (max - z) / T each, i.e.
-// intervals of logits in decreasing order, kept per warp and then summed (the
-// bins follow the distribution, so few threads add to the same bin at once).
-// Scanning it from the top gives the bin that holds the boundary.  Then an exact
-// radix descent over the logits' order-preserving 32-bit keys, restricted to that
-// bin: four rounds, each a 256-bin histogram of the bin's tokens that share the
-// key bits fixed so far, scanned from the highest key down.  The boundary key is
-// then exact; the tokens equal to it (a tie group) share one weight, so how many
-// of them the target needs is a division, and the drawn one is found by its rank
-// among them in index order.
+// "The first token (in order) at which the running count or mass reaches a
+// target" (the top-k boundary, the top-p boundary, the drawn token) is found in
+// two levels.  Level 0, computed once per row: a 256-bin histogram (token count
+// and mass) over bins of one sixteenth of (max - z) / T, i.e. intervals of logits
+// in decreasing order, the last bin holding everything more than 16 units below
+// the maximum; it is kept per warp (the tail bin in registers) and then summed.
+// A scan from the top gives the bin that holds the boundary and the count and
+// mass above it.  Level 1: that bin's tokens are gathered into shared memory,
+// sorted by (logit down, index up) with a bitonic sort, and scanned in order --
+// the boundary token, its rank and the mass through it are then exact.  A bin
+// too large for shared memory (many equal or nearly equal logits) is resolved by
+// an exact radix descent over the logits' order-preserving keys within the bin
+// instead, and ties by rank in index order.
 #include "internal.h"
 
 namespace llama {
@@ -31,22 +31,30 @@ namespace {
 constexpr int kSampThreads = 1024;
 constexpr int kWarps = kSampThreads / 32;
 constexpr int kBins = 256;
-constexpr float kBinsPerNat = 8.0f;              // level-0 bins per unit of (max - z) / T
+constexpr int kTailBin = kBins - 1;
+constexpr float kBinsPerNat = 16.0f;             // level-0 bins per unit of (max - z) / T
 constexpr float kMassScale = 1099511627776.0f;   // 2^40: fixed-point weight of the largest logit
+constexpr int kListCap = 16384;                  // tokens of one level-0 bin sorted in shared memory
 
 struct SampSmem {
-    unsigned int pc[kWarps][kBins];              // level 0, per warp
-    unsigned long long pm[kWarps][kBins];
+    union {
+        struct {
+            unsigned int pc[kWarps][kBins];      // histograms kept per warp
+            unsigned long long pm[kWarps][kBins];
+        } h;
+        unsigned long long list[kListCap];       // one bin's tokens: key << 32 | (~index)
+    } u;
     unsigned int cnt0[kBins];                    // level 0, summed
     unsigned long long mass0[kBins];
-    unsigned int cnt[kBins];                     // key rounds
+    unsigned int cnt[kBins];                     // key rounds of the large-bin path
     unsigned long long mass[kBins];
     float red_v[kWarps];
     int red_i[kWarps];
-    unsigned int scan[kWarps];
-    // search state, written by warp 0
-    unsigned int prefix, above_c, tie_c, chosen;
-    unsigned long long above_m;
+    unsigned int scan_c[kWarps];
+    unsigned long long scan_m[kWarps];
+    // search state, written by one thread or warp 0
+    unsigned int prefix, above_c, tie_c, chosen, n_list, rank;
+    unsigned long long above_m, mass_through;
     int found;
 };
 constexpr size_t kSampSmem = sizeof(SampSmem);
@@ -66,7 +74,7 @@ __device__ __forceinline__ unsigned long long weight_of(float z, float m, float 
     return __float2ull_rn(__fmul_rn(e, kMassScale));
 }
 
-// Level-0 bin of a logit: floor(8 (m - z) / T), at most 255 (monotone in z: a bin
+// Level-0 bin of a logit: floor(16 (m - z) / T), at most 255 (monotone in z: a bin
 // is an interval of logits, bin 0 the highest).
 __device__ __forceinline__ int level0_bin(float z, float m, float t) {
     return (int)fminf(__fmul_rn(__fdiv_rn(__fsub_rn(m, z), t), kBinsPerNat), (float)(kBins - 1));
@@ -80,13 +88,6 @@ __device__ __forceinline__ unsigned long long mul_shift24(unsigned long long a, 
 }
 
 enum SelMode { SEL_COUNT_GE = 0, SEL_MASS_GE = 1, SEL_MASS_GT = 2 };
-
-struct Sel {
-    uint32_t key;                // the boundary key
-    uint32_t above_c;            // tokens with a larger key
-    unsigned long long above_m;  // their mass
-    uint32_t tie_c;              // tokens with exactly this key
-};
 
 // Warp 0: scan 256 bins in order (bin o for level 0, where bin 0 is the highest;
 // bin 255 - o for key rounds, where the highest key is bin 255) from running
@@ -164,24 +165,130 @@ __device__ void scan_bins(const unsigned int* cnt, const unsigned long long* mas
     }
 }
 
-// The first token in order at which the running count reaches `target`
-// (SEL_COUNT_GE) or the running mass reaches it (SEL_MASS_GE) or exceeds it
-// (SEL_MASS_GT): the level-0 bin from the row's level-0 histogram, then the exact
-// key by a radix descent over that bin's tokens.
+// Per-warp histograms of the threads' (bin, weight) pairs summed into cnt / mass.
+__device__ __forceinline__ void sum_warp_histograms(SampSmem& sm, unsigned int* cnt, unsigned long long* mass) {
+    for (int b = threadIdx.x; b < kBins; b += blockDim.x) {
+        unsigned int c = 0;
+        unsigned long long ms = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            c += sm.u.h.pc[w][b];
+            ms += sm.u.h.pm[w][b];
+        }
+        cnt[b] = c;
+        mass[b] = ms;
+    }
+}
+
+__device__ __forceinline__ void zero_warp_histograms(SampSmem& sm) {
+    for (int i = threadIdx.x; i < kWarps * kBins; i += blockDim.x) {
+        (&sm.u.h.pc[0][0])[i] = 0;
+        (&sm.u.h.pm[0][0])[i] = 0;
+    }
+}
+
 template <int MODE>
-__device__ Sel select_boundary(const float* __restrict__ z, int V, float m, float t, unsigned long long target,
-                               SampSmem& sm) {
-    const int tid = threadIdx.x, warp = tid >> 5;
+__device__ __forceinline__ bool reached(uint32_t count, unsigned long long mass, unsigned long long target) {
+    return MODE == SEL_COUNT_GE ? count >= target : MODE == SEL_MASS_GE ? mass >= target : mass > target;
+}
+
+// The boundary token: the first token in order at which the running count
+// reaches `target` (SEL_COUNT_GE), or the running mass reaches it (SEL_MASS_GE) or
+// exceeds it (SEL_MASS_GT).  Leaves in sm its 0-based rank (sm.rank), the mass of
+// the tokens up to and including it (sm.mass_through) and its index (sm.found).
+template <int MODE>
+__device__ void find_boundary(const float* __restrict__ z, int V, float m, float t, unsigned long long target,
+                              SampSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (warp == 0) scan_bins<MODE, true>(sm.cnt0, sm.mass0, 0u, 0ull, target, sm);
+    if (tid == 0) sm.n_list = 0;
     __syncthreads();
     const int b0 = (int)sm.chosen;
+    const uint32_t above_c = sm.above_c;
+    const unsigned long long above_m = sm.above_m;
+    const uint32_t n_bin = sm.cnt0[b0];
+    if (n_bin <= (uint32_t)kListCap) {
+        // ---- level 1: gather the bin's tokens, sort them, scan in order
+        for (int i0 = 0; i0 < V; i0 += blockDim.x) {
+            const int i = i0 + tid;
+            const float zi = i < V ? z[i] : 0.f;
+            const bool in = i < V && level0_bin(zi, m, t) == b0;
+            const unsigned ballot = __ballot_sync(0xffffffffu, in);
+            if (ballot) {
+                unsigned int base = 0;
+                if (lane == __ffs(ballot) - 1) base = atomicAdd(&sm.n_list, (unsigned int)__popc(ballot));
+                base = __shfl_sync(0xffffffffu, base, __ffs(ballot) - 1);
+                if (in) {
+                    const unsigned int at = base + __popc(ballot & ((1u << lane) - 1u));
+                    sm.u.list[at] = ((unsigned long long)order_key(zi) << 32) | (unsigned long long)(~(uint32_t)i);
+                }
+            }
+        }
+        __syncthreads();
+        const int n = (int)sm.n_list;
+        int n2 = 1;
+        while (n2 < n) n2 <<= 1;
+        for (int i = n + tid; i < n2; i += blockDim.x) sm.u.list[i] = 0ull;   // sorts after every token
+        __syncthreads();
+        for (int k = 2; k <= n2; k <<= 1)
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = tid; i < n2; i += blockDim.x) {
+                    const int ixj = i ^ j;
+                    if (ixj > i) {
+                        const unsigned long long a = sm.u.list[i], b = sm.u.list[ixj];
+                        const bool down = (i & k) == 0;   // descending overall
+                        if (down ? (a < b) : (a > b)) {
+                            sm.u.list[i] = b;
+                            sm.u.list[ixj] = a;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        // running mass in order: contiguous segments per thread, block scan of the segment sums
+        const int seg = (n + blockDim.x - 1) / blockDim.x;
+        const int lo = min(n, tid * seg), hi = min(n, lo + seg);
+        unsigned long long ms = 0;
+        for (int i = lo; i < hi; ++i) ms += weight_of(key_logit((uint32_t)(sm.u.list[i] >> 32)), m, t);
+        unsigned long long inc = ms;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += o;
+        }
+        if (lane == 31) sm.scan_m[warp] = inc;
+        if (tid == 0) {   // an unreachable target ends at the bin's last token
+            sm.rank = above_c + (uint32_t)max(n - 1, 0);
+            sm.found = n > 0 ? (int)~(uint32_t)(sm.u.list[n - 1] & 0xffffffffull) : 0;
+        }
+        __syncthreads();
+        unsigned long long run = above_m + inc - ms;
+        for (int w = 0; w < warp; ++w) run += sm.scan_m[w];
+        if (tid == 0) {
+            unsigned long long total = above_m;
+            for (int w = 0; w < kWarps; ++w) total += sm.scan_m[w];
+            sm.mass_through = total;
+        }
+        __syncthreads();
+        for (int i = lo; i < hi; ++i) {
+            const unsigned long long e = sm.u.list[i];
+            const unsigned long long w = weight_of(key_logit((uint32_t)(e >> 32)), m, t);
+            const bool before = reached<MODE>(above_c + (uint32_t)i, run, target);
+            run += w;
+            if (!before && reached<MODE>(above_c + (uint32_t)i + 1, run, target)) {
+                sm.rank = above_c + (uint32_t)i;
+                sm.mass_through = run;
+                sm.found = (int)~(uint32_t)(e & 0xffffffffull);
+                break;
+            }
+        }
+        __syncthreads();
+        return;
+    }
+    // ---- a bin too large to sort: radix descent over the keys of the bin's tokens
     uint32_t prefix = 0;
     for (int r = 0; r < 4; ++r) {
         const int shift = 24 - 8 * r;
-        for (int i = tid; i < kBins; i += blockDim.x) {
-            sm.cnt[i] = 0;
-            sm.mass[i] = 0;
-        }
+        zero_warp_histograms(sm);
         const uint32_t above_c0 = sm.above_c;
         const unsigned long long above_m0 = sm.above_m;
         __syncthreads();
@@ -191,21 +298,55 @@ __device__ Sel select_boundary(const float* __restrict__ z, int V, float m, floa
             const uint32_t k = order_key(zi);
             if (r > 0 && ((k ^ prefix) >> (shift + 8)) != 0) continue;
             const uint32_t bin = (k >> shift) & (kBins - 1);
-            atomicAdd(&sm.cnt[bin], 1u);
-            atomicAdd(&sm.mass[bin], weight_of(zi, m, t));
+            atomicAdd(&sm.u.h.pc[warp][bin], 1u);
+            atomicAdd(&sm.u.h.pm[warp][bin], weight_of(zi, m, t));
         }
+        __syncthreads();
+        sum_warp_histograms(sm, sm.cnt, sm.mass);
         __syncthreads();
         if (warp == 0) scan_bins<MODE, false>(sm.cnt, sm.mass, above_c0, above_m0, target, sm);
         __syncthreads();
         prefix |= sm.chosen << shift;
     }
-    Sel s;
-    s.key = prefix;
-    s.above_c = sm.above_c;
-    s.above_m = sm.above_m;
-    s.tie_c = sm.tie_c;
-    __syncthreads();   // sm is reused by the caller's next step
-    return s;
+    const unsigned long long wk = weight_of(key_logit(prefix), m, t);
+    const uint32_t ac = sm.above_c, tie = sm.tie_c;
+    const unsigned long long am = sm.above_m;
+    unsigned long long j;   // how many tokens of the tie group the target needs (1-based)
+    if (MODE == SEL_COUNT_GE) j = target - ac;
+    else if (MODE == SEL_MASS_GE) j = wk ? (target - am + wk - 1) / wk : 1;
+    else j = wk ? (target - am) / wk + 1 : 1;
+    if (j < 1) j = 1;
+    if (j > tie) j = tie;
+    // the j-th token (in index order) with the boundary key
+    const int len = (V + blockDim.x - 1) / blockDim.x;
+    const int lo = min(V, tid * len), hi = min(V, lo + len);
+    unsigned int c = 0;
+    for (int i = lo; i < hi; ++i) c += order_key(z[i]) == prefix;
+    unsigned int inc = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned int o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+    }
+    if (lane == 31) sm.scan_c[warp] = inc;
+    if (tid == 0) {
+        sm.rank = ac + (uint32_t)j - 1;
+        sm.mass_through = am + j * wk;
+        sm.found = 0;
+    }
+    __syncthreads();
+    unsigned int base = 0;
+    for (int w = 0; w < warp; ++w) base += sm.scan_c[w];
+    const unsigned int excl = base + inc - c;
+    if (c > 0 && j > excl && j <= excl + c) {
+        unsigned int need = (unsigned int)(j - excl);
+        for (int i = lo; i < hi; ++i)
+            if (order_key(z[i]) == prefix && --need == 0) {
+                sm.found = i;
+                break;
+            }
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict__ logits, int V, float t,
@@ -215,7 +356,6 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     extern __shared__ __align__(16) uint8_t samp_smem_raw[];
     SampSmem& sm = *reinterpret_cast<SampSmem*>(samp_smem_raw);
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n_warps = blockDim.x >> 5;
     const float* z = logits + (size_t)row * V;
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -235,7 +375,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     if (lane == 0) { sm.red_v[warp] = best; sm.red_i[warp] = bi; }
     __syncthreads();
     if (tid == 0) {
-        for (int w = 1; w < n_warps; ++w)
+        for (int w = 1; w < kWarps; ++w)
             if (sm.red_v[w] > best || (sm.red_v[w] == best && sm.red_i[w] < bi)) { best = sm.red_v[w]; bi = sm.red_i[w]; }
         sm.red_v[0] = best;
         sm.red_i[0] = bi == INT32_MAX ? 0 : bi;
@@ -247,31 +387,35 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
         if (tid == 0) ids[row] = argmax;
         return;
     }
-    __syncthreads();
 
-    // 2. the level-0 histogram (per warp, then summed) and the normaliser Z
-    for (int i = tid; i < kWarps * kBins; i += blockDim.x) {
-        (&sm.pc[0][0])[i] = 0;
-        (&sm.pm[0][0])[i] = 0;
-    }
+    // 2. the level-0 histogram (per warp, the tail bin in registers) and the normaliser Z
+    zero_warp_histograms(sm);
     __syncthreads();
+    unsigned int tail_c = 0;
+    unsigned long long tail_m = 0;
     for (int i = tid; i < V; i += blockDim.x) {
         const float zi = z[i];
         const int b = level0_bin(zi, m, t);
-        atomicAdd(&sm.pc[warp][b], 1u);
-        atomicAdd(&sm.pm[warp][b], weight_of(zi, m, t));
+        const unsigned long long w = weight_of(zi, m, t);
+        if (b == kTailBin) {
+            ++tail_c;
+            tail_m += w;
+        } else {
+            atomicAdd(&sm.u.h.pc[warp][b], 1u);
+            atomicAdd(&sm.u.h.pm[warp][b], w);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        tail_c += __shfl_xor_sync(0xffffffffu, tail_c, off);
+        tail_m += __shfl_xor_sync(0xffffffffu, tail_m, off);
+    }
+    if (lane == 0) {
+        sm.u.h.pc[warp][kTailBin] += tail_c;
+        sm.u.h.pm[warp][kTailBin] += tail_m;
     }
     __syncthreads();
-    for (int b = tid; b < kBins; b += blockDim.x) {
-        unsigned int c = 0;
-        unsigned long long ms = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            c += sm.pc[w][b];
-            ms += sm.pm[w][b];
-        }
-        sm.cnt0[b] = c;
-        sm.mass0[b] = ms;
-    }
+    sum_warp_histograms(sm, sm.cnt0, sm.mass0);
     __syncthreads();
     unsigned long long Z = 0;   // every warp sums the 256 bins (8 per lane)
 #pragma unroll
@@ -283,10 +427,10 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     uint32_t n_k = (uint32_t)V;
     unsigned long long S_k = Z;
     if (top_k > 0 && top_k < V) {
-        const Sel s = select_boundary<SEL_COUNT_GE>(z, V, m, t, (unsigned long long)top_k, sm);
-        const unsigned long long w = weight_of(key_logit(s.key), m, t);
+        find_boundary<SEL_COUNT_GE>(z, V, m, t, (unsigned long long)top_k, sm);
         n_k = (uint32_t)top_k;
-        S_k = s.above_m + (unsigned long long)(top_k - s.above_c) * w;
+        S_k = sm.mass_through;
+        __syncthreads();
     }
     // 4. top-p: the fewest first tokens whose mass reaches p of the total
     uint32_t n_p = (uint32_t)V;
@@ -294,13 +438,10 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     if (p_q24 < (1u << 24)) {
         unsigned long long target = mul_shift24(p_q24, Z, true);
         if (target == 0) target = 1;
-        const Sel s = select_boundary<SEL_MASS_GE>(z, V, m, t, target, sm);
-        const unsigned long long w = weight_of(key_logit(s.key), m, t);
-        unsigned long long j = w ? (target - s.above_m + w - 1) / w : 1;
-        if (j < 1) j = 1;
-        if (j > s.tie_c) j = s.tie_c;
-        n_p = s.above_c + (uint32_t)j;
-        S_p = s.above_m + j * w;
+        find_boundary<SEL_MASS_GE>(z, V, m, t, target, sm);
+        n_p = sm.rank + 1;
+        S_p = sm.mass_through;
+        __syncthreads();
     }
     const unsigned long long S = n_k <= n_p ? S_k : S_p;
 
@@ -309,40 +450,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     u = u > 0.0f ? u : 0.0f;
     unsigned long long u_q24 = (unsigned long long)(u * 16777216.0f);
     if (u_q24 > (1ull << 24) - 1) u_q24 = (1ull << 24) - 1;
-    const unsigned long long target = mul_shift24(u_q24, S, false);
-    const Sel s = select_boundary<SEL_MASS_GT>(z, V, m, t, target, sm);
-    const unsigned long long w = weight_of(key_logit(s.key), m, t);
-    unsigned long long j = w ? (target - s.above_m) / w + 1 : 1;
-    if (j > s.tie_c) j = s.tie_c;
-    if (j < 1) j = 1;
-
-    // 6. the j-th token (in index order) among those with the boundary key
-    const int len = (V + blockDim.x - 1) / blockDim.x;
-    const int lo = min(V, tid * len), hi = min(V, lo + len);
-    unsigned int c = 0;
-    for (int i = lo; i < hi; ++i) c += order_key(z[i]) == s.key;
-    // exclusive scan of c over the block in thread order
-    unsigned int inc = c;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const unsigned int o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-    }
-    if (lane == 31) sm.scan[warp] = inc;
-    if (tid == 0) sm.found = argmax;
-    __syncthreads();
-    unsigned int base = 0;
-    for (int w2 = 0; w2 < warp; ++w2) base += sm.scan[w2];
-    const unsigned int excl = base + inc - c;
-    if (c > 0 && j > excl && j <= excl + c) {
-        unsigned int need = (unsigned int)(j - excl);
-        for (int i = lo; i < hi; ++i)
-            if (order_key(z[i]) == s.key && --need == 0) {
-                sm.found = i;
-                break;
-            }
-    }
-    __syncthreads();
+    find_boundary<SEL_MASS_GT>(z, V, m, t, mul_shift24(u_q24, S, false), sm);
     if (tid == 0) ids[row] = sm.found;
 }
 
