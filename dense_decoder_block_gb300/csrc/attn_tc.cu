@@ -383,10 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 //                TMEM lane quarter, exchanging the row max and two quarter sums
 //                through shared memory; P (bf16 pairs) overwrites the first 64
 //                columns of the S row once both halves hold their scores, the
-//                row's (m, l) goes to columns 64, 65.  (One warpgroup per chunk
-//                on alternate chunks, thread = row, gave the same chunk time: it
-//                is set by the chain softmax -> PV -> fold -> next S, not by one
-//                warp's softmax.)
+//                row's (m, l) goes to shared memory for the fold, so the next S
+//                into that buffer waits for nothing but its K chunk.
 //   warps 12-15  fold of every chunk into the running (O, M, L), thread = row,
 //                with the row's O in registers; then o = O * (1 / L)
 // Warp 3 only keeps the roles aligned to warpgroups.  A chunk that is wholly
@@ -406,11 +404,14 @@ constexpr int PF_OFF_K = 2 * kSub;                   // [stage] K: 2 sub-tiles
 constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
 constexpr int PF_OFF_BAR = PF_OFF_V + 4 * kSub;
 constexpr int PF_OFF_XCH = PF_OFF_BAR + 256;         // softmax halves' exchange: 4 x 128 floats
-constexpr int PF_SMEM_BYTES = PF_OFF_XCH + 2048 + 1024;
+constexpr int PF_OFF_ML = PF_OFF_XCH + 2048;         // [chunk % 4][row] (m, l) of each row, for the fold
+constexpr int PF_SMEM_BYTES = PF_OFF_ML + 4 * 128 * 8 + 1024;
 constexpr int PF_TM_S = 0, PF_TM_OC = 256;   // S[parity] at 0 / 128, O_c[parity] at 256 / 384
-// In S[parity], the softmax leaves P (bf16 pairs) in columns 0..63 and the row's
-// (m, l) in columns 64, 65.
-constexpr int PF_TM_ML = 64;
+// In S[parity], the softmax leaves P (bf16 pairs) in columns 0..63; the row's
+// (m, l) goes to shared memory, four chunks deep: the fold of chunk i has read it
+// before the softmax of chunk i + 4 can start (S(i + 4) is issued after PV(i + 2),
+// which waits for the fold to release O_c of chunk i), so S(i + 2) needs nothing
+// from the fold and the MMA issues it right behind PV(i).
 static_assert(PF_SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // Barrier of `n` threads (whole warps) on hardware barrier `id` (1..15; 0 is
@@ -428,10 +429,10 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 // ascending key order -- half 0 holds L0, L1, half 1 passes L2, L3 over.  Block c
 // (keys 16c .. 16c+15) of P, packed as bf16 pairs, goes to columns 8c .. 8c+7 of
 // the S row once both halves hold their scores in registers; half 0 writes the
-// row's (m, l) to the ML columns.  `xch` is 4 x 128 floats of shared memory; `bar`
-// the barrier id of this lane quarter.
+// row's (m, l) to *ml.  `xch` is 4 x 128 floats of shared memory; `bar` the
+// barrier id of this lane quarter.
 __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int row, int jmax, float scale_log2,
-                                                  float* xch, int bar, float& m_out) {
+                                                  float* xch, int bar, float2* ml, float& m_out) {
     float v[64];
     ptx::tmem_ld<32>(s_taddr + h * 64, v);
     ptx::tmem_ld<32>(s_taddr + h * 64 + 32, v + 32);
@@ -480,7 +481,7 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
     named_bar_sync(bar, 64);   // L2, L3 written; the maxima read
     if (h == 0) {
         const float l = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), xch[256 + row]), xch[384 + row]);
-        ptx::tmem_st2(s_taddr + PF_TM_ML, m, l);
+        *ml = make_float2(m, l);
     }
     ptx::tmem_wait_st();
     m_out = m;
@@ -499,7 +500,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint64_t* v_empty = bars + 7;    // [2] MMA (after PV) -> TMA
     uint64_t* s_full = bars + 9;     // [2] MMA (after S) -> softmax
     uint64_t* p_full = bars + 11;    // [2] softmax (P, m, l written) -> MMA, fold
-    uint64_t* s_free = bars + 13;    // [2] fold (m, l read) -> MMA
     uint64_t* oc_full = bars + 15;   // [2] MMA (after PV) -> fold
     uint64_t* oc_free = bars + 17;   // [2] fold (O_c read) -> MMA
     uint32_t* tmem_holder = (uint32_t*)(bars + 19);
@@ -531,7 +531,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ptx::mbar_init(&v_empty[i], 1);
             ptx::mbar_init(&s_full[i], 1);
             ptx::mbar_init(&p_full[i], 8);
-            ptx::mbar_init(&s_free[i], 4);
             ptx::mbar_init(&oc_full[i], 1);
             ptx::mbar_init(&oc_free[i], 4);
         }
@@ -593,8 +592,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const uint32_t q_addr = ptx::smem_u32(sm + PF_OFF_Q);
                 auto issue_s = [&](int i) -> bool {
                     const int k = i & 1;
+                    // S(i) overwrites the S buffer of chunk i - 2: PV(i - 2), which read its P,
+                    // was issued before and the MMAs run in issue order; its (m, l) is in
+                    // shared memory
                     if (!ptx::mbar_wait(&k_full[k], (i >> 1) & 1, err)) return false;
-                    if (i >= 2 && !ptx::mbar_wait(&s_free[k], ((i >> 1) & 1) ^ 1, err)) return false;
                     ptx::tc_fence_after();
                     const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
 #pragma unroll
@@ -647,7 +648,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
             float m;
             // both halves reach the two barriers inside on every chunk, whatever `ok` says
-            softmax_half_tmem(tmem + lane_addr + PF_TM_S + k * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, m);
+            float2* ml = reinterpret_cast<float2*>(sm + PF_OFF_ML) + (i & 3) * 128 + row;
+            softmax_half_tmem(tmem + lane_addr + PF_TM_S + k * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, ml,
+                              m);
             if (h == 0) {
                 // value rows past the last visible key of this tile are zeroed (they may hold
                 // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
@@ -683,14 +686,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int i = 0; i < n_iter; ++i) {
             const int k = i & 1;
             if (ok) ok = ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err);
-            ptx::tc_fence_after();
-            float ml[2];
-            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + k * 128 + PF_TM_ML, ml);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s_free[k]);
-            const float m = ml[0], l = ml[1];
+            const float2 ml = reinterpret_cast<const float2*>(sm + PF_OFF_ML)[(i & 3) * 128 + row];
+            const float m = ml.x, l = ml.y;
             if (ok) ok = ptx::mbar_wait(&oc_full[k], (i >> 1) & 1, err);
             ptx::tc_fence_after();
             // Per row: skip a chunk with no visible key, start from the first one, fold the

@@ -5,7 +5,8 @@
 //
 // One CTA per row.  Token order is by decreasing logit, equal logits by
 // increasing index (the greedy tie rule).  Each token's softmax weight
-// e^{(z - max)/T} is evaluated in fp32 and held as a 2^-40 fixed-point integer,
+// e^{(z - max)/T} is evaluated in fp32 (the hardware 2^x, relative error below
+// 2^-22) and held as a 2^-40 fixed-point integer,
 // so every sum of weights -- the normaliser, the mass of a set of tokens, the
 // cumulative mass up to a token -- is an exact integer sum whatever order the
 // threads add in: the kept set and the drawn token do not depend on scheduling.
@@ -68,16 +69,25 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Softmax weight e^{(z - m)/T} of one logit as a 2^-40 fixed-point integer.
-__device__ __forceinline__ unsigned long long weight_of(float z, float m, float t) {
-    const float e = expf(__fdiv_rn(__fsub_rn(z, m), t));
+// Per-row constants: the largest logit m, c = log2(e) / T for the weights and
+// 16 / T for the level-0 bins.
+struct RowScale {
+    float m, c, bin;
+};
+
+// Softmax weight e^{(z - m)/T} = 2^{(z - m) c} of one logit as a 2^-40 fixed-point
+// integer.  ex2.approx (relative error below 2^-22) on the special-function unit:
+// the same value wherever it is evaluated, which is all the searches below need.
+__device__ __forceinline__ unsigned long long weight_of(float z, const RowScale& r) {
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(__fmul_rn(__fsub_rn(z, r.m), r.c)));
     return __float2ull_rn(__fmul_rn(e, kMassScale));
 }
 
 // Level-0 bin of a logit: floor(16 (m - z) / T), at most 255 (monotone in z: a bin
 // is an interval of logits, bin 0 the highest).
-__device__ __forceinline__ int level0_bin(float z, float m, float t) {
-    return (int)fminf(__fmul_rn(__fdiv_rn(__fsub_rn(m, z), t), kBinsPerNat), (float)(kBins - 1));
+__device__ __forceinline__ int level0_bin(float z, const RowScale& r) {
+    return (int)fminf(__fmul_rn(__fsub_rn(r.m, z), r.bin), (float)(kBins - 1));
 }
 
 // ceil or floor of a * b / 2^24 for a <= 2^24, b < 2^57 (the product needs 81 bits).
@@ -196,7 +206,7 @@ __device__ __forceinline__ bool reached(uint32_t count, unsigned long long mass,
 // exceeds it (SEL_MASS_GT).  Leaves in sm its 0-based rank (sm.rank), the mass of
 // the tokens up to and including it (sm.mass_through) and its index (sm.found).
 template <int MODE>
-__device__ void find_boundary(const float* __restrict__ z, int V, float m, float t, unsigned long long target,
+__device__ void find_boundary(const float* __restrict__ z, int V, const RowScale& rs, unsigned long long target,
                               SampSmem& sm) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (warp == 0) scan_bins<MODE, true>(sm.cnt0, sm.mass0, 0u, 0ull, target, sm);
@@ -211,7 +221,7 @@ __device__ void find_boundary(const float* __restrict__ z, int V, float m, float
         for (int i0 = 0; i0 < V; i0 += blockDim.x) {
             const int i = i0 + tid;
             const float zi = i < V ? z[i] : 0.f;
-            const bool in = i < V && level0_bin(zi, m, t) == b0;
+            const bool in = i < V && level0_bin(zi, rs) == b0;
             const unsigned ballot = __ballot_sync(0xffffffffu, in);
             if (ballot) {
                 unsigned int base = 0;
@@ -248,7 +258,7 @@ __device__ void find_boundary(const float* __restrict__ z, int V, float m, float
         const int seg = (n + blockDim.x - 1) / blockDim.x;
         const int lo = min(n, tid * seg), hi = min(n, lo + seg);
         unsigned long long ms = 0;
-        for (int i = lo; i < hi; ++i) ms += weight_of(key_logit((uint32_t)(sm.u.list[i] >> 32)), m, t);
+        for (int i = lo; i < hi; ++i) ms += weight_of(key_logit((uint32_t)(sm.u.list[i] >> 32)), rs);
         unsigned long long inc = ms;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -271,7 +281,7 @@ __device__ void find_boundary(const float* __restrict__ z, int V, float m, float
         __syncthreads();
         for (int i = lo; i < hi; ++i) {
             const unsigned long long e = sm.u.list[i];
-            const unsigned long long w = weight_of(key_logit((uint32_t)(e >> 32)), m, t);
+            const unsigned long long w = weight_of(key_logit((uint32_t)(e >> 32)), rs);
             const bool before = reached<MODE>(above_c + (uint32_t)i, run, target);
             run += w;
             if (!before && reached<MODE>(above_c + (uint32_t)i + 1, run, target)) {
@@ -294,12 +304,12 @@ __device__ void find_boundary(const float* __restrict__ z, int V, float m, float
         __syncthreads();
         for (int i = tid; i < V; i += blockDim.x) {
             const float zi = z[i];
-            if (level0_bin(zi, m, t) != b0) continue;
+            if (level0_bin(zi, rs) != b0) continue;
             const uint32_t k = order_key(zi);
             if (r > 0 && ((k ^ prefix) >> (shift + 8)) != 0) continue;
             const uint32_t bin = (k >> shift) & (kBins - 1);
             atomicAdd(&sm.u.h.pc[warp][bin], 1u);
-            atomicAdd(&sm.u.h.pm[warp][bin], weight_of(zi, m, t));
+            atomicAdd(&sm.u.h.pm[warp][bin], weight_of(zi, rs));
         }
         __syncthreads();
         sum_warp_histograms(sm, sm.cnt, sm.mass);
@@ -308,7 +318,7 @@ __device__ void find_boundary(const float* __restrict__ z, int V, float m, float
         __syncthreads();
         prefix |= sm.chosen << shift;
     }
-    const unsigned long long wk = weight_of(key_logit(prefix), m, t);
+    const unsigned long long wk = weight_of(key_logit(prefix), rs);
     const uint32_t ac = sm.above_c, tie = sm.tie_c;
     const unsigned long long am = sm.above_m;
     unsigned long long j;   // how many tokens of the tie group the target needs (1-based)
@@ -388,6 +398,11 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
         return;
     }
 
+    RowScale rs;
+    rs.m = m;
+    rs.c = __fdiv_rn(1.4426950408889634f, t);
+    rs.bin = __fdiv_rn(kBinsPerNat, t);
+
     // 2. the level-0 histogram (per warp, the tail bin in registers) and the normaliser Z
     zero_warp_histograms(sm);
     __syncthreads();
@@ -395,8 +410,8 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     unsigned long long tail_m = 0;
     for (int i = tid; i < V; i += blockDim.x) {
         const float zi = z[i];
-        const int b = level0_bin(zi, m, t);
-        const unsigned long long w = weight_of(zi, m, t);
+        const int b = level0_bin(zi, rs);
+        const unsigned long long w = weight_of(zi, rs);
         if (b == kTailBin) {
             ++tail_c;
             tail_m += w;
@@ -427,7 +442,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     uint32_t n_k = (uint32_t)V;
     unsigned long long S_k = Z;
     if (top_k > 0 && top_k < V) {
-        find_boundary<SEL_COUNT_GE>(z, V, m, t, (unsigned long long)top_k, sm);
+        find_boundary<SEL_COUNT_GE>(z, V, rs, (unsigned long long)top_k, sm);
         n_k = (uint32_t)top_k;
         S_k = sm.mass_through;
         __syncthreads();
@@ -438,7 +453,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     if (p_q24 < (1u << 24)) {
         unsigned long long target = mul_shift24(p_q24, Z, true);
         if (target == 0) target = 1;
-        find_boundary<SEL_MASS_GE>(z, V, m, t, target, sm);
+        find_boundary<SEL_MASS_GE>(z, V, rs, target, sm);
         n_p = sm.rank + 1;
         S_p = sm.mass_through;
         __syncthreads();
@@ -450,7 +465,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     u = u > 0.0f ? u : 0.0f;
     unsigned long long u_q24 = (unsigned long long)(u * 16777216.0f);
     if (u_q24 > (1ull << 24) - 1) u_q24 = (1ull << 24) - 1;
-    find_boundary<SEL_MASS_GT>(z, V, m, t, mul_shift24(u_q24, S, false), sm);
+    find_boundary<SEL_MASS_GT>(z, V, rs, mul_shift24(u_q24, S, false), sm);
     if (tid == 0) ids[row] = sm.found;
 }
 

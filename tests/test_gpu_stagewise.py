@@ -210,12 +210,18 @@ def check_attention(name, q, kc, vc, positions, got):
 
 # ----------------------------------------------------------------------------- the test
 
-@pytest.fixture(scope="module")
-def run():
+@pytest.fixture(scope="module", params=[1.0, 0.02], ids=["x-N(0,1)", "x-N(0,0.02)"])
+def run(request):
     """GPU: prefill B x T at the 8B shape, then one decode step at position T.
-    Returns the inputs, the GPU intermediates of both calls and the GPU cache."""
+    Returns the inputs, the GPU intermediates of both calls and the GPU cache.
+    Two input scales: the block workloads' x ~ N(0, 1), and x ~ N(0, 0.02) -- the
+    first block of the stack, whose input is an embedding row of N(0, 0.02)
+    weights, so that the branches are some fifty times larger than the residual
+    and nothing of theirs hides under its rounding."""
     max_seq = T + 8
     inp = workloads.make_block_inputs(DIMS, B, T + 1, max_seq=max_seq, random_gains=True)
+    if request.param != 1.0:
+        inp.x = (inp.x.float() * request.param).to(torch.bfloat16)
     blk, ddb = gpu_block(inp, max_seq)
     dev = torch.device("cuda:0")
     kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
@@ -235,7 +241,7 @@ def run():
     w = {k: _to64(v) for k, v in inp.weights.items()}
     g = {k: _to64(v) for k, v in inp.gains.items()}
     return dict(x=_to64(inp.x), w=w, g=g, pf=mid_p, dec=mid_d, y_p=_to64(y_p), y_d=_to64(y_d),
-                kc=_to64(kc), vc=_to64(vc))
+                kc=_to64(kc), vc=_to64(vc), scale=request.param)
 
 
 @pytest.mark.parametrize("mode", ["prefill", "decode"])
@@ -250,7 +256,7 @@ def test_each_stage_matches_the_oracle_step(run, mode):
         mid, y, tok = r["dec"], r["y_d"].reshape(B, -1), [T]
         x = r["x"][:, T:T + 1].reshape(B, -1)
     nt = len(tok)
-    tag = f"{mode} 8B B={B}" + (f" T={T}" if mode == "prefill" else f" pos={T}")
+    tag = f"{mode} 8B B={B}" + (f" T={T}" if mode == "prefill" else f" pos={T}") + f" x*{r['scale']}"
     # 1. RMSNorm_1
     check_rmsnorm(f"{tag} xn", x, g["g_attn"], mid["xn"])
     xn = mid["xn"]
