@@ -726,7 +726,7 @@ extern "C" int llama_lmhead_argmax(const void* h, int batch, int h_stride, const
 
 extern "C" int llama_sample(const float* logits, int batch, int vocab, float temperature, int top_k, float top_p,
                             const float* uniforms, int32_t* ids, void* stream) {
-    if (batch < 0 || vocab <= 0 || vocab > (1 << 23) || batch > 65535) return LLAMA_ERR_INVALID_ARG;
+    if (batch < 0 || vocab <= 0 || vocab > (1 << 20) || batch > 65535) return LLAMA_ERR_INVALID_ARG;
     if (!(temperature >= 0.f) || std::isinf(temperature) || top_k < 0 || !(top_p > 0.f && top_p <= 1.f))
         return LLAMA_ERR_INVALID_ARG;
     if (batch == 0) return LLAMA_OK;

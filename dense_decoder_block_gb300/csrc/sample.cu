@@ -40,8 +40,12 @@ constexpr int kListCap = 16384;                  // tokens of one level-0 bin so
 struct SampSmem {
     union {
         struct {
-            unsigned int pc[kWarps][kBins];      // histograms kept per warp
-            unsigned long long pm[kWarps][kBins];
+            // histograms kept per warp; a bin's mass in three 32-bit parts of 14, 14 and 13
+            // bits (native 32-bit shared atomics; a warp adds at most 2^15 weights of at
+            // most 2^40, so no part overflows)
+            unsigned int pc[kWarps][kBins];
+            unsigned int pm[kWarps][kBins][3];
+            unsigned long long tail_m[kWarps];   // the tail bin's mass, summed in registers
         } h;
         unsigned long long list[kListCap];       // one bin's tokens: key << 32 | (~index)
     } u;
@@ -182,7 +186,9 @@ __device__ __forceinline__ void sum_warp_histograms(SampSmem& sm, unsigned int* 
         unsigned long long ms = 0;
         for (int w = 0; w < kWarps; ++w) {
             c += sm.u.h.pc[w][b];
-            ms += sm.u.h.pm[w][b];
+            ms += (unsigned long long)sm.u.h.pm[w][b][0] + ((unsigned long long)sm.u.h.pm[w][b][1] << 14) +
+                  ((unsigned long long)sm.u.h.pm[w][b][2] << 28);
+            if (b == kTailBin) ms += sm.u.h.tail_m[w];
         }
         cnt[b] = c;
         mass[b] = ms;
@@ -192,8 +198,19 @@ __device__ __forceinline__ void sum_warp_histograms(SampSmem& sm, unsigned int* 
 __device__ __forceinline__ void zero_warp_histograms(SampSmem& sm) {
     for (int i = threadIdx.x; i < kWarps * kBins; i += blockDim.x) {
         (&sm.u.h.pc[0][0])[i] = 0;
-        (&sm.u.h.pm[0][0])[i] = 0;
+        (&sm.u.h.pm[0][0][0])[3 * i] = 0;
+        (&sm.u.h.pm[0][0][0])[3 * i + 1] = 0;
+        (&sm.u.h.pm[0][0][0])[3 * i + 2] = 0;
     }
+    if (threadIdx.x < kWarps) sm.u.h.tail_m[threadIdx.x] = 0;
+}
+
+// One token into warp `w`'s histogram: its count and its weight's three parts.
+__device__ __forceinline__ void add_to_warp_histogram(SampSmem& sm, int w, int bin, unsigned long long weight) {
+    atomicAdd(&sm.u.h.pc[w][bin], 1u);
+    atomicAdd(&sm.u.h.pm[w][bin][0], (unsigned int)(weight & 0x3fffull));
+    atomicAdd(&sm.u.h.pm[w][bin][1], (unsigned int)((weight >> 14) & 0x3fffull));
+    atomicAdd(&sm.u.h.pm[w][bin][2], (unsigned int)(weight >> 28));
 }
 
 template <int MODE>
@@ -308,8 +325,7 @@ __device__ void find_boundary(const float* __restrict__ z, int V, const RowScale
             const uint32_t k = order_key(zi);
             if (r > 0 && ((k ^ prefix) >> (shift + 8)) != 0) continue;
             const uint32_t bin = (k >> shift) & (kBins - 1);
-            atomicAdd(&sm.u.h.pc[warp][bin], 1u);
-            atomicAdd(&sm.u.h.pm[warp][bin], weight_of(zi, rs));
+            add_to_warp_histogram(sm, warp, bin, weight_of(zi, rs));
         }
         __syncthreads();
         sum_warp_histograms(sm, sm.cnt, sm.mass);
@@ -416,8 +432,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
             ++tail_c;
             tail_m += w;
         } else {
-            atomicAdd(&sm.u.h.pc[warp][b], 1u);
-            atomicAdd(&sm.u.h.pm[warp][b], w);
+            add_to_warp_histogram(sm, warp, b, w);
         }
     }
 #pragma unroll
@@ -427,7 +442,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     }
     if (lane == 0) {
         sm.u.h.pc[warp][kTailBin] += tail_c;
-        sm.u.h.pm[warp][kTailBin] += tail_m;
+        sm.u.h.tail_m[warp] = tail_m;
     }
     __syncthreads();
     sum_warp_histograms(sm, sm.cnt0, sm.mass0);

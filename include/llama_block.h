@@ -289,7 +289,7 @@ int llama_lmhead_argmax_noalloc(const void* h, int batch, int h_stride, const vo
  * summed exactly in 2^-40 fixed point, top_p and the uniforms are taken to 24
  * bits: the result does not depend on thread scheduling.  Logits must be finite
  * (-inf allowed, weight zero).  Requires temperature >= 0, top_k >= 0,
- * 0 < top_p <= 1, 1 <= vocab <= 2^23, batch <= 65535; otherwise
+ * 0 < top_p <= 1, 1 <= vocab <= 2^20, batch <= 65535; otherwise
  * LLAMA_ERR_INVALID_ARG.  No workspace, nothing allocated. */
 int llama_sample(const float* logits, int batch, int vocab, float temperature, int top_k, float top_p,
                  const float* uniforms, int32_t* ids, void* stream);

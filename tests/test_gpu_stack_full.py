@@ -16,7 +16,11 @@ layers, and the comparison is made layer by layer instead ("hidden states
 teacher-forced", like the token teacher forcing): each block of the GPU stack
 is checked against the oracle's block applied to that block's GPU input, at
 every position of the prefill and of both decode steps, with the bound every
-block parity test uses (2e-2 of rms beyond two bf16 ulps); the head is checked
+block parity test uses (2e-2 of rms beyond two bf16 ulps).  The first block
+takes the embedding rows, N(0, 0.02): its branches are some fifty times its
+residual, and the composed bound does not describe it (the softmax weights the
+GPU rounds, R8, show through); it is checked stage by stage instead, on the GPU's
+own intermediates of the same call, like tests/test_gpu_stagewise.py; the head is checked
 on the GPU's final hidden state (fp32 logits, max |err| / rms <= 2e-2), and the
 greedy ids wherever the oracle's top-2 margin exceeds twice the error.  The
 free-running difference (the oracle run on its own from the embedding) is
@@ -33,6 +37,7 @@ import workloads
 from oracle import block as ob
 from tests.blockrun import check_bf16_output
 from tests.parity_log import record_parity
+from tests.test_gpu_stagewise import check_block_stages
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +96,26 @@ def test_full_stack_layers_and_head_match_oracle():
     hidden = [np.concatenate(h, axis=1) for h in hidden]   # [2, T + STEPS, d]
     n = T + STEPS
 
+    # block 0 once more on its own, to read its intermediates from the workspace
+    blk0 = st.blocks[0]
+    x0 = torch.empty(B, T, dims.d_model, dtype=torch.bfloat16, device=dev)
+    ddb.llama_embed(ids_dev[:, :T].contiguous(), B * T, w_embed, V, dims.d_model, x0)
+    kv0 = ddb.KVCache(torch.zeros(B, dims.n_kv_heads, T, dims.head_dim, dtype=torch.bfloat16, device=dev),
+                      torch.zeros(B, dims.n_kv_heads, T, dims.head_dim, dtype=torch.bfloat16, device=dev))
+    ws0 = blk0.workspace(B, T)
+    y0 = torch.empty_like(x0)
+    blk0.prefill(x0, kv0, y0, ws0)
+    torch.cuda.synchronize()
+    sel = np.concatenate([np.arange(r * T, (r + 1) * T) for r in ROWS])
+    mid0 = {k: v.double().cpu().numpy()[sel] for k, v in blk0.intermediates(ws0, B, T).items()}
+    y0_rows = y0[ROWS].double().cpu().numpy()
+    assert np.array_equal(y0_rows, hidden[1][:, :T]), "block 0 alone differs from block 0 in the stack"
+    w0 = {k: workloads.to_numpy64(v) for k, v in layers[0][0].items()}
+    g0 = {k: workloads.to_numpy64(v) for k, v in layers[0][1].items()}
+    check_block_stages("32-layer stack block 0 (embedding rows, prefill)", hidden[0][:, :T].reshape(2 * T, -1), mid0,
+                       y0_rows.reshape(2 * T, -1), kv0.k[ROWS].double().cpu().numpy(),
+                       kv0.v[ROWS].double().cpu().numpy(), list(range(T)), w0, g0, len(ROWS))
+
     to64 = workloads.to_numpy64
     assert np.array_equal(hidden[0], ob.embed(ids[ROWS].numpy(), to64(w_embed)))
     free = hidden[0]
@@ -133,6 +158,6 @@ def test_full_stack_layers_and_head_match_oracle():
         fe = np.abs(got - free_ref)
         record_parity(f"[parity] 32-layer stack, {what} logits against the free-running oracle: "
                       f"max|err|/rms = {fe.max() / rms:.3e}, rms err / rms = {np.sqrt(np.mean(fe ** 2)) / rms:.3e}")
-    for l, (raw, frac, beyond, rms_err) in enumerate(figs):
+    for l, (raw, frac, beyond, rms_err) in enumerate(figs[1:], start=1):
         assert beyond <= 2e-2 and rms_err <= 5e-3, f"block {l}: beyond 2 ulps {beyond:.3e}, rms err {rms_err:.3e}"
 

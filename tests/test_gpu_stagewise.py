@@ -255,22 +255,30 @@ def test_each_stage_matches_the_oracle_step(run, mode):
     else:
         mid, y, tok = r["dec"], r["y_d"].reshape(B, -1), [T]
         x = r["x"][:, T:T + 1].reshape(B, -1)
-    nt = len(tok)
     tag = f"{mode} 8B B={B}" + (f" T={T}" if mode == "prefill" else f" pos={T}") + f" x*{r['scale']}"
+    check_block_stages(tag, x, mid, y, r["kc"], r["vc"], tok, w, g, B)
+
+
+def check_block_stages(tag, x, mid, y, kc, vc, tok, w, g, nb):
+    """Every stage of one 8B-shaped block call against the oracle's step on the
+    GPU's own inputs.  x, y [nb * len(tok), d]; mid: the call's intermediates (rows in
+    the same order); kc, vc [nb, Hkv, S, dh] the cache after the call; tok: the
+    positions of the call's tokens (the same for every sequence)."""
+    hq, hkv, dh = DIMS.n_heads, DIMS.n_kv_heads, DIMS.head_dim
+    nt = len(tok)
     # 1. RMSNorm_1
     check_rmsnorm(f"{tag} xn", x, g["g_attn"], mid["xn"])
     xn = mid["xn"]
     ang = ob.rope_angles(tok, dh, DIMS.rope_theta)                     # [nt, dh/2]
-    ang_m = np.tile(ang, (B, 1))[:, None, :]                           # [B*nt, 1, dh/2]
+    ang_m = np.tile(ang, (nb, 1))[:, None, :]                          # [nb*nt, 1, dh/2]
     # 2-3. projections, RoPE, cache rows
-    check_rotated(f"{tag} q (rotated)", xn, w["wq"], hq, ang_m, mid["q"].reshape(B * nt, hq, dh))
-    k_got = r["kc"][:, :, tok].transpose(0, 2, 1, 3).reshape(B * nt, hkv, dh)
+    check_rotated(f"{tag} q (rotated)", xn, w["wq"], hq, ang_m, mid["q"].reshape(nb * nt, hq, dh))
+    k_got = kc[:, :, tok].transpose(0, 2, 1, 3).reshape(nb * nt, hkv, dh)
     check_rotated(f"{tag} k cache rows", xn, w["wk"], hkv, ang_m, k_got)
-    v_got = r["vc"][:, :, tok].transpose(0, 2, 1, 3).reshape(B * nt, hkv * dh)
+    v_got = vc[:, :, tok].transpose(0, 2, 1, 3).reshape(nb * nt, hkv * dh)
     check_projection(f"{tag} v cache rows", xn, w["wv"], v_got)
     # 4. attention from the GPU's q and cache
-    check_attention(f"{tag} o", mid["q"].reshape(B, nt, hq, dh), r["kc"], r["vc"], tok,
-                    mid["o"].reshape(B, nt, hq * dh))
+    check_attention(f"{tag} o", mid["q"].reshape(nb, nt, hq, dh), kc, vc, tok, mid["o"].reshape(nb, nt, hq * dh))
     # 5. O projection + residual
     check_residual(f"{tag} h", x, mid["o"], w["wo"], mid["h"])
     # 6. RMSNorm_2
