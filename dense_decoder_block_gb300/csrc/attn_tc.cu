@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Pipelined prefill attention.  Same unit (one 128-row query tile of a KV group,
 // its chunks in ascending order) and the same arithmetic as above, split over
 // roles that overlap:
-//   warp 0       TMA: the Q tile once, then K chunks through a two-stage ring
-//   warp 2       TMA: V chunks through a two-stage ring (K(i+2) loads once S(i)
+//   warp 0       TMA: the Q tile once, then K chunks through a three-stage ring
+//   warp 2       TMA: V chunks through a two-stage ring (K(i+3) loads once S(i)
 //                has read K(i); V(i+2) once PV(i) has read V(i))
 //   warp 1       TMEM owner + MMA: PV(i) into O_c[i % 2] with P read from
 //                TMEM, then S(i+2) = Q K^T into the S buffer that chunk i used
@@ -399,10 +399,16 @@ constexpr int kPfRegsSoftmax = 112;
 constexpr int kPfRegsFold = 232;
 constexpr int kPfRegsNeeded = 128 * kPfRegsCtrl + 256 * kPfRegsSoftmax + 128 * kPfRegsFold;
 static_assert(kPfRegsNeeded <= 128 * kPfThreads, "register split exceeds the launch allocation");
-constexpr int PF_OFF_Q = 0;                          // Q: 2 sub-tiles
-constexpr int PF_OFF_K = 2 * kSub;                   // [stage] K: 2 sub-tiles
-constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
-constexpr int PF_OFF_BAR = PF_OFF_V + 4 * kSub;
+// K and V stream through rings of their own.  K is three chunks deep: a chunk of K
+// is requested when S two chunks back has read its slot, and under load its copy
+// takes about as long as two chunks of compute, so a two-deep ring left the next
+// S waiting for its K (measured per chunk in one CTA's timeline at T = 8192).
+constexpr int kPfStagesK = 3;
+constexpr int kPfStagesV = 2;
+constexpr int PF_OFF_Q = 0;                                    // Q: 2 sub-tiles
+constexpr int PF_OFF_K = 2 * kSub;                             // [stage] K: 2 sub-tiles
+constexpr int PF_OFF_V = PF_OFF_K + kPfStagesK * 2 * kSub;     // [stage] V: 2 sub-tiles
+constexpr int PF_OFF_BAR = PF_OFF_V + kPfStagesV * 2 * kSub;
 constexpr int PF_OFF_XCH = PF_OFF_BAR + 256;         // softmax halves' exchange: 4 x 128 floats
 constexpr int PF_OFF_ML = PF_OFF_XCH + 2048;         // [chunk % 4][row] (m, l) of each row, for the fold
 constexpr int PF_SMEM_BYTES = PF_OFF_ML + 4 * 128 * 8 + 1024;
@@ -494,15 +500,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + PF_OFF_BAR);
     uint64_t* q_full = bars + 0;
-    uint64_t* k_full = bars + 1;     // [2] TMA -> MMA
-    uint64_t* k_empty = bars + 3;    // [2] MMA (after S) -> TMA
-    uint64_t* v_full = bars + 5;     // [2] TMA -> MMA (and the softmax, before it zeroes rows)
-    uint64_t* v_empty = bars + 7;    // [2] MMA (after PV) -> TMA
-    uint64_t* s_full = bars + 9;     // [2] MMA (after S) -> softmax
-    uint64_t* p_full = bars + 11;    // [2] softmax (P, m, l written) -> MMA, fold
-    uint64_t* oc_full = bars + 15;   // [2] MMA (after PV) -> fold
-    uint64_t* oc_free = bars + 17;   // [2] fold (O_c read) -> MMA
-    uint32_t* tmem_holder = (uint32_t*)(bars + 19);
+    uint64_t* k_full = bars + 1;                           // [K stages] TMA -> MMA
+    uint64_t* k_empty = k_full + kPfStagesK;               // [K stages] MMA (after S) -> TMA
+    uint64_t* v_full = k_empty + kPfStagesK;               // [V stages] TMA -> MMA (and the softmax, before it zeroes rows)
+    uint64_t* v_empty = v_full + kPfStagesV;               // [V stages] MMA (after PV) -> TMA
+    uint64_t* s_full = v_empty + kPfStagesV;               // [2] MMA (after S) -> softmax
+    uint64_t* p_full = s_full + 2;                         // [2] softmax (P, m, l written) -> MMA, fold
+    uint64_t* oc_full = p_full + 2;                        // [2] MMA (after PV) -> fold
+    uint64_t* oc_free = oc_full + 2;                       // [2] fold (O_c read) -> MMA
+    uint32_t* tmem_holder = (uint32_t*)(oc_free + 2);
+    static_assert(1 + 2 * kPfStagesK + 2 * kPfStagesV + 8 + 1 <= 32, "barriers fit their 256 bytes");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
@@ -525,14 +532,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&k_full[i], 1);
-            ptx::mbar_init(&k_empty[i], 1);
-            ptx::mbar_init(&v_full[i], 1);
-            ptx::mbar_init(&v_empty[i], 1);
             ptx::mbar_init(&s_full[i], 1);
             ptx::mbar_init(&p_full[i], 8);
             ptx::mbar_init(&oc_full[i], 1);
             ptx::mbar_init(&oc_free[i], 4);
+        }
+        for (int i = 0; i < kPfStagesK; ++i) {
+            ptx::mbar_init(&k_full[i], 1);
+            ptx::mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < kPfStagesV; ++i) {
+            ptx::mbar_init(&v_full[i], 1);
+            ptx::mbar_init(&v_empty[i], 1);
         }
         ptx::fence_mbar_init();
     }
@@ -571,10 +582,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                             : "memory");
                 }
                 const int head_row0 = (b * a.n_kv_heads + g) * a.kv_seq;
+                const int n_st = is_k ? kPfStagesK : kPfStagesV;
                 int issued = 0;
                 for (int i = 0; i < n_iter; ++i, ++issued) {
-                    const int st = i & 1;
-                    if (i >= 2 && !ptx::mbar_wait(&empty[st], ((i >> 1) & 1) ^ 1, err)) break;
+                    const int st = i % n_st;
+                    if (i >= n_st && !ptx::mbar_wait(&empty[st], ((i / n_st) & 1) ^ 1, err)) break;
                     uint8_t* dst = ring + st * 2 * kSub;
                     const int row = head_row0 + i * kAttnChunk;
                     ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
@@ -584,20 +596,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 // no copy may still be landing when the CTA exits (it has landed already
                 // unless a wait above gave up)
                 if (is_k) ptx::mbar_wait_drain(q_full, 0);
-                for (int i = max(0, issued - 2); i < issued; ++i) ptx::mbar_wait_drain(&full[i & 1], (i >> 1) & 1);
+                for (int i = max(0, issued - n_st); i < issued; ++i)
+                    ptx::mbar_wait_drain(&full[i % n_st], (i / n_st) & 1);
             }
         } else if (warp == 1) {
             // ------------------------------------------------------------------ MMA issuer
             if (lane == 0) {
                 const uint32_t q_addr = ptx::smem_u32(sm + PF_OFF_Q);
                 auto issue_s = [&](int i) -> bool {
-                    const int k = i & 1;
+                    const int k = i & 1;            // S buffer in TMEM
+                    const int ks_ = i % kPfStagesK;  // K slot
                     // S(i) overwrites the S buffer of chunk i - 2: PV(i - 2), which read its P,
                     // was issued before and the MMAs run in issue order; its (m, l) is in
                     // shared memory
-                    if (!ptx::mbar_wait(&k_full[k], (i >> 1) & 1, err)) return false;
+                    if (!ptx::mbar_wait(&k_full[ks_], (i / kPfStagesK) & 1, err)) return false;
                     ptx::tc_fence_after();
-                    const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
+                    const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + ks_ * 2 * kSub);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
@@ -605,7 +619,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                        ptx::sw128_kmajor_desc(k_addr + off), IDESC_S, ks > 0 ? 1u : 0u);
                     }
                     ptx::umma_commit(&s_full[k]);
-                    ptx::umma_commit(&k_empty[k]);
+                    ptx::umma_commit(&k_empty[ks_]);
                     return true;
                 };
                 bool ok = ptx::mbar_wait(q_full, 0, err);
@@ -615,15 +629,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     const int k = i & 1;
                     if (!ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err)) break;
                     if (i >= 2 && !ptx::mbar_wait(&oc_free[k], ((i >> 1) & 1) ^ 1, err)) break;
-                    if (!ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err)) break;
+                    const int vs = i % kPfStagesV;
+                    if (!ptx::mbar_wait(&v_full[vs], (i / kPfStagesV) & 1, err)) break;
                     ptx::tc_fence_after();
-                    const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + k * 2 * kSub);
+                    const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + vs * 2 * kSub);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)   // P of keys 16ks.. in TMEM columns 8ks..
                         umma_bf16_ts(tmem + PF_TM_OC + k * 128, tmem + PF_TM_S + k * 128 + ks * 8,
                                      ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
                     ptx::umma_commit(&oc_full[k]);
-                    ptx::umma_commit(&v_empty[k]);
+                    ptx::umma_commit(&v_empty[vs]);
                     if (i + 2 < n_iter) ok = issue_s(i + 2);
                 }
             }
@@ -655,17 +670,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 // value rows past the last visible key of this tile are zeroed (they may hold
                 // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
                 // the chunk's V has landed
+                const int vs = i % kPfStagesV;
                 if (i * kAttnChunk + kAttnChunk - 1 > kv_last && ok)
-                    ok = ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err);
+                    ok = ptx::mbar_wait(&v_full[vs], (i / kPfStagesV) & 1, err);
                 if (i * kAttnChunk + row > kv_last) {
-                    uint8_t* vrow = sm + PF_OFF_V + k * 2 * kSub + row * 128;
+                    uint8_t* vrow = sm + PF_OFF_V + vs * 2 * kSub + row * 128;
 #pragma unroll
                     for (int c16 = 0; c16 < 8; ++c16) {
                         *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(vrow + kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
                     }
                 }
-                ptx::fence_proxy_async_smem();
+                // the zeroed rows (generic-proxy writes) must be visible to the PV MMA
+                if (i * kAttnChunk + kAttnChunk - 1 > kv_last) ptx::fence_proxy_async_smem();
             }
             ptx::tc_fence_before();
             __syncwarp();
