@@ -101,6 +101,24 @@ __device__ __forceinline__ unsigned long long mul_shift24(unsigned long long a, 
     return q + ((ceil_ && (lo & 0xffffffull)) ? 1ull : 0ull);
 }
 
+// f(i, z[i]) for this thread's share of the row (i = tid, tid + blockDim, ... in
+// increasing order), eight loads in flight per thread: a pass over a row is
+// otherwise bound by the latency of one load after another.
+constexpr int kRowUnroll = 8;
+template <typename F>
+__device__ __forceinline__ void for_row(const float* __restrict__ z, int V, F&& f) {
+    const int step = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + (kRowUnroll - 1) * step < V; i += kRowUnroll * step) {
+        float v[kRowUnroll];
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) v[u] = __ldg(z + i + u * step);
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) f(i + u * step, v[u]);
+    }
+    for (; i < V; i += step) f(i, __ldg(z + i));
+}
+
 enum SelMode { SEL_COUNT_GE = 0, SEL_MASS_GE = 1, SEL_MASS_GT = 2 };
 
 // Warp 0: scan 256 bins in order (bin o for level 0, where bin 0 is the highest;
@@ -235,18 +253,26 @@ __device__ void find_boundary(const float* __restrict__ z, int V, const RowScale
     const uint32_t n_bin = sm.cnt0[b0];
     if (n_bin <= (uint32_t)kListCap) {
         // ---- level 1: gather the bin's tokens, sort them, scan in order
-        for (int i0 = 0; i0 < V; i0 += blockDim.x) {
-            const int i = i0 + tid;
-            const float zi = i < V ? z[i] : 0.f;
-            const bool in = i < V && level0_bin(zi, rs) == b0;
-            const unsigned ballot = __ballot_sync(0xffffffffu, in);
-            if (ballot) {
-                unsigned int base = 0;
-                if (lane == __ffs(ballot) - 1) base = atomicAdd(&sm.n_list, (unsigned int)__popc(ballot));
-                base = __shfl_sync(0xffffffffu, base, __ffs(ballot) - 1);
-                if (in) {
-                    const unsigned int at = base + __popc(ballot & ((1u << lane) - 1u));
-                    sm.u.list[at] = ((unsigned long long)order_key(zi) << 32) | (unsigned long long)(~(uint32_t)i);
+        for (int i0 = 0; i0 < V; i0 += kRowUnroll * blockDim.x) {   // the same trip count in every warp
+            float v[kRowUnroll];
+#pragma unroll
+            for (int u = 0; u < kRowUnroll; ++u) {
+                const int i = i0 + u * blockDim.x + tid;
+                v[u] = i < V ? __ldg(z + i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kRowUnroll; ++u) {
+                const int i = i0 + u * blockDim.x + tid;
+                const bool in = i < V && level0_bin(v[u], rs) == b0;
+                const unsigned ballot = __ballot_sync(0xffffffffu, in);
+                if (ballot) {
+                    unsigned int base = 0;
+                    if (lane == __ffs(ballot) - 1) base = atomicAdd(&sm.n_list, (unsigned int)__popc(ballot));
+                    base = __shfl_sync(0xffffffffu, base, __ffs(ballot) - 1);
+                    if (in) {
+                        const unsigned int at = base + __popc(ballot & ((1u << lane) - 1u));
+                        sm.u.list[at] = ((unsigned long long)order_key(v[u]) << 32) | (unsigned long long)(~(uint32_t)i);
+                    }
                 }
             }
         }
@@ -258,15 +284,14 @@ __device__ void find_boundary(const float* __restrict__ z, int V, const RowScale
         __syncthreads();
         for (int k = 2; k <= n2; k <<= 1)
             for (int j = k >> 1; j > 0; j >>= 1) {
-                for (int i = tid; i < n2; i += blockDim.x) {
-                    const int ixj = i ^ j;
-                    if (ixj > i) {
-                        const unsigned long long a = sm.u.list[i], b = sm.u.list[ixj];
-                        const bool down = (i & k) == 0;   // descending overall
-                        if (down ? (a < b) : (a > b)) {
-                            sm.u.list[i] = b;
-                            sm.u.list[ixj] = a;
-                        }
+                for (int p = tid; p < (n2 >> 1); p += blockDim.x) {   // pair p: (i, i + j), bit j of i clear
+                    const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+                    const int ixj = i | j;
+                    const unsigned long long a = sm.u.list[i], b = sm.u.list[ixj];
+                    const bool down = (i & k) == 0;   // descending overall
+                    if (down ? (a < b) : (a > b)) {
+                        sm.u.list[i] = b;
+                        sm.u.list[ixj] = a;
                     }
                 }
                 __syncthreads();
@@ -319,14 +344,13 @@ __device__ void find_boundary(const float* __restrict__ z, int V, const RowScale
         const uint32_t above_c0 = sm.above_c;
         const unsigned long long above_m0 = sm.above_m;
         __syncthreads();
-        for (int i = tid; i < V; i += blockDim.x) {
-            const float zi = z[i];
-            if (level0_bin(zi, rs) != b0) continue;
+        for_row(z, V, [&](int, float zi) {
+            if (level0_bin(zi, rs) != b0) return;
             const uint32_t k = order_key(zi);
-            if (r > 0 && ((k ^ prefix) >> (shift + 8)) != 0) continue;
+            if (r > 0 && ((k ^ prefix) >> (shift + 8)) != 0) return;
             const uint32_t bin = (k >> shift) & (kBins - 1);
             add_to_warp_histogram(sm, warp, bin, weight_of(zi, rs));
-        }
+        });
         __syncthreads();
         sum_warp_histograms(sm, sm.cnt, sm.mass);
         __syncthreads();
@@ -388,10 +412,9 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     // 1. the largest logit and its first index
     float best = -INFINITY;
     int bi = INT32_MAX;
-    for (int i = tid; i < V; i += blockDim.x) {
-        const float v = z[i];
-        if (v > best) { best = v; bi = i; }
-    }
+    for_row(z, V, [&](int i, float v) {
+        if (v > best) { best = v; bi = i; }   // increasing i: the first maximum stays
+    });
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, best, off);
@@ -424,8 +447,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
     __syncthreads();
     unsigned int tail_c = 0;
     unsigned long long tail_m = 0;
-    for (int i = tid; i < V; i += blockDim.x) {
-        const float zi = z[i];
+    for_row(z, V, [&](int, float zi) {
         const int b = level0_bin(zi, rs);
         const unsigned long long w = weight_of(zi, rs);
         if (b == kTailBin) {
@@ -434,7 +456,7 @@ __global__ void __launch_bounds__(kSampThreads) k_sample(const float* __restrict
         } else {
             add_to_warp_histogram(sm, warp, b, w);
         }
-    }
+    });
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         tail_c += __shfl_xor_sync(0xffffffffu, tail_c, off);
