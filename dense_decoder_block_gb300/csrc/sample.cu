@@ -108,6 +108,33 @@ constexpr int kRowUnroll = 8;
 template <typename F>
 __device__ __forceinline__ void for_row(const float* __restrict__ z, int V, F&& f) {
     const int step = blockDim.x;
+    if ((V & 3) == 0 && ((uintptr_t)z & 15) == 0) {
+        // 16-byte loads: thread t takes elements 4t .. 4t + 3, then 4(t + step) ..
+        const float4* z4 = reinterpret_cast<const float4*>(z);
+        const int V4 = V >> 2;
+        int i = threadIdx.x;
+        for (; i + (kRowUnroll - 1) * step < V4; i += kRowUnroll * step) {
+            float4 v[kRowUnroll];
+#pragma unroll
+            for (int u = 0; u < kRowUnroll; ++u) v[u] = __ldg(z4 + i + u * step);
+#pragma unroll
+            for (int u = 0; u < kRowUnroll; ++u) {
+                const int e = 4 * (i + u * step);
+                f(e, v[u].x);
+                f(e + 1, v[u].y);
+                f(e + 2, v[u].z);
+                f(e + 3, v[u].w);
+            }
+        }
+        for (; i < V4; i += step) {
+            const float4 v = __ldg(z4 + i);
+            f(4 * i, v.x);
+            f(4 * i + 1, v.y);
+            f(4 * i + 2, v.z);
+            f(4 * i + 3, v.w);
+        }
+        return;
+    }
     int i = threadIdx.x;
     for (; i + (kRowUnroll - 1) * step < V; i += kRowUnroll * step) {
         float v[kRowUnroll];
@@ -253,26 +280,52 @@ __device__ void find_boundary(const float* __restrict__ z, int V, const RowScale
     const uint32_t n_bin = sm.cnt0[b0];
     if (n_bin <= (uint32_t)kListCap) {
         // ---- level 1: gather the bin's tokens, sort them, scan in order
-        for (int i0 = 0; i0 < V; i0 += kRowUnroll * blockDim.x) {   // the same trip count in every warp
-            float v[kRowUnroll];
-#pragma unroll
-            for (int u = 0; u < kRowUnroll; ++u) {
-                const int i = i0 + u * blockDim.x + tid;
-                v[u] = i < V ? __ldg(z + i) : 0.f;
+        // append one token (warp-collective: every lane calls it the same number of times)
+        auto append = [&](int i, float zi, bool valid) {
+            const bool in = valid && level0_bin(zi, rs) == b0;
+            const unsigned ballot = __ballot_sync(0xffffffffu, in);
+            if (ballot) {
+                unsigned int base = 0;
+                if (lane == __ffs(ballot) - 1) base = atomicAdd(&sm.n_list, (unsigned int)__popc(ballot));
+                base = __shfl_sync(0xffffffffu, base, __ffs(ballot) - 1);
+                if (in) {
+                    const unsigned int at = base + __popc(ballot & ((1u << lane) - 1u));
+                    sm.u.list[at] = ((unsigned long long)order_key(zi) << 32) | (unsigned long long)(~(uint32_t)i);
+                }
             }
+        };
+        if ((V & 3) == 0 && ((uintptr_t)z & 15) == 0) {
+            const float4* z4 = reinterpret_cast<const float4*>(z);
+            const int V4 = V >> 2;
+            for (int i0 = 0; i0 < V4; i0 += kRowUnroll * blockDim.x) {   // the same trip count in every warp
+                float4 v[kRowUnroll];
 #pragma unroll
-            for (int u = 0; u < kRowUnroll; ++u) {
-                const int i = i0 + u * blockDim.x + tid;
-                const bool in = i < V && level0_bin(v[u], rs) == b0;
-                const unsigned ballot = __ballot_sync(0xffffffffu, in);
-                if (ballot) {
-                    unsigned int base = 0;
-                    if (lane == __ffs(ballot) - 1) base = atomicAdd(&sm.n_list, (unsigned int)__popc(ballot));
-                    base = __shfl_sync(0xffffffffu, base, __ffs(ballot) - 1);
-                    if (in) {
-                        const unsigned int at = base + __popc(ballot & ((1u << lane) - 1u));
-                        sm.u.list[at] = ((unsigned long long)order_key(v[u]) << 32) | (unsigned long long)(~(uint32_t)i);
-                    }
+                for (int u = 0; u < kRowUnroll; ++u) {
+                    const int i = i0 + u * blockDim.x + tid;
+                    v[u] = i < V4 ? __ldg(z4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kRowUnroll; ++u) {
+                    const int i = i0 + u * blockDim.x + tid;
+                    const bool valid = i < V4;
+                    append(4 * i, v[u].x, valid);
+                    append(4 * i + 1, v[u].y, valid);
+                    append(4 * i + 2, v[u].z, valid);
+                    append(4 * i + 3, v[u].w, valid);
+                }
+            }
+        } else {
+            for (int i0 = 0; i0 < V; i0 += kRowUnroll * blockDim.x) {   // the same trip count in every warp
+                float v[kRowUnroll];
+#pragma unroll
+                for (int u = 0; u < kRowUnroll; ++u) {
+                    const int i = i0 + u * blockDim.x + tid;
+                    v[u] = i < V ? __ldg(z + i) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < kRowUnroll; ++u) {
+                    const int i = i0 + u * blockDim.x + tid;
+                    append(i, v[u], i < V);
                 }
             }
         }

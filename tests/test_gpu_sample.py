@@ -98,19 +98,22 @@ def test_sample_matches_oracle(case, ties):
     assert exact >= B - near
 
 
-def test_sample_small_vocab_and_argument_checks():
+@pytest.mark.parametrize("vocab", [1000, 1001], ids=["16B-rows", "unaligned-rows"])
+def test_sample_small_vocab_and_argument_checks(vocab):
+    """A small vocabulary, with rows a multiple of 16 bytes long (vector loads) and not."""
     import dense_decoder_block_gb300 as ddb
-    z, u = _logits(3, 1000, 7)
-    got = _gpu(z, u, 0.9, 20, 0.8)
-    zn = z.double().numpy()
-    for b in range(3):
-        _, ok = _allowed(zn[b], 0.9, 20, 0.8, float(u[b]))
-        assert int(got[b]) in ok
+    z, u = _logits(3, vocab, 7)
+    for temperature, top_k, top_p in ((0.9, 20, 0.8), (1.0, 0, 1.0), (0.5, 0, 0.7)):
+        got = _gpu(z, u, temperature, top_k, top_p)
+        zn = z.double().numpy()
+        for b in range(3):
+            _, ok = _allowed(zn[b], temperature, top_k, top_p, float(u[b]))
+            assert int(got[b]) in ok
     dev = torch.device("cuda:0")
     ids = torch.empty(3, dtype=torch.int32, device=dev)
     for bad in ((-1.0, 0, 1.0), (1.0, -1, 1.0), (1.0, 0, 0.0), (1.0, 0, 1.5)):
         with pytest.raises(ddb.LlamaError):
-            ddb.llama_sample(z.to(dev), 3, 1000, bad[0], bad[1], bad[2], u.to(dev), ids)
+            ddb.llama_sample(z.to(dev), 3, vocab, bad[0], bad[1], bad[2], u.to(dev), ids)
 
 
 def test_sample_uniform_sweep_realises_the_distribution():
