@@ -254,7 +254,7 @@ int run_block(llama_block b, const void* x, int B, int T, const llama_kv_cache* 
         // The token-tiled (prefill) QKV stores q and k unrotated and a vectorised
         // kernel rotates them in place: the per-column table loads of a fused RoPE
         // kept that projection's epilogue warps behind its MMAs.
-        eq.rope_later = pick_gemm_path(pq, PATH_AUTO) == PATH_TOKEN_TILED;
+        eq.rope_later = pick_gemm_path(pq, PATH_AUTO) == PATH_TOKEN_TILED && !gemm_tt_split(pq, PATH_AUTO);
         LLAMA_TRY(launch_gemm(pq, eq, PATH_AUTO, w.gemm_partial, s), "qkv");
         if (eq.rope_later)
             LLAMA_TRY(launch_rope_inplace(w.q, kv->k, M, T, d.n_heads, d.n_kv_heads, kv->max_seq, start_pos, pos_dev,

@@ -122,9 +122,21 @@ cudaError_t kernel_setup_once(const void* kern, cudaError_t (*setup)(const void*
     return e;
 }
 
+bool gemm_tt_split(const GemmProblem& p, int path) {
+    // A token-tiled projection whose 256-token tiles would keep under 70% of the SMs
+    // busy runs its K-segments on separate CTAs (split mode of gemm_tt.cuh) and
+    // leaves them to the reduction kernels, as the weight-streaming schedule does.
+    // (An M = 128 MMA takes as long at N = 128 as at N = 256, so narrower token
+    // tiles would not add throughput, only tiles.)
+    if (pick_gemm_path(p, path) != PATH_TOKEN_TILED || p.dual || n_segments(p) <= 1) return false;
+    const long tiles = (long)(p.F / kTileF) * ((p.M + 255) / 256);
+    return 10 * tiles < 7L * device_sm_count();
+}
+
 size_t gemm_partial_bytes(const GemmProblem& p, int path) {
-    if (pick_gemm_path(p, path) != PATH_WEIGHT_STREAM) return 0;
     const int segs = n_segments(p);
+    if (gemm_tt_split(p, path)) return (size_t)segs * p.M * p.F * sizeof(float);
+    if (pick_gemm_path(p, path) != PATH_WEIGHT_STREAM) return 0;
     if (segs <= 1) return 0;
     const int bn = p.M <= 16 ? 16 : 32;   // the weight-streaming tile width for this M
     return (size_t)segs * bn * (p.dual ? 2 : 1) * p.F * sizeof(float);
@@ -133,7 +145,7 @@ size_t gemm_partial_bytes(const GemmProblem& p, int path) {
 int gemm_num_segments(const GemmProblem& p) { return n_segments(p); }
 
 bool gemm_needs_reduce(const GemmProblem& p, int path) {
-    return pick_gemm_path(p, path) == PATH_WEIGHT_STREAM && n_segments(p) > 1;
+    return (pick_gemm_path(p, path) == PATH_WEIGHT_STREAM && n_segments(p) > 1) || gemm_tt_split(p, path);
 }
 
 // Instantiated in gemm_token_tiled.cu / gemm_weight_stream.cu
@@ -166,6 +178,8 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float*
         if (ka.n_segs > 1 && !partial) return cudaErrorInvalidValue;
         return launch_weight_stream(p, ka, a0, a1, a2, p.x, s);
     }
+    ka.split = gemm_tt_split(p, path) ? 1 : 0;
+    if (ka.split && !partial) return cudaErrorInvalidValue;
     return launch_token_tiled(p, ka, a0, a1, a2, p.x, s);
 }
 

@@ -39,8 +39,9 @@ struct GemmKArgs {
     int n_segs, seg_kb;
     int q_tiles, k_tiles;     // QKV: feature tiles per map (wq, wk); the rest are wv
     int group;                // token-tiled: token blocks taken per feature tile in a row
+    int split;                // token-tiled: one (tile, K-segment) unit per CTA pass, fp32 results out
     GemmEpi e;
-    float* partial;   // weight-streaming: fp32 segment results [seg][acc][M][F]
+    float* partial;   // weight-streaming and split token-tiled: fp32 segment results [seg][acc][M][F]
 };
 
 // ------------------------------------------------------------------ epilogue store of one column

@@ -22,7 +22,7 @@ static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUten
     CUtensorMap mb;
     if (!make_tmap_bf16(&mb, x, (uint64_t)p.M, (uint64_t)p.K, BN, nullptr)) return cudaErrorInvalidValue;
     const int n_blocks = (p.M + BN - 1) / BN;
-    const int tiles = (p.F / kTileF) * n_blocks;
+    const int tiles = (p.F / kTileF) * n_blocks * (ka.split ? ka.n_segs : 1);
     const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
     // token blocks per group: about 32 MB of activations (a quarter of L2), at least one
     GemmKArgs k = ka;
@@ -66,6 +66,7 @@ cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const 
         if (ka.e.kind != EPI_SWIGLU) return cudaErrorInvalidValue;
         return run_tt<128, true, EPI_SWIGLU>(p, ka, a0, a1, a2, x, s);
     }
+    if (ka.split) return dispatch_tt<256>(p, ka, a0, a1, a2, x, s);
     return tt_width(p) == 128 ? dispatch_tt<128>(p, ka, a0, a1, a2, x, s) : dispatch_tt<256>(p, ka, a0, a1, a2, x, s);
 }
 

@@ -17,6 +17,16 @@
 // issuer, warps 2-3 idle; warps 4..19 = epilogue, warp w reading TMEM lane
 // quarter w % 4 and column quarter (w - 4) / 4.  Warpgroup 0 gives registers
 // to the epilogue warpgroups, whose running sums take 64 per thread.
+//
+// Split mode (few tokens, a.split): the work units are (feature tile, K-segment,
+// token block) instead of whole tiles, so that more SMs share a projection whose
+// tiles would not fill them; each unit's segment result goes out in fp32, laid
+// out [segment][token][feature] as the weight-streaming kernel lays it, and the
+// same reduction kernels add the segments in ascending order and apply the
+// epilogue.  Per output the operations are the same (one MMA chain per segment,
+// ascending fp32 sum, the same epilogue functions).  Units of one feature tile
+// and segment are consecutive, so the CTAs that share a weight tile read it in
+// step.
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -68,6 +78,8 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
     const int m_tiles = a.F / kTileF;
     const int n_blocks = (a.M + BN - 1) / BN;
     const int n_tiles = m_tiles * n_blocks;
+    const bool split = a.split != 0;
+    const int n_work = split ? n_tiles * a.n_segs : n_tiles;   // units per pass of the CTAs
     int* err = a.e.err;
 
     // tile t -> (feature tile m, token block n), groups of a.group token blocks
@@ -78,6 +90,22 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
         const int gn = min(G, n_blocks - grp * G);
         m = rem / gn;
         n = grp * G + (rem - m * gn);
+    };
+    // work item w -> (feature tile m, token block n, k-blocks [kb0, kb1), segment)
+    auto work_of = [&](int w, int& m, int& n, int& kb0, int& kb1, int& seg) {
+        if (split) {
+            m = w / (a.n_segs * n_blocks);
+            const int rem = w - m * a.n_segs * n_blocks;
+            seg = rem / n_blocks;
+            n = rem - seg * n_blocks;
+            kb0 = seg * a.seg_kb;
+            kb1 = min(kb0 + a.seg_kb, total_kb);
+        } else {
+            tile_mn(w, m, n);
+            seg = 0;
+            kb0 = 0;
+            kb1 = total_kb;
+        }
     };
 
     if (threadIdx.x == 0) {
@@ -106,23 +134,23 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                 uint32_t phase = 0;
                 int it = 0;
                 bool waited = false, ok = true;
-                // Token block of this CTA's i-th k-block load (i < total k-blocks of the CTA).
-                auto load_b_of = [&](int i) {
-                    int m, n;
-                    tile_mn(blockIdx.x + (i / total_kb) * gridDim.x, m, n);
-                    ptx::tma_load_2d(smem + (i % C::STAGES) * C::STAGE_BYTES + NACC * kABytes, &mB,
-                                     &full[i % C::STAGES], (i % total_kb) * kBlockK, n * BN);
+                // (k-block, token block) of the first STAGES loads: their activations are
+                // issued once the grid dependency resolves
+                int pre_kb[C::STAGES], pre_n[C::STAGES];
+                auto load_b_of = [&](int j) {
+                    ptx::tma_load_2d(smem + j * C::STAGE_BYTES + NACC * kABytes, &mB, &full[j], pre_kb[j] * kBlockK,
+                                     pre_n[j] * BN);
                 };
-                for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                    int m, n;
-                    tile_mn(t, m, n);
+                for (int t = blockIdx.x; t < n_work && ok; t += gridDim.x) {
+                    int m, n, kb0, kb1, seg;
+                    work_of(t, m, n, kb0, kb1, seg);
                     const CUtensorMap* mapA = &mA0;
                     int arow = m * kTileF;
                     if constexpr (EPI == EPI_QKV) {
                         if (m >= a.q_tiles + a.k_tiles) { mapA = &mA2; arow = (m - a.q_tiles - a.k_tiles) * kTileF; }
                         else if (m >= a.q_tiles) { mapA = &mA1; arow = (m - a.q_tiles) * kTileF; }
                     }
-                    for (int kb = 0; kb < total_kb; ++kb, ++it) {
+                    for (int kb = kb0; kb < kb1; ++kb, ++it) {
                         uint8_t* dst = smem + stage * C::STAGE_BYTES;
                         if (it >= C::STAGES && !ptx::mbar_wait(&empty[stage], phase ^ 1, err)) { ok = false; break; }
                         ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
@@ -130,13 +158,17 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                         if (DUAL) ptx::tma_load_2d(dst + kABytes, &mA1, &full[stage], kb * kBlockK, arow);
                         if (waited) {
                             ptx::tma_load_2d(dst + NACC * kABytes, &mB, &full[stage], kb * kBlockK, n * BN);
-                        } else if (it == C::STAGES - 1) {
-                            // The weights do not depend on the previous kernel: the first stages
-                            // of them are in flight before waiting for it; then the activations.
-                            ptx::griddep_wait();
-                            ptx::griddep_launch_dependents();
-                            for (int j = 0; j <= it; ++j) load_b_of(j);
-                            waited = true;
+                        } else {
+                            pre_kb[it] = kb;
+                            pre_n[it] = n;
+                            if (it == C::STAGES - 1) {
+                                // The weights do not depend on the previous kernel: the first stages
+                                // of them are in flight before waiting for it; then the activations.
+                                ptx::griddep_wait();
+                                ptx::griddep_launch_dependents();
+                                for (int j = 0; j <= it; ++j) load_b_of(j);
+                                waited = true;
+                            }
                         }
                         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
                     }
@@ -156,8 +188,11 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                 int stage = 0, use = 0;
                 uint32_t phase = 0;
                 bool ok = true;
-                for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                    for (int seg = 0; seg < a.n_segs && ok; ++seg, ++use) {
+                for (int t = blockIdx.x; t < n_work && ok; t += gridDim.x) {
+                    int wm, wn, wkb0, wkb1, wseg;
+                    work_of(t, wm, wn, wkb0, wkb1, wseg);
+                    const int seg_first = split ? wseg : 0, seg_end = split ? wseg + 1 : a.n_segs;
+                    for (int seg = seg_first; seg < seg_end && ok; ++seg, ++use) {
                         const int buf = use & 1;
                         if (!ptx::mbar_wait(&tempty[buf], ((use >> 1) & 1) ^ 1, err)) { ok = false; break; }
                         ptx::tc_fence_after();
@@ -198,16 +233,17 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         int use = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-            int m, n;
-            tile_mn(t, m, n);
+        for (int t = blockIdx.x; t < n_work; t += gridDim.x) {
+            int m, n, wkb0, wkb1, wseg;
+            work_of(t, m, n, wkb0, wkb1, wseg);
             // -0 + s == s for every fp32 s, so the sum starts exactly at segment 0
             float acc[NACC][CPT];
 #pragma unroll
             for (int ac = 0; ac < NACC; ++ac)
 #pragma unroll
                 for (int j = 0; j < CPT; ++j) acc[ac][j] = -0.0f;
-            for (int seg = 0; seg < a.n_segs; ++seg, ++use) {
+            const int seg_first = split ? wseg : 0, seg_end = split ? wseg + 1 : a.n_segs;
+            for (int seg = seg_first; seg < seg_end; ++seg, ++use) {
                 const int buf = use & 1;
                 if (ok) ok = ptx::mbar_wait(&tfull[buf], (use >> 1) & 1, err);
                 ptx::tc_fence_after();
@@ -227,7 +263,17 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
             }
-            if (ok) {
+            if (ok && split) {
+                // the unit's fp32 segment result, [seg][token][feature] (the reduction adds them)
+                if constexpr (!DUAL) {
+                    const int f = m * kTileF + row;
+                    const int n0 = n * BN + cg * CPT;
+                    float* dst = a.partial + ((size_t)wseg * a.M + n0) * a.F + f;
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j)
+                        if (n0 + j < a.M) dst[(size_t)j * a.F] = acc[0][j];
+                }
+            } else if (ok) {
                 if constexpr (DUAL) {
                     // lane = token n * BN + row, columns = features m * 128 + cg * CPT + j
                     const int tok = n * BN + row;

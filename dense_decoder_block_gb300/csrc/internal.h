@@ -53,8 +53,12 @@ size_t gemm_partial_bytes(const GemmProblem& p, int path);
 int pick_gemm_path(const GemmProblem& p, int path);
 int gemm_num_segments(const GemmProblem& p);
 // True when the projection leaves segment results for a reduction kernel
-// (weight-streaming schedule with more than one K-segment).
+// (weight-streaming schedule with more than one K-segment, or the token-tiled
+// schedule in split mode).
 bool gemm_needs_reduce(const GemmProblem& p, int path);
+// True when a token-tiled projection runs its K-segments on separate CTAs (few
+// tokens: its whole tiles would leave most SMs idle).
+bool gemm_tt_split(const GemmProblem& p, int path);
 // K-segment length (in 64-element k-blocks) for a projection of n_tiles feature
 // tiles and total_kb k-blocks: the fewest segments whose units fill 70-100% of
 // the n_sm SMs in one wave; failing that, the one that minimises the
