@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                 bool waited = false, ok = true;
                 // (k-block, token block) of the first STAGES loads: their activations are
                 // issued once the grid dependency resolves
-                int pre_kb[C::STAGES], pre_n[C::STAGES];
+                int pre_kb[C::STAGES] = {}, pre_n[C::STAGES] = {};
                 auto load_b_of = [&](int j) {
                     ptx::tma_load_2d(smem + j * C::STAGE_BYTES + NACC * kABytes, &mB, &full[j], pre_kb[j] * kBlockK,
                                      pre_n[j] * BN);
