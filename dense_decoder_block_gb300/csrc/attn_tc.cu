@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Pipelined prefill attention.  Same unit (one 128-row query tile of a KV group,
 // its chunks in ascending order) and the same arithmetic as above, split over
 // roles that overlap:
-//   warp 0       TMA: the Q tile once, then K chunks through a three-stage ring
-//   warp 2       TMA: V chunks through a two-stage ring (K(i+3) loads once S(i)
+//   warp 0       TMA: the Q tile once, then K chunks through a two-stage ring
+//   warp 2       TMA: V chunks through a two-stage ring (K(i+2) loads once S(i)
 //                has read K(i); V(i+2) once PV(i) has read V(i))
 //   warp 1       TMEM owner + MMA: PV(i) into O_c[i % 2] with P read from
 //                TMEM, then S(i+2) = Q K^T into the S buffer that chunk i used
@@ -383,8 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //                TMEM lane quarter, exchanging the row max and two quarter sums
 //                through shared memory; P (bf16 pairs) overwrites the first 64
 //                columns of the S row once both halves hold their scores, the
-//                row's (m, l) goes to shared memory for the fold, so the next S
-//                into that buffer waits for nothing but its K chunk.
+//                row's (m, l) goes to columns 64, 65.  (One warpgroup per chunk
+//                on alternate chunks, thread = row, gave the same chunk time: it
+//                is set by the chain softmax -> PV -> fold -> next S, not by one
+//                warp's softmax.)
 //   warps 12-15  fold of every chunk into the running (O, M, L), thread = row,
 //                with the row's O in registers; then o = O * (1 / L)
 // Warp 3 only keeps the roles aligned to warpgroups.  A chunk that is wholly
@@ -399,25 +401,16 @@ constexpr int kPfRegsSoftmax = 112;
 constexpr int kPfRegsFold = 232;
 constexpr int kPfRegsNeeded = 128 * kPfRegsCtrl + 256 * kPfRegsSoftmax + 128 * kPfRegsFold;
 static_assert(kPfRegsNeeded <= 128 * kPfThreads, "register split exceeds the launch allocation");
-// K and V stream through rings of their own.  K is three chunks deep: a chunk of K
-// is requested when S two chunks back has read its slot, and under load its copy
-// takes about as long as two chunks of compute, so a two-deep ring left the next
-// S waiting for its K (measured per chunk in one CTA's timeline at T = 8192).
-constexpr int kPfStagesK = 3;
-constexpr int kPfStagesV = 2;
-constexpr int PF_OFF_Q = 0;                                    // Q: 2 sub-tiles
-constexpr int PF_OFF_K = 2 * kSub;                             // [stage] K: 2 sub-tiles
-constexpr int PF_OFF_V = PF_OFF_K + kPfStagesK * 2 * kSub;     // [stage] V: 2 sub-tiles
-constexpr int PF_OFF_BAR = PF_OFF_V + kPfStagesV * 2 * kSub;
+constexpr int PF_OFF_Q = 0;                          // Q: 2 sub-tiles
+constexpr int PF_OFF_K = 2 * kSub;                   // [stage] K: 2 sub-tiles
+constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
+constexpr int PF_OFF_BAR = PF_OFF_V + 4 * kSub;
 constexpr int PF_OFF_XCH = PF_OFF_BAR + 256;         // softmax halves' exchange: 4 x 128 floats
-constexpr int PF_OFF_ML = PF_OFF_XCH + 2048;         // [chunk % 4][row] (m, l) of each row, for the fold
-constexpr int PF_SMEM_BYTES = PF_OFF_ML + 4 * 128 * 8 + 1024;
+constexpr int PF_SMEM_BYTES = PF_OFF_XCH + 2048 + 1024;
 constexpr int PF_TM_S = 0, PF_TM_OC = 256;   // S[parity] at 0 / 128, O_c[parity] at 256 / 384
-// In S[parity], the softmax leaves P (bf16 pairs) in columns 0..63; the row's
-// (m, l) goes to shared memory, four chunks deep: the fold of chunk i has read it
-// before the softmax of chunk i + 4 can start (S(i + 4) is issued after PV(i + 2),
-// which waits for the fold to release O_c of chunk i), so S(i + 2) needs nothing
-// from the fold and the MMA issues it right behind PV(i).
+// In S[parity], the softmax leaves P (bf16 pairs) in columns 0..63 and the row's
+// (m, l) in columns 64, 65.
+constexpr int PF_TM_ML = 64;
 static_assert(PF_SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // Barrier of `n` threads (whole warps) on hardware barrier `id` (1..15; 0 is
@@ -435,10 +428,10 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 // ascending key order -- half 0 holds L0, L1, half 1 passes L2, L3 over.  Block c
 // (keys 16c .. 16c+15) of P, packed as bf16 pairs, goes to columns 8c .. 8c+7 of
 // the S row once both halves hold their scores in registers; half 0 writes the
-// row's (m, l) to *ml.  `xch` is 4 x 128 floats of shared memory; `bar` the
-// barrier id of this lane quarter.
+// row's (m, l) to the ML columns.  `xch` is 4 x 128 floats of shared memory; `bar`
+// the barrier id of this lane quarter.
 __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int row, int jmax, float scale_log2,
-                                                  float* xch, int bar, float2* ml, float& m_out) {
+                                                  float* xch, int bar, float& m_out) {
     float v[64];
     ptx::tmem_ld<32>(s_taddr + h * 64, v);
     ptx::tmem_ld<32>(s_taddr + h * 64 + 32, v + 32);
@@ -487,7 +480,7 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
     named_bar_sync(bar, 64);   // L2, L3 written; the maxima read
     if (h == 0) {
         const float l = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), xch[256 + row]), xch[384 + row]);
-        *ml = make_float2(m, l);
+        ptx::tmem_st2(s_taddr + PF_TM_ML, m, l);
     }
     ptx::tmem_wait_st();
     m_out = m;
@@ -500,16 +493,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + PF_OFF_BAR);
     uint64_t* q_full = bars + 0;
-    uint64_t* k_full = bars + 1;                           // [K stages] TMA -> MMA
-    uint64_t* k_empty = k_full + kPfStagesK;               // [K stages] MMA (after S) -> TMA
-    uint64_t* v_full = k_empty + kPfStagesK;               // [V stages] TMA -> MMA (and the softmax, before it zeroes rows)
-    uint64_t* v_empty = v_full + kPfStagesV;               // [V stages] MMA (after PV) -> TMA
-    uint64_t* s_full = v_empty + kPfStagesV;               // [2] MMA (after S) -> softmax
-    uint64_t* p_full = s_full + 2;                         // [2] softmax (P, m, l written) -> MMA, fold
-    uint64_t* oc_full = p_full + 2;                        // [2] MMA (after PV) -> fold
-    uint64_t* oc_free = oc_full + 2;                       // [2] fold (O_c read) -> MMA
-    uint32_t* tmem_holder = (uint32_t*)(oc_free + 2);
-    static_assert(1 + 2 * kPfStagesK + 2 * kPfStagesV + 8 + 1 <= 32, "barriers fit their 256 bytes");
+    uint64_t* k_full = bars + 1;     // [2] TMA -> MMA
+    uint64_t* k_empty = bars + 3;    // [2] MMA (after S) -> TMA
+    uint64_t* v_full = bars + 5;     // [2] TMA -> MMA (and the softmax, before it zeroes rows)
+    uint64_t* v_empty = bars + 7;    // [2] MMA (after PV) -> TMA
+    uint64_t* s_full = bars + 9;     // [2] MMA (after S) -> softmax
+    uint64_t* p_full = bars + 11;    // [2] softmax (P, m, l written) -> MMA, fold
+    uint64_t* s_free = bars + 13;    // [2] fold (m, l read) -> MMA
+    uint64_t* oc_full = bars + 15;   // [2] MMA (after PV) -> fold
+    uint64_t* oc_free = bars + 17;   // [2] fold (O_c read) -> MMA
+    uint32_t* tmem_holder = (uint32_t*)(bars + 19);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
@@ -532,18 +525,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(q_full, 1);
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&s_full[i], 1);
-            ptx::mbar_init(&p_full[i], 8);
-            ptx::mbar_init(&oc_full[i], 1);
-            ptx::mbar_init(&oc_free[i], 4);
-        }
-        for (int i = 0; i < kPfStagesK; ++i) {
             ptx::mbar_init(&k_full[i], 1);
             ptx::mbar_init(&k_empty[i], 1);
-        }
-        for (int i = 0; i < kPfStagesV; ++i) {
             ptx::mbar_init(&v_full[i], 1);
             ptx::mbar_init(&v_empty[i], 1);
+            ptx::mbar_init(&s_full[i], 1);
+            ptx::mbar_init(&p_full[i], 8);
+            ptx::mbar_init(&s_free[i], 4);
+            ptx::mbar_init(&oc_full[i], 1);
+            ptx::mbar_init(&oc_free[i], 4);
         }
         ptx::fence_mbar_init();
     }
@@ -582,11 +572,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                             : "memory");
                 }
                 const int head_row0 = (b * a.n_kv_heads + g) * a.kv_seq;
-                const int n_st = is_k ? kPfStagesK : kPfStagesV;
                 int issued = 0;
                 for (int i = 0; i < n_iter; ++i, ++issued) {
-                    const int st = i % n_st;
-                    if (i >= n_st && !ptx::mbar_wait(&empty[st], ((i / n_st) & 1) ^ 1, err)) break;
+                    const int st = i & 1;
+                    if (i >= 2 && !ptx::mbar_wait(&empty[st], ((i >> 1) & 1) ^ 1, err)) break;
                     uint8_t* dst = ring + st * 2 * kSub;
                     const int row = head_row0 + i * kAttnChunk;
                     ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
@@ -596,22 +585,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 // no copy may still be landing when the CTA exits (it has landed already
                 // unless a wait above gave up)
                 if (is_k) ptx::mbar_wait_drain(q_full, 0);
-                for (int i = max(0, issued - n_st); i < issued; ++i)
-                    ptx::mbar_wait_drain(&full[i % n_st], (i / n_st) & 1);
+                for (int i = max(0, issued - 2); i < issued; ++i) ptx::mbar_wait_drain(&full[i & 1], (i >> 1) & 1);
             }
         } else if (warp == 1) {
             // ------------------------------------------------------------------ MMA issuer
             if (lane == 0) {
                 const uint32_t q_addr = ptx::smem_u32(sm + PF_OFF_Q);
                 auto issue_s = [&](int i) -> bool {
-                    const int k = i & 1;            // S buffer in TMEM
-                    const int ks_ = i % kPfStagesK;  // K slot
-                    // S(i) overwrites the S buffer of chunk i - 2: PV(i - 2), which read its P,
-                    // was issued before and the MMAs run in issue order; its (m, l) is in
-                    // shared memory
-                    if (!ptx::mbar_wait(&k_full[ks_], (i / kPfStagesK) & 1, err)) return false;
+                    const int k = i & 1;
+                    if (!ptx::mbar_wait(&k_full[k], (i >> 1) & 1, err)) return false;
+                    if (i >= 2 && !ptx::mbar_wait(&s_free[k], ((i >> 1) & 1) ^ 1, err)) return false;
                     ptx::tc_fence_after();
-                    const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + ks_ * 2 * kSub);
+                    const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
@@ -619,7 +604,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                        ptx::sw128_kmajor_desc(k_addr + off), IDESC_S, ks > 0 ? 1u : 0u);
                     }
                     ptx::umma_commit(&s_full[k]);
-                    ptx::umma_commit(&k_empty[ks_]);
+                    ptx::umma_commit(&k_empty[k]);
                     return true;
                 };
                 bool ok = ptx::mbar_wait(q_full, 0, err);
@@ -629,16 +614,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     const int k = i & 1;
                     if (!ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err)) break;
                     if (i >= 2 && !ptx::mbar_wait(&oc_free[k], ((i >> 1) & 1) ^ 1, err)) break;
-                    const int vs = i % kPfStagesV;
-                    if (!ptx::mbar_wait(&v_full[vs], (i / kPfStagesV) & 1, err)) break;
+                    if (!ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err)) break;
                     ptx::tc_fence_after();
-                    const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + vs * 2 * kSub);
+                    const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + k * 2 * kSub);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)   // P of keys 16ks.. in TMEM columns 8ks..
                         umma_bf16_ts(tmem + PF_TM_OC + k * 128, tmem + PF_TM_S + k * 128 + ks * 8,
                                      ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
                     ptx::umma_commit(&oc_full[k]);
-                    ptx::umma_commit(&v_empty[vs]);
+                    ptx::umma_commit(&v_empty[k]);
                     if (i + 2 < n_iter) ok = issue_s(i + 2);
                 }
             }
@@ -663,26 +647,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
             float m;
             // both halves reach the two barriers inside on every chunk, whatever `ok` says
-            float2* ml = reinterpret_cast<float2*>(sm + PF_OFF_ML) + (i & 3) * 128 + row;
-            softmax_half_tmem(tmem + lane_addr + PF_TM_S + k * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, ml,
-                              m);
+            softmax_half_tmem(tmem + lane_addr + PF_TM_S + k * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, m);
             if (h == 0) {
                 // value rows past the last visible key of this tile are zeroed (they may hold
                 // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
                 // the chunk's V has landed
-                const int vs = i % kPfStagesV;
                 if (i * kAttnChunk + kAttnChunk - 1 > kv_last && ok)
-                    ok = ptx::mbar_wait(&v_full[vs], (i / kPfStagesV) & 1, err);
+                    ok = ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err);
                 if (i * kAttnChunk + row > kv_last) {
-                    uint8_t* vrow = sm + PF_OFF_V + vs * 2 * kSub + row * 128;
+                    uint8_t* vrow = sm + PF_OFF_V + k * 2 * kSub + row * 128;
 #pragma unroll
                     for (int c16 = 0; c16 < 8; ++c16) {
                         *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(vrow + kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
                     }
                 }
-                // the zeroed rows (generic-proxy writes) must be visible to the PV MMA
-                if (i * kAttnChunk + kAttnChunk - 1 > kv_last) ptx::fence_proxy_async_smem();
+                ptx::fence_proxy_async_smem();
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -703,8 +683,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int i = 0; i < n_iter; ++i) {
             const int k = i & 1;
             if (ok) ok = ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err);
-            const float2 ml = reinterpret_cast<const float2*>(sm + PF_OFF_ML)[(i & 3) * 128 + row];
-            const float m = ml.x, l = ml.y;
+            ptx::tc_fence_after();
+            float ml[2];
+            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + k * 128 + PF_TM_ML, ml);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&s_free[k]);
+            const float m = ml[0], l = ml[1];
             if (ok) ok = ptx::mbar_wait(&oc_full[k], (i >> 1) & 1, err);
             ptx::tc_fence_after();
             // Per row: skip a chunk with no visible key, start from the first one, fold the
