@@ -125,10 +125,14 @@ cudaError_t kernel_setup_once(const void* kern, cudaError_t (*setup)(const void*
 bool gemm_tt_split(const GemmProblem& p, int path) {
     // A token-tiled projection whose 256-token tiles would keep under 70% of the SMs
     // busy runs its K-segments on separate CTAs (split mode of gemm_tt.cuh) and
-    // leaves them to the reduction kernels, as the weight-streaming schedule does.
-    // (An M = 128 MMA takes as long at N = 128 as at N = 256, so narrower token
-    // tiles would not add throughput, only tiles.)
+    // leaves them to the reduction kernels, as the weight-streaming schedule does --
+    // when K is at least twice F, so that the MMA time saved outweighs writing and
+    // reading the fp32 segment results (8B prefill at 512 tokens: the down projection
+    // 72 -> 61 us with its reduction; QKV and O, K <= F, measured slower split).
+    // An M = 128 MMA takes as long at N = 128 as at N = 256 (a microbenchmark of the
+    // kernels' MMA shapes), so narrower token tiles would add tiles, not throughput.
     if (pick_gemm_path(p, path) != PATH_TOKEN_TILED || p.dual || n_segments(p) <= 1) return false;
+    if (p.K < 2 * p.F) return false;
     const long tiles = (long)(p.F / kTileF) * ((p.M + 255) / 256);
     return 10 * tiles < 7L * device_sm_count();
 }

@@ -78,9 +78,9 @@ def _prefill_case(dims, wts, wts64, T, B=1):
     y = run_prefill(blk, ddb, inp.x.to(dev), kc, vc)
     torch.cuda.synchronize()
     assert blk.poll_error() == 0
-    # 8 when the token-tiled projections carry their epilogues; with few tokens a projection
-    # runs its K-segments on separate CTAs and a reduction applies the epilogue (QKV's takes
-    # the RoPE kernel's place, O's the RMSNorm_2 kernel's, down's is one more)
+    # 8 when the token-tiled projections carry their epilogues; with few tokens the down
+    # projection runs its K-segments on separate CTAs and a reduction kernel applies its
+    # epilogue (one more)
     assert blk.launch_count() == (9 if T < 1024 else 8)
     rows = _sample_rows(T)
     kc64 = np.zeros((B, dims.n_kv_heads, max_seq, dims.head_dim))
