@@ -695,6 +695,76 @@ def extra_70b(ddb, device, hbm, bf16_peak, peak_kind):
     return res
 
 
+def run_survey(args, rank, world, device):
+    """One call of each kernel family the default line does not time on its own, each
+    after a warm-up call, for a per-kernel launch list under a profiler (every input
+    is a few GB at most): the 70B-shaped decode block (batch 16, 8192 cached
+    positions: two-segment gate/up, its reduction, 8 query heads per KV head), the
+    LM head with the greedy choice and the sampling head (batch 32, 128,256
+    logits), the embedding gather, decode with 16 query heads per KV head (the
+    wide-group attention), the fp32 tiny block (CUDA-core kernels) and the 8B
+    prefill at 512 tokens (split down projection and its reduction)."""
+    import dense_decoder_block_gb300 as ddb
+    ddb.lib()
+    stream = torch.cuda.current_stream(device)
+    calls = {}
+
+    def timed(name, fn, launches=None):
+        fn()
+        torch.cuda.synchronize(device)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        calls[name] = {"us": round(a.elapsed_time(b) * 1e3, 2)}
+        if launches is not None:
+            calls[name]["kernels"] = launches()
+
+    def block_case(name, dims, B, T, P, dtype=torch.bfloat16, std=0.02):
+        wts = workloads.make_weights(dims, dtype=dtype, weight_std=std)
+        inp = workloads.make_block_inputs(dims, B, T, dtype=dtype, cache_len=P, max_seq=P + T + 8, weights=wts)
+        blk = ddb.LlamaBlock(dims, {k: v.to(device) for k, v in wts[0].items()},
+                             {k: v.to(device) for k, v in wts[1].items()}, P + T + 8)
+        kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+        x = inp.x.to(device)
+        y = torch.empty_like(x)
+        ws = blk.workspace(B, T)
+        if T == 1:
+            timed(name, lambda: blk.decode(x, kv, P, y, ws), blk.launch_count)
+        else:
+            timed(name, lambda: blk.prefill_at(x, kv, P, y, ws), blk.launch_count)
+        assert blk.poll_error() == 0
+
+    cfg70 = workloads.BLOCK_70B
+    block_case("decode_70b_b16_pos8192", cfg70["dims"], cfg70["decode_batch"], 1, cfg70["cache_len"],
+               std=cfg70["weight_std"])
+    block_case("decode_wide_group_16q_per_kv_b4_pos1000",
+               workloads.BlockDims(d_model=2048, n_heads=16, n_kv_heads=1, head_dim=128, d_ff=4096), 4, 1, 1000)
+    block_case("decode_tiny_fp32_pos16", workloads.TINY, 1, 1, 16, dtype=torch.float32)
+    block_case("prefill_8b_t512", workloads.LLAMA3_8B, 1, 512, 0)
+
+    d, V, B = 4096, workloads.VOCAB, 32
+    gen = torch.Generator(device=device)
+    gen.manual_seed(5)
+    h = torch.randn(B, d, generator=gen, device=device).to(torch.bfloat16)
+    g_f = torch.ones(d, dtype=torch.bfloat16, device=device)
+    w_out = torch.randn(V, d, generator=gen, device=device).mul_(0.02).to(torch.bfloat16)
+    ids = torch.empty(B, dtype=torch.int32, device=device)
+    logits = torch.empty(B, V, dtype=torch.float32, device=device)
+    hws = torch.empty(ddb.llama_lmhead_workspace_bytes(B, d, V), dtype=torch.uint8, device=device)
+    timed("lmhead_argmax_b32", lambda: ddb.llama_lmhead_argmax(h, B, d, g_f, w_out, V, d, 1e-5, ids, logits, hws,
+                                                               hws.numel()))
+    u = torch.rand(B, generator=gen, device=device)
+    timed("sample_b32_top_p_0.9", lambda: ddb.llama_sample(logits, B, V, 1.0, 0, 0.9, u, ids))
+    tok = workloads.make_token_ids(B, 1, V, seed=3).to(device).view(-1)
+    x = torch.empty(B, d, dtype=torch.bfloat16, device=device)
+    timed("embed_b32", lambda: ddb.llama_embed(tok, B, w_out, V, d, x))
+    return {"metric": METRIC, "workload": "kernel survey (one call of each kernel family, after a warm-up call)",
+            "unit": "us per call", "calls": calls}
+
+
 # ----------------------------------------------------------------------------- oracle timing
 
 def oracle_decode_sample(dims, wts32, seqs: int):
@@ -773,9 +843,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("decode", "prefill", "stack"), default="decode",
+    ap.add_argument("--workload", choices=("decode", "prefill", "stack", "survey"), default="decode",
                     help="decode: the 8B decode block (default); prefill: the 8B causal prefill block at --tokens; "
-                         "stack: 32 blocks + embedding + LM head, prefill then greedy decode")
+                         "stack: 32 blocks + embedding + LM head, prefill then greedy decode; survey: one call of "
+                         "each other kernel family, for a per-kernel profile")
     ap.add_argument("--tokens", type=int, default=2048, help="prefill tokens (with --workload prefill)")
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -797,9 +868,9 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    run = {"decode": run_ours, "prefill": run_prefill, "stack": run_stack}[args.workload]
+    run = {"decode": run_ours, "prefill": run_prefill, "stack": run_stack, "survey": run_survey}[args.workload]
     out = run(args, rank, world, device)
-    if rank == 0 and args.cpu_baseline and world == 1:
+    if rank == 0 and args.cpu_baseline and world == 1 and args.workload != "survey":
         out["cpu_baseline"] = cpu_baseline_line(workloads.LLAMA3_8B)
     if rank == 0:
         print(json.dumps(out), flush=True)
