@@ -204,29 +204,85 @@ __global__ void k_embed(const int32_t* __restrict__ ids, const T* __restrict__ w
 // argmax over one row of fp32 logits; ties go to the lowest index.  If the
 // projection that wrote the logits recorded an error in *err (a bounded wait
 // expired), the row's id is that (negative) code instead.
-__global__ void __launch_bounds__(1024) k_argmax_rows(const float* __restrict__ logits, int vocab,
-                                                      int32_t* __restrict__ ids, const int* __restrict__ err) {
-    __shared__ float sv[32];
-    __shared__ int si[32];
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+//
+// One cluster of kArgmaxSplit CTAs per row: CTA c scans the c-th contiguous slice
+// of the row with 16-byte loads, eight in flight per thread, and sends its
+// (maximum, first index) to CTA 0 of the cluster through distributed shared
+// memory.  (One CTA per row left 32 rows of 128,256 logits on 32 SMs, bound by
+// load latency at 63 us.)
+constexpr int kArgmaxSplit = 8;
+constexpr int kArgmaxThreads = 512;
+
+__device__ __forceinline__ void better(float& best, int& bi, float ov, int oi) {
+    if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+}
+
+__global__ void __launch_bounds__(kArgmaxThreads) k_argmax_rows(const float* __restrict__ logits, int vocab,
+                                                                int32_t* __restrict__ ids,
+                                                                const int* __restrict__ err) {
+    __shared__ float sv[kArgmaxThreads / 32];
+    __shared__ int si[kArgmaxThreads / 32];
+    __shared__ float cv[kArgmaxSplit];
+    __shared__ int ci[kArgmaxSplit];
+    uint32_t c;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(c));
+    const int row = blockIdx.x / kArgmaxSplit, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* lr = logits + (size_t)row * vocab;
+    const int per = (vocab + 4 * kArgmaxSplit - 1) / (4 * kArgmaxSplit) * 4;   // slice length, 4-aligned
+    const int lo = min(vocab, (int)c * per), hi = min(vocab, lo + per);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float best = -INFINITY;
     int bi = INT32_MAX;
-    for (int i = tid; i < vocab; i += blockDim.x) {
-        const float v = lr[i];
-        if (v > best) { best = v; bi = i; }   // ascending i: the first maximum stays
+    auto take = [&](int i, float v) {
+        if (v > best) { best = v; bi = i; }   // ascending i per thread: the first maximum stays
+    };
+    if ((vocab & 3) == 0 && ((uintptr_t)lr & 15) == 0) {
+        const float4* l4 = reinterpret_cast<const float4*>(lr);
+        const int e4 = hi >> 2, step = kArgmaxThreads;
+        int i = (lo >> 2) + tid;
+        for (; i + 7 * step < e4; i += 8 * step) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(l4 + i + u * step);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = 4 * (i + u * step);
+                take(e, v[u].x);
+                take(e + 1, v[u].y);
+                take(e + 2, v[u].z);
+                take(e + 3, v[u].w);
+            }
+        }
+        for (; i < e4; i += step) {
+            const float4 v = __ldg(l4 + i);
+            take(4 * i, v.x);
+            take(4 * i + 1, v.y);
+            take(4 * i + 2, v.z);
+            take(4 * i + 3, v.w);
+        }
+    } else {
+        for (int i = lo + tid; i < hi; i += kArgmaxThreads) take(i, __ldg(lr + i));
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
-    }
+    for (int off = 16; off > 0; off >>= 1)
+        better(best, bi, __shfl_xor_sync(0xffffffffu, best, off), __shfl_xor_sync(0xffffffffu, bi, off));
     if (lane == 0) { sv[warp] = best; si[warp] = bi; }
     __syncthreads();
     if (tid == 0) {
-        for (int w = 1; w < (int)(blockDim.x / 32); ++w)
-            if (sv[w] > best || (sv[w] == best && si[w] < bi)) { best = sv[w]; bi = si[w]; }
+        for (int w = 1; w < kArgmaxThreads / 32; ++w) better(best, bi, sv[w], si[w]);
+        // this slice's result into slot c of CTA 0
+        uint32_t av = (uint32_t)__cvta_generic_to_shared(&cv[c]), ai = (uint32_t)__cvta_generic_to_shared(&ci[c]);
+        uint32_t rv, ri;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(rv) : "r"(av));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(ri) : "r"(ai));
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rv), "f"(best) : "memory");
+        asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(ri), "r"(bi) : "memory");
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (c == 0 && tid == 0) {
+        best = cv[0];
+        bi = ci[0];
+        for (int k = 1; k < kArgmaxSplit; ++k) better(best, bi, cv[k], ci[k]);
         const int code = err ? *err : 0;
         ids[row] = code != 0 ? code : (bi == INT32_MAX) ? 0 : bi;
     }
@@ -279,8 +335,20 @@ cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, in
 cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, const int* err,
                                cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    k_argmax_rows<<<rows, 1024, 0, s>>>(logits, vocab, ids, err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows * kArgmaxSplit);
+    cfg.blockDim = dim3(kArgmaxThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kArgmaxSplit;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_argmax_rows, logits, vocab, ids, err);
 }
 
 }  // namespace llama

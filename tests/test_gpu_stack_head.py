@@ -51,6 +51,39 @@ def test_lmhead_argmax_matches_oracle(batch):
     rms = np.sqrt(np.mean(ref ** 2))
     assert np.max(np.abs(got - ref)) / rms <= LOGIT_TOL
     _check_ids(ids.cpu().numpy(), ref, LOGIT_TOL * rms)
+    # the greedy choice is integer work on the kernel's own fp32 logits: exact
+    assert np.array_equal(ids.cpu().numpy(), np.argmax(logits.cpu().numpy(), axis=1))
+
+
+@pytest.mark.parametrize("shift", [1, 4, workloads.VOCAB // 2], ids=["same-thread", "next-thread", "other-slice"])
+@pytest.mark.parametrize("offset", [0, 1], ids=["aligned-logits", "unaligned-logits"])
+def test_lmhead_argmax_ties_take_the_first_index(shift, offset):
+    """Weight rows repeated at a distance `shift` give every logit twice (the
+    projection sums each output column in the same order); the id must be the
+    first index of the maximum wherever the two copies tie, which puts the
+    tie inside one thread's 16-byte load, across neighbouring threads, or across
+    the CTAs that split a row.  A logits buffer one float off 16-byte alignment
+    takes the scalar loads."""
+    import dense_decoder_block_gb300 as ddb
+    ddb.lib()
+    batch, V = 32, workloads.VOCAB
+    h, g, w = _head_inputs(batch, seed=11)
+    src = np.arange(V)
+    rep = src[(src // shift) % 2 == 1] if shift < V // 2 else src[V // 2:]
+    w[rep] = w[rep - shift]
+    dev = torch.device("cuda:0")
+    ids = torch.empty(batch, dtype=torch.int32, device=dev)
+    buf = torch.empty(batch * V + offset, dtype=torch.float32, device=dev)
+    logits = buf[offset:].view(batch, V)
+    nbytes = ddb.llama_lmhead_workspace_bytes(batch, 4096, V)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ddb.llama_lmhead_argmax(h.to(dev), batch, 4096, g.to(dev), w.to(dev), V, 4096, 1e-5, ids, logits, ws, nbytes)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    got = ids.cpu().numpy()
+    assert np.array_equal(got, np.argmax(lg, axis=1))
+    ties = sum(int(np.count_nonzero(lg[b] == lg[b].max()) > 1) for b in range(batch))
+    assert ties == batch, f"only {ties} of {batch} rows have their maximum twice"
 
 
 def test_embed_gather_and_bad_id():
