@@ -71,6 +71,34 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two fp32 lanes in one 64-bit register pair, for the packed f32x2 arithmetic of
+// sm_100 and later: each lane is the IEEE round-to-nearest operation of its scalar
+// form (no flush to zero), so a packed result equals the two scalar results bit for
+// bit -- it halves the instructions, not the precision.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {   // a * b + c, one rounding
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // The softmax of one query row over one 128-key chunk.  Every kernel computes
 // exactly this (prefill with one thread per row, decode with four lanes per row):
 //   m   = c * max_{j <= jmax} S_j,  c = log2(e) / sqrt(d_h)   (keys 0..jmax visible;
@@ -451,28 +479,38 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
     named_bar_sync(bar, 64);   // both halves' maxima written, both S halves read
     const float m = __fmul_rn(fmaxf(xch[row], xch[128 + row]), scale_log2);
     const float m_use = (jmax >= 0) ? m : 0.f;   // a row with no visible key: every p is 0
-    float lq[2] = {0.f, 0.f};
+    if (!full) {
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {   // keys 64h + 16cb ..
-        float* vb = v + cb * 16;
-        if (!full) {
+        for (int j = 0; j < 64; ++j)
+            if (j > jl) v[j] = -INFINITY;
+    }
+    // The two quarter sums of this half advance together, one packed add per step:
+    // lane 0 takes the keys of blocks 0, 1 (quarter 2h) and lane 1 those of blocks
+    // 2, 3 (quarter 2h + 1), each in ascending key order.
+    const uint64_t c2 = pack2(scale_log2, scale_log2), nm2 = pack2(-m_use, -m_use);
+    uint64_t lq2 = pack2(0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-                if (cb * 16 + t > jl) vb[t] = -INFINITY;
-        }
-        uint32_t packed[8];
-        float lc = lq[cb >> 1];
+    for (int cp = 0; cp < 2; ++cp) {   // blocks cp (keys 64h + 16cp ..) and cp + 2
+        const float* va = v + cp * 16;
+        const float* vb = v + (cp + 2) * 16;
+        uint32_t pa[8], pb[8];
 #pragma unroll
         for (int t = 0; t < 16; t += 2) {
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(softmax_p(vb[t], scale_log2, m_use),
-                                                            softmax_p(vb[t + 1], scale_log2, m_use));
-            lc = __fadd_rn(lc, __low2float(pb));
-            lc = __fadd_rn(lc, __high2float(pb));
-            packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+            float xa0, xa1, xb0, xb1;
+            unpack2(fma2(pack2(va[t], va[t + 1]), c2, nm2), xa0, xa1);
+            unpack2(fma2(pack2(vb[t], vb[t + 1]), c2, nm2), xb0, xb1);
+            const __nv_bfloat162 ba = __floats2bfloat162_rn(ex2(xa0), ex2(xa1));
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(ex2(xb0), ex2(xb1));
+            lq2 = add2(lq2, pack2(__low2float(ba), __low2float(bb)));
+            lq2 = add2(lq2, pack2(__high2float(ba), __high2float(bb)));
+            pa[t >> 1] = *reinterpret_cast<const uint32_t*>(&ba);
+            pb[t >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
         }
-        lq[cb >> 1] = lc;
-        tmem_st8(s_taddr + (h * 4 + cb) * 8, packed);
+        tmem_st8(s_taddr + (h * 4 + cp) * 8, pa);
+        tmem_st8(s_taddr + (h * 4 + cp + 2) * 8, pb);
     }
+    float lq[2];
+    unpack2(lq2, lq[0], lq[1]);
     if (h == 1) {
         xch[256 + row] = lq[0];
         xch[384 + row] = lq[1];
@@ -720,10 +758,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(&oc_free[k]);
                 }
+                if (fold) {   // o = fma(o, alpha, oc * beta), two columns per instruction
+                    const uint64_t a2 = pack2(alpha, alpha), b2 = pack2(beta, beta);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float& o = O[cb * 32 + j];
-                    o = fold ? __fmaf_rn(o, alpha, __fmul_rn(oc[j], beta)) : (use ? oc[j] : o);
+                    for (int j = 0; j < 32; j += 2) {
+                        float& o0 = O[cb * 32 + j];
+                        float& o1 = O[cb * 32 + j + 1];
+                        unpack2(fma2(pack2(o0, o1), a2, mul2(pack2(oc[j], oc[j + 1]), b2)), o0, o1);
+                    }
+                } else if (use) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) O[cb * 32 + j] = oc[j];
                 }
             }
             started = started || use;
