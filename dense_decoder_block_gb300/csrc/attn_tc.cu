@@ -93,9 +93,25 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+
+// acc + (the bf16 in the low / high half of p), exactly fadd(acc, float(half)):
+// the mixed-precision add widens its bf16 operand exactly and rounds once.
+__device__ __forceinline__ float add_bf16_lo(uint32_t p, float acc) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+        : "=f"(r) : "r"(p), "f"(acc));
+    return r;
+}
+__device__ __forceinline__ float add_bf16_hi(uint32_t p, float acc) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+        : "=f"(r) : "r"(p), "f"(acc));
+    return r;
+}
+// max(a, b, c), exact like every max
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
 
@@ -466,16 +482,23 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
     ptx::tmem_wait_ld();
     const int jl = jmax - h * 64;   // last visible key of this half, local index
     const bool full = __all_sync(0xffffffffu, jl >= 63);
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    float mx;
     if (full) {
+        float a0 = v[0], a1 = v[1];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+        for (int j = 2; j < 64; j += 4) {
+            a0 = max3(a0, v[j], v[j + 1]);
+            a1 = max3(a1, v[j + 2], v[j + 3]);
+        }
+        mx = fmaxf(a0, a1);
     } else {
+        float a[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int j = 0; j < 64; ++j)
-            if (j <= jl) mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+            if (j <= jl) a[j & 3] = fmaxf(a[j & 3], v[j]);
+        mx = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
     }
-    xch[h * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    xch[h * 128 + row] = mx;
     named_bar_sync(bar, 64);   // both halves' maxima written, both S halves read
     const float m = __fmul_rn(fmaxf(xch[row], xch[128 + row]), scale_log2);
     const float m_use = (jmax >= 0) ? m : 0.f;   // a row with no visible key: every p is 0
@@ -484,11 +507,11 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
         for (int j = 0; j < 64; ++j)
             if (j > jl) v[j] = -INFINITY;
     }
-    // The two quarter sums of this half advance together, one packed add per step:
-    // lane 0 takes the keys of blocks 0, 1 (quarter 2h) and lane 1 those of blocks
-    // 2, 3 (quarter 2h + 1), each in ascending key order.
+    // The two quarter sums of this half (blocks 0, 1: quarter 2h; blocks 2, 3:
+    // quarter 2h + 1) advance side by side, each in ascending key order, each
+    // rounded p added straight from its bf16 half.
     const uint64_t c2 = pack2(scale_log2, scale_log2), nm2 = pack2(-m_use, -m_use);
-    uint64_t lq2 = pack2(0.f, 0.f);
+    float lq[2] = {0.f, 0.f};
 #pragma unroll
     for (int cp = 0; cp < 2; ++cp) {   // blocks cp (keys 64h + 16cp ..) and cp + 2
         const float* va = v + cp * 16;
@@ -501,16 +524,14 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
             unpack2(fma2(pack2(vb[t], vb[t + 1]), c2, nm2), xb0, xb1);
             const __nv_bfloat162 ba = __floats2bfloat162_rn(ex2(xa0), ex2(xa1));
             const __nv_bfloat162 bb = __floats2bfloat162_rn(ex2(xb0), ex2(xb1));
-            lq2 = add2(lq2, pack2(__low2float(ba), __low2float(bb)));
-            lq2 = add2(lq2, pack2(__high2float(ba), __high2float(bb)));
             pa[t >> 1] = *reinterpret_cast<const uint32_t*>(&ba);
             pb[t >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
+            lq[0] = add_bf16_hi(pa[t >> 1], add_bf16_lo(pa[t >> 1], lq[0]));
+            lq[1] = add_bf16_hi(pb[t >> 1], add_bf16_lo(pb[t >> 1], lq[1]));
         }
         tmem_st8(s_taddr + (h * 4 + cp) * 8, pa);
         tmem_st8(s_taddr + (h * 4 + cp + 2) * 8, pb);
     }
-    float lq[2];
-    unpack2(lq2, lq[0], lq[1]);
     if (h == 1) {
         xch[256 + row] = lq[0];
         xch[384 + row] = lq[1];
