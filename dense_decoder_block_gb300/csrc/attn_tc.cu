@@ -130,15 +130,16 @@ __device__ __forceinline__ float softmax_p(float s, float scale_log2, float m) {
 template <int N>
 __device__ __forceinline__ void softmax_keys(const float* sv, int j0, int jmax, float scale_log2, float m,
                                              uint32_t* packed, float& lq) {
+    const uint64_t c2 = pack2(scale_log2, scale_log2), nm2 = pack2(-m, -m);
 #pragma unroll
     for (int j = 0; j < N; j += 2) {
-        float p0 = 0.f, p1 = 0.f;
-        if (j0 + j <= jmax) p0 = softmax_p(sv[j], scale_log2, m);
-        if (j0 + j + 1 <= jmax) p1 = softmax_p(sv[j + 1], scale_log2, m);
+        float x0, x1;   // fma(s, c, -m) for the pair, as softmax_p forms it
+        unpack2(fma2(pack2(sv[j], sv[j + 1]), c2, nm2), x0, x1);
+        const float p0 = (j0 + j <= jmax) ? ex2(x0) : 0.f;
+        const float p1 = (j0 + j + 1 <= jmax) ? ex2(x1) : 0.f;
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        lq = __fadd_rn(lq, __low2float(pb));
-        lq = __fadd_rn(lq, __high2float(pb));
         packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+        lq = add_bf16_hi(packed[j >> 1], add_bf16_lo(packed[j >> 1], lq));
     }
 }
 __device__ __forceinline__ void softmax_quarter(const float* sv, int j0, int jmax, float scale_log2, float m,
