@@ -27,7 +27,7 @@ __all__ = [
     "llama_block_destroy",
     "llama_block_workspace_bytes", "llama_block_workspace_offsets", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
     "llama_block_decode_devpos", "llama_block_decode_seqpos",
-    "llama_block_poll_error", "llama_block_last_error", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
+    "llama_block_poll_error", "llama_block_last_error", "llama_block_selftest_wait_timeout", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
     "llama_embed", "llama_lmhead_workspace_bytes",
     "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_sample", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
 ]
@@ -181,6 +181,11 @@ def llama_block_poll_error(h, stream=None) -> int:
     return int(lib().llama_block_poll_error(h, _stream(stream)))
 
 
+def llama_block_selftest_wait_timeout(h, budget_ns, stream=None) -> None:
+    _check(h, lib().llama_block_selftest_wait_timeout(h, int(budget_ns), _stream(stream)),
+           "llama_block_selftest_wait_timeout")
+
+
 def llama_rmsnorm(x, g, y, rows, d, eps, stream=None) -> None:
     rc = lib().llama_rmsnorm(_ptr(x), _ptr(g), _ptr(y), rows, d, C.c_float(eps), _dtype_code(x.dtype),
                              _stream(stream))
@@ -300,6 +305,9 @@ class LlamaBlock:
 
     def poll_error(self, stream=None) -> int:
         return llama_block_poll_error(self.h, stream)
+
+    def selftest_wait_timeout(self, budget_ns, stream=None) -> None:
+        llama_block_selftest_wait_timeout(self.h, budget_ns, stream)
 
     def launch_count(self) -> int:
         return llama_block_launch_count(self.h)

@@ -602,6 +602,14 @@ extern "C" int llama_block_poll_error(llama_block b, void* stream) {
     return LLAMA_OK;
 }
 
+extern "C" int llama_block_selftest_wait_timeout(llama_block b, unsigned long long budget_ns, void* stream) {
+    if (!b) return LLAMA_ERR_INVALID_ARG;
+    if (budget_ns == 0 || budget_ns > 2000000000ull) budget_ns = 2000000000ull;
+    cudaError_t e = launch_expire_wait(b->err_dev, budget_ns, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(b, e, "wait self-test launch");
+    return LLAMA_OK;
+}
+
 extern "C" const char* llama_block_last_error(llama_block b) { return b ? b->last_error.c_str() : ""; }
 
 extern "C" int llama_block_set_stage_events(llama_block b, void* const* events, int n_events) {

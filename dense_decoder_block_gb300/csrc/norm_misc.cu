@@ -2,6 +2,7 @@
 #include <cfloat>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace llama {
 
@@ -288,6 +289,20 @@ __global__ void __launch_bounds__(kArgmaxThreads) k_argmax_rows(const float* __r
     }
 }
 
+// Failure-path self-test: one warp waits, through the same bounded wait every
+// tcgen05 kernel uses, on an mbarrier that nothing arrives on.  The wait gives up
+// after budget_ns, records LLAMA_ERR_DEVICE_TIMEOUT in *err, and the kernel
+// returns -- no trap, no fault; the context stays usable.
+__global__ void k_expire_wait(int* err, unsigned long long budget_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)ptx::mbar_wait_for(&bar, 0, err, budget_ns);
+}
+
 }  // namespace
 
 cudaError_t launch_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype,
@@ -329,6 +344,11 @@ cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, in
                          cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     k_embed<bf16><<<n, 256, 0, s>>>(ids, (const bf16*)w, (bf16*)x, vocab, d, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expire_wait(int* err, unsigned long long budget_ns, cudaStream_t s) {
+    k_expire_wait<<<1, 32, 0, s>>>(err, budget_ns);
     return cudaGetLastError();
 }
 

@@ -79,7 +79,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // loads that go through it.  err may be null: the wait is still bounded, it just
 // has nowhere to record the expiry.
 constexpr uint64_t kErrPollNs = 200000ull;   // 200 us
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* err, uint64_t budget_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     uint32_t spins = 0;
@@ -88,12 +88,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
         if ((++spins & 63u) == 0) {
             const uint64_t dt = globaltimer() - t0;
             if (err && dt > kErrPollNs && (spins & 4095u) == 0 && *((volatile int*)err) != 0) return false;
-            if (dt > kWaitBudgetNs) {
+            if (dt > budget_ns) {
                 if (err) atomicCAS(err, 0, -6 /* LLAMA_ERR_DEVICE_TIMEOUT */);
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    return mbar_wait_for(bar, parity, err, kWaitBudgetNs);
 }
 
 // Bounded wait that ignores the error word: used only to let copies already in

@@ -203,6 +203,15 @@ int llama_block_decode_seqpos(llama_block blk, const void* x, int batch, const l
  * LLAMA_ERR_POS_RANGE). */
 int llama_block_poll_error(llama_block blk, void* stream);
 
+/* Failure-path self-test.  Launches on `stream` one warp that waits, through the
+ * same bounded mbarrier wait every tensor-core kernel of the library uses, on a
+ * barrier nothing arrives on.  After budget_ns nanoseconds (0 or more than 2 s:
+ * the kernels' own 2 s budget) the wait gives up, records
+ * LLAMA_ERR_DEVICE_TIMEOUT in the handle's error word and the kernel returns:
+ * llama_block_poll_error then reports it, and the handle and the CUDA context stay
+ * usable.  Returns LLAMA_OK once the launch is queued. */
+int llama_block_selftest_wait_timeout(llama_block blk, unsigned long long budget_ns, void* stream);
+
 /* Message of the last failure on this handle ("" if none).  Valid until the
  * next call on the handle. */
 const char* llama_block_last_error(llama_block blk);

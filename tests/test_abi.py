@@ -75,6 +75,7 @@ def test_null_arguments_are_rejected_without_a_gpu(lib_path):
     dev = ctypes.c_void_p(1)
     assert lib.llama_device_ptr_of_host(None, ctypes.byref(dev)) == _native.LLAMA_ERR_INVALID_ARG
     assert lib.llama_block_set_stage_events(None, None, 0) == _native.LLAMA_ERR_INVALID_ARG
+    assert lib.llama_block_selftest_wait_timeout(None, 1000000, None) == _native.LLAMA_ERR_INVALID_ARG
 
 
 def test_product_package_does_not_import_the_oracle():

@@ -194,6 +194,35 @@ def test_error_paths():
     assert e.value.code == ddb.LLAMA_ERR_UNSUPPORTED_DIMS
 
 
+def test_bounded_wait_expiry_is_reported_and_the_handle_recovers():
+    """The failure path of every tensor-core kernel's mbarrier waits, run for real:
+    a wait that nothing satisfies gives up after its budget, records
+    LLAMA_ERR_DEVICE_TIMEOUT in the handle's error word and returns (no trap, no
+    fault); the host reads the code once, and the next decode on the same handle and
+    context gives the same bits as before."""
+    import time
+    import dense_decoder_block_gb300 as ddb
+    inp = workloads.make_block_inputs(MID, 2, 1, cache_len=40, max_seq=48)
+    blk, _ = gpu_block(inp, 48)
+    dev = torch.device("cuda:0")
+    kv = ddb.KVCache(inp.k_cache.to(dev), inp.v_cache.to(dev))
+    x = inp.x.to(dev)
+    y0 = torch.empty_like(x)
+    ws = blk.workspace(2, 1)
+    blk.decode(x, kv, 40, y0, ws)
+    assert blk.poll_error() == 0
+    t0 = time.perf_counter()
+    blk.selftest_wait_timeout(20_000_000)   # 20 ms
+    assert blk.poll_error() == ddb.LLAMA_ERR_DEVICE_TIMEOUT
+    waited = time.perf_counter() - t0
+    assert 0.015 <= waited < 1.5, waited
+    assert blk.poll_error() == 0            # read once, then cleared
+    y1 = torch.empty_like(x)
+    blk.decode(x, kv, 40, y1, ws)
+    assert blk.poll_error() == 0
+    assert torch.equal(y0, y1)
+
+
 def test_rmsnorm_step_matches_oracle():
     import dense_decoder_block_gb300 as ddb
     from oracle.bf16 import round_bf16
