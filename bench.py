@@ -626,9 +626,24 @@ def extra_sample(ddb, device, stream):
     u = torch.rand(32, generator=gen, device=device)
     ids = torch.empty(32, dtype=torch.int32, device=device)
     out = {}
+    calls = 20
     for name, k, p in (("top_p_0.9", 0, 0.9), ("top_k_50_top_p_0.9", 50, 0.9)):
-        ms = time_region(lambda: ddb.llama_sample(z, 32, workloads.VOCAB, 1.0, k, p, u, ids), 20, 3, stream)
-        out[name] = {"us_per_call": round(ms * 1e3, 2), "logits_mb": round(32 * workloads.VOCAB * 4 / 1e6, 2)}
+        # device time: the calls captured once in a CUDA graph and replayed (the
+        # Python marshalling of an eager call takes about as long as the kernel)
+        cap = torch.cuda.Stream(device)
+        for _ in range(3):
+            ddb.llama_sample(z, 32, workloads.VOCAB, 1.0, k, p, u, ids, stream=cap)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(calls):
+                    ddb.llama_sample(z, 32, workloads.VOCAB, 1.0, k, p, u, ids, stream=cap)
+        ms = time_region(g.replay, 5, 2, stream) / calls
+        eager = time_region(lambda: ddb.llama_sample(z, 32, workloads.VOCAB, 1.0, k, p, u, ids), calls, 3, stream)
+        out[name] = {"us_per_call": round(ms * 1e3, 2), "us_per_eager_call": round(eager * 1e3, 2),
+                     "logits_mb": round(32 * workloads.VOCAB * 4 / 1e6, 2),
+                     "hbm_frac": round(32 * workloads.VOCAB * 4 / (ms / 1e3) / 1e9 / 6760.6, 4)}
     return out
 
 
