@@ -180,6 +180,18 @@ def committed_traffic(kernel_key: str):
     return None
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (each rank's timed region: the job takes as long
+    as its slowest replica); x itself on a single rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, device):
@@ -255,9 +267,7 @@ def run_ours(args, rank, world, device):
     clocks = clk.summary()
     ms_step = ms / args.steps
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, world, device)
         ms_step = ms / args.steps
     tokens = B * world * args.steps
     value = tokens / (ms / 1e3)
@@ -297,12 +307,7 @@ def run_ours(args, rank, world, device):
             fn()
         e1.record(stream)
         barrier()
-        t = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([t], dtype=torch.float64, device=device)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            t = float(tt.item())
-        return t
+        return max_over_ranks(e0.elapsed_time(e1), world, device)
 
     e2e_ms = timed(graph_h.replay)
 
