@@ -715,6 +715,126 @@ def extra_70b(ddb, device, hbm, bf16_peak, peak_kind):
     return res
 
 
+TRACE_NAMES = {1: "rmsnorm", 2: "gemm_ws", 3: "gemm_tt", 4: "reduce_qkv", 5: "reduce_resid", 6: "reduce_swiglu",
+               7: "reduce_resid_norm", 8: "attn_decode", 9: "attn_combine", 10: "attn_prefill", 11: "rope",
+               12: "attn_wide"}
+
+
+def timeline_stages(rec, order):
+    """Per-launch figures from a per-CTA trace of one step.  `order` lists the
+    step's launches as (stage name, kernel id) in launch order; launches sharing an
+    id are told apart by CTA index: a launch's CTA i starts before CTA i of the
+    next launch of that kernel, which is several launches later."""
+    rows = sorted(zip(rec["kernel"], rec["t_start"], rec["t_release"], rec["t_end"], rec["cta"]), key=lambda r: r[1])
+    t0 = min(r[1] for r in rows)
+    uses = {}
+    for name, kid in order:
+        uses.setdefault(kid, []).append(name)
+    groups = {name: [] for name, _ in order}
+    seen = {}
+    for r in rows:   # the j-th record of a (kernel, CTA index) in time belongs to the j-th launch of that kernel
+        names = uses.get(r[0])
+        if not names:
+            continue
+        j = seen.get((r[0], r[4]), 0)
+        seen[(r[0], r[4])] = j + 1
+        if j < len(names):
+            groups[names[j]].append(r)
+    out = {}
+    prev_end = None
+    for name, _ in order:
+        rs = groups[name]
+        if not rs:
+            out[name] = {"ctas": 0}
+            continue
+        first = min(r[1] for r in rs) - t0
+        last = max(r[3] for r in rs) - t0
+        rel = [r[2] - t0 for r in rs if r[2]]
+        durs = sorted(r[3] - r[1] for r in rs)
+        out[name] = {"ctas": len(rs), "first_start_us": round(first / 1e3, 2), "last_end_us": round(last / 1e3, 2),
+                     "span_us": round((last - first) / 1e3, 2),
+                     "last_release_us": round(max(rel) / 1e3, 2) if rel else None,
+                     "cta_us_median": round(durs[len(durs) // 2] / 1e3, 2),
+                     "start_after_previous_end_us": None if prev_end is None else round((first - prev_end) / 1e3, 2)}
+        prev_end = last
+    out["step_us"] = round((max(r[3] for r in rows) - t0) / 1e3, 2)
+    return out
+
+
+def run_timeline(args, rank, world, device):
+    """One replayed decode step (the default workload: 8B block, batch 32, pos 1000)
+    and one 2048-token prefill, each traced CTA by CTA (llama_trace_begin, in the
+    library's trace build): when each launch's first CTA starts, its last ends and
+    its CTAs' durations -- from kernel start, not from the dependency release.  A
+    traced step runs a few microseconds longer than the product build's."""
+    from dense_decoder_block_gb300 import _native
+    from dense_decoder_block_gb300 import build as _build
+    _native.load(_build.build(trace=True))   # the trace build of the same sources
+    import dense_decoder_block_gb300 as ddb
+    dims = workloads.LLAMA3_8B
+    B = args.batch
+    wts = workloads.make_weights(dims, weight_std=0.02)
+    inp = workloads.make_block_inputs(dims, B, 1, cache_len=POS, max_seq=MAX_SEQ, weights=wts)
+    w = {k: v.to(device) for k, v in inp.weights.items()}
+    g = {k: v.to(device) for k, v in inp.gains.items()}
+    blk = ddb.LlamaBlock(dims, w, g, MAX_SEQ)
+    kv = ddb.KVCache(inp.k_cache.to(device), inp.v_cache.to(device))
+    x = inp.x.to(device)
+    y = torch.empty_like(x)
+    ws = blk.workspace(B, 1)
+    pos_dev = torch.tensor([POS], dtype=torch.int32, device=device)
+    cap = torch.cuda.Stream(device)
+    for _ in range(args.warmup):
+        blk.decode(x, kv, POS, y, ws)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            blk.decode_devpos(x, kv, pos_dev, y, ws, cap)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    decode_order = [("rmsnorm_1", 1), ("qkv", 2), ("qkv_reduce", 4), ("attention", 8), ("attention_combine", 9),
+                    ("o_proj", 2 | 1 << 8), ("o_reduce_rmsnorm_2", 7), ("gate_up", 2 | 2 << 8),
+                    ("down", 2 | 1 << 8), ("down_reduce", 5)]
+    steps = []
+    for _ in range(max(1, min(args.steps, 5))):
+        with ddb.Trace(1 << 14, device) as tr:
+            graph.replay()
+            torch.cuda.synchronize(device)
+        steps.append(timeline_stages(tr.records(), decode_order))
+    assert blk.poll_error() == 0
+    best = min(steps, key=lambda st: st["step_us"])
+    by = decode_step_bytes(dims, B, POS)
+    hbm = peaks()[0]
+    res = {"metric": "per-CTA timeline of one replayed decode step and one prefill", "workload": "timeline",
+           "decode_8b_b32_pos1000": best, "decode_steps_traced": [st["step_us"] for st in steps],
+           "decode_step_hbm_frac": round(by / (best["step_us"] / 1e6) / 1e9 / hbm, 4)}
+    del graph, blk, kv, w
+    torch.cuda.empty_cache()
+
+    T = 2048
+    pinp = workloads.make_block_inputs(dims, 1, T, max_seq=T, weights=wts)
+    w = {k: v.to(device) for k, v in pinp.weights.items()}
+    g = {k: v.to(device) for k, v in pinp.gains.items()}
+    pblk = ddb.LlamaBlock(dims, w, g, T)
+    pkv = ddb.KVCache(pinp.k_cache.to(device), pinp.v_cache.to(device))
+    px = pinp.x.to(device)
+    py = torch.empty_like(px)
+    pws = pblk.workspace(1, T)
+    for _ in range(args.warmup):
+        pblk.prefill(px, pkv, py, pws)
+    torch.cuda.synchronize(device)
+    prefill_order = [("rmsnorm_1", 1), ("qkv", 3), ("rope", 11), ("attention", 10), ("o_proj", 3 | 1 << 8),
+                     ("rmsnorm_2", 1), ("gate_up", 3 | 2 << 8), ("down", 3 | 1 << 8)]
+    with ddb.Trace(1 << 16, device) as tr:
+        pblk.prefill(px, pkv, py, pws)
+        torch.cuda.synchronize(device)
+    assert pblk.poll_error() == 0
+    res["prefill_8b_t2048"] = timeline_stages(tr.records(), prefill_order)
+    return res
+
+
 def run_survey(args, rank, world, device):
     """One call of each kernel family the default line does not time on its own, each
     after a warm-up call, for a per-kernel launch list under a profiler (every input
@@ -863,10 +983,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("decode", "prefill", "stack", "survey"), default="decode",
+    ap.add_argument("--workload", choices=("decode", "prefill", "stack", "survey", "timeline"), default="decode",
                     help="decode: the 8B decode block (default); prefill: the 8B causal prefill block at --tokens; "
                          "stack: 32 blocks + embedding + LM head, prefill then greedy decode; survey: one call of "
-                         "each other kernel family, for a per-kernel profile")
+                         "each other kernel family, for a per-kernel profile; timeline: one decode step and one "
+                         "prefill traced CTA by CTA")
     ap.add_argument("--tokens", type=int, default=2048, help="prefill tokens (with --workload prefill)")
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -888,9 +1009,10 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    run = {"decode": run_ours, "prefill": run_prefill, "stack": run_stack, "survey": run_survey}[args.workload]
+    run = {"decode": run_ours, "prefill": run_prefill, "stack": run_stack, "survey": run_survey,
+           "timeline": run_timeline}[args.workload]
     out = run(args, rank, world, device)
-    if rank == 0 and args.cpu_baseline and world == 1 and args.workload != "survey":
+    if rank == 0 and args.cpu_baseline and world == 1 and args.workload not in ("survey", "timeline"):
         out["cpu_baseline"] = cpu_baseline_line(workloads.LLAMA3_8B)
     if rank == 0:
         print(json.dumps(out), flush=True)

@@ -27,7 +27,7 @@ __all__ = [
     "llama_block_destroy",
     "llama_block_workspace_bytes", "llama_block_workspace_offsets", "llama_block_prefill", "llama_block_prefill_at", "llama_block_decode",
     "llama_block_decode_devpos", "llama_block_decode_seqpos",
-    "llama_block_poll_error", "llama_block_last_error", "llama_block_selftest_wait_timeout", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
+    "llama_block_poll_error", "llama_block_last_error", "llama_block_selftest_wait_timeout", "Trace", "llama_block_set_stage_events", "llama_block_launch_count", "HostMapped",
     "llama_embed", "llama_lmhead_workspace_bytes",
     "llama_lmhead_argmax", "llama_lmhead_argmax_noalloc", "llama_sample", "llama_rmsnorm", "LLAMA_BF16", "LLAMA_F32",
 ]
@@ -179,6 +179,41 @@ def llama_block_launch_count(h) -> int:
 
 def llama_block_poll_error(h, stream=None) -> int:
     return int(lib().llama_block_poll_error(h, _stream(stream)))
+
+
+class Trace:
+    """Per-CTA timeline of the block's kernels while the context is open
+    (llama_trace_begin / llama_trace_end; the trace build of the library only:
+    load it with `_native.load(build.build(trace=True))` before the first call).
+    After exit, `records()` gives the columns kernel, sm, cta, t_start,
+    t_release, t_end (ns) on the host."""
+
+    def __init__(self, capacity: int = 1 << 16, device=None):
+        import torch
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.capacity = int(capacity)
+        self.buf = torch.zeros(self.capacity, 4, dtype=torch.int64, device=dev)
+        self.count = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def __enter__(self):
+        rc = lib().llama_trace_begin(_ptr(self.buf), _ptr(self.count), self.capacity)
+        if rc != LLAMA_OK:
+            raise LlamaError(rc, "llama_trace_begin")
+        return self
+
+    def __exit__(self, *exc):
+        lib().llama_trace_end()
+        return False
+
+    def records(self):
+        import torch
+        torch.cuda.synchronize(self.buf.device)
+        n = min(int(self.count.item()), self.capacity)
+        r = self.buf[:n].cpu()
+        w0 = r[:, 0]
+        return {"kernel": (w0 & 0xffff).tolist(), "sm": ((w0 >> 16) & 0xffff).tolist(),
+                "cta": ((w0 >> 32) & 0xffffffff).tolist(), "t_start": r[:, 1].tolist(),
+                "t_release": r[:, 2].tolist(), "t_end": r[:, 3].tolist(), "claimed": int(self.count.item())}
 
 
 def llama_block_selftest_wait_timeout(h, budget_ns, stream=None) -> None:

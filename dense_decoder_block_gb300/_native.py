@@ -70,6 +70,8 @@ SIGNATURES = {
     "llama_block_poll_error": (C.c_int, [C.c_void_p, C.c_void_p]),
     "llama_block_last_error": (C.c_char_p, [C.c_void_p]),
     "llama_block_selftest_wait_timeout": (C.c_int, [C.c_void_p, C.c_ulonglong, C.c_void_p]),
+    "llama_trace_begin": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint]),
+    "llama_trace_end": (C.c_int, []),
     "llama_block_set_stage_events": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p), C.c_int]),
     "llama_block_launch_count": (C.c_int, [C.c_void_p]),
     "llama_device_ptr_of_host": (C.c_int, [C.c_void_p, C.POINTER(C.c_void_p)]),

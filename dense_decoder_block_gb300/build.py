@@ -4,6 +4,10 @@ Each .cu under csrc/ is compiled to an object in parallel, then linked into
 ``dense_decoder_block_gb300/libllama_block.so`` (CUDA runtime linked
 statically).  A stamp of the sources and flags skips rebuilding when nothing
 changed.  Run as ``python -m dense_decoder_block_gb300.build``.
+
+``build(trace=True)`` (``--trace``) builds the same sources with LLAMA_TRACE
+into ``libllama_block_trace.so``: the variant whose kernels record the per-CTA
+timeline (llama_trace_begin); the product library carries none of that code.
 """
 from __future__ import annotations
 
@@ -19,7 +23,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libllama_block.so")
-STAMP = os.path.join(BUILD, "stamp.txt")
+TRACE_LIB = os.path.join(PKG, "libllama_block_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
@@ -36,7 +40,7 @@ def _sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _digest() -> str:
+def _digest(extra) -> str:
     h = hashlib.sha256()
     files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
     files.append(os.path.join(ROOT, "include", "llama_block.h"))
@@ -44,25 +48,29 @@ def _digest() -> str:
         h.update(f.encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(ARCH + CFLAGS).encode())
+    h.update(" ".join(ARCH + CFLAGS + extra).encode())
     h.update(os.uname().machine.encode())
     return h.hexdigest()
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    digest = _digest()
-    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
-        with open(STAMP) as f:
+def build(verbose: bool = False, force: bool = False, trace: bool = False) -> str:
+    extra = ["-DLLAMA_TRACE"] if trace else []
+    lib = TRACE_LIB if trace else LIB
+    bdir = os.path.join(BUILD, "trace") if trace else BUILD
+    stamp = os.path.join(bdir, "stamp.txt")
+    digest = _digest(extra)
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
+        with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
-    os.makedirs(BUILD, exist_ok=True)
+                return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(bdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def compile_one(src_obj):
         src, obj = src_obj
-        cmd = [nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -71,16 +79,16 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         list(ex.map(compile_one, zip(srcs, objs)))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="--force" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="--force" in sys.argv, trace="--trace" in sys.argv))

@@ -602,6 +602,26 @@ extern "C" int llama_block_poll_error(llama_block b, void* stream) {
     return LLAMA_OK;
 }
 
+#ifdef LLAMA_TRACE
+static int trace_set_all(const TraceCtl& c) {
+    for (auto set : {trace_set_norm, trace_set_gemm_ws, trace_set_gemm_tt, trace_set_reduce, trace_set_attn_tc,
+                     trace_set_attn_simt})
+        if (set(c) != cudaSuccess) return LLAMA_ERR_CUDA;
+    return LLAMA_OK;
+}
+
+extern "C" int llama_trace_begin(unsigned long long* records, unsigned int* count, unsigned int capacity) {
+    if (!records || !count || capacity == 0) return LLAMA_ERR_INVALID_ARG;
+    return trace_set_all(TraceCtl{records, count, capacity});
+}
+
+extern "C" int llama_trace_end(void) { return trace_set_all(TraceCtl{nullptr, nullptr, 0}); }
+#else
+// the product build records nothing
+extern "C" int llama_trace_begin(unsigned long long*, unsigned int*, unsigned int) { return LLAMA_ERR_UNSUPPORTED_DIMS; }
+extern "C" int llama_trace_end(void) { return LLAMA_OK; }
+#endif
+
 extern "C" int llama_block_selftest_wait_timeout(llama_block b, unsigned long long budget_ns, void* stream) {
     if (!b) return LLAMA_ERR_INVALID_ARG;
     if (budget_ns == 0 || budget_ns > 2000000000ull) budget_ns = 2000000000ull;

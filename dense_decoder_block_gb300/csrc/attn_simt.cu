@@ -269,10 +269,12 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode_chunks(const AttnK a) 
 
 template <typename T, int DH>
 __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
     // The position is set before the step, never by the kernels this one overlaps.
     const int pos = a.pos_seq ? a.pos_seq[b] : base_position(a);
     ptx_wait();
+    TRACE(const unsigned long long tr1 = trace_stamp();)
     if (threadIdx.x == 0) ptx_launch_dependents();
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int g = h / n_rep, r = h % n_rep;
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     const float* base = a.partial + (((size_t)b * a.n_kv_heads + g) * a.n_chunks * n_rep + r) * part_stride(DH);
     T* dst = reinterpret_cast<T*>(a.o) + (size_t)b * a.n_heads * DH + (size_t)h * DH;
     fold_row<T, DH>(base, (size_t)n_rep * part_stride(DH), pos / kAttnChunk + 1, lane, dst);
+    TRACE(trace_cta(TR_ATTN_COMBINE, tr0, tr1);)
 }
 
 template <typename T, int DH>
@@ -343,6 +346,8 @@ cudaError_t combine_impl(const AttnArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+LLAMA_TRACE_UNIT(attn_simt)
 
 size_t attn_decode_partial_bytes(int batch, int n_kv_heads, int n_chunks, int n_rep, int head_dim) {
     return (size_t)batch * n_kv_heads * n_chunks * n_rep * part_stride(head_dim) * sizeof(float);

@@ -231,6 +231,7 @@ __device__ __forceinline__ void softmax_row(uint32_t s_taddr, int jmax, float sc
 // lane quarter w % 4).
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_tc_wide(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV, const TcArgs a) {
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
+    TRACE(const unsigned long long tr1 = trace_stamp();)
 
     const int g = blockIdx.y, b = blockIdx.z;
     const int n_rep = a.n_heads / a.n_kv_heads;
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
+    TRACE(trace_cta(TR_ATTN_WIDE, tr0, tr1);)
 }
 
 // ----------------------------------------------------------------------------- prefill
@@ -549,6 +552,7 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
 __global__ void __launch_bounds__(kPfThreads, 1)
     k_attn_pf(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
               const __grid_constant__ CUtensorMap mV, const TcArgs a) {
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + PF_OFF_BAR);
@@ -566,6 +570,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
+    TRACE(const unsigned long long tr1 = trace_stamp();)
 
     // blockIdx.x = (sequence, KV head), blockIdx.y = query tile from the last: CTAs are
     // dispatched in linear order, so every group's longest tiles go first
@@ -818,6 +823,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
+    TRACE(trace_cta(TR_ATTN_PF, tr0, tr1);)
 }
 
 // ----------------------------------------------------------------------------- decode
@@ -923,6 +929,10 @@ __device__ __forceinline__ void tmem_ld_quarter(uint32_t taddr, int q, float (&o
 __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_constant__ CUtensorMap mK,
                                                                 const __grid_constant__ CUtensorMap mV,
                                                                 const TcArgs a) {
+    TRACE(const unsigned long long tr0 = trace_stamp();)
+    // trace builds: when the first producer's wait returned
+    TRACE(__shared__ unsigned long long s_tr_release;)
+    TRACE(if (threadIdx.x == 0) s_tr_release = 0;)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + D_OFF_BAR);
@@ -1041,6 +1051,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
                 const DecUnit d = dec_unit(dm, u_begin + i);
                 if (!waited && d.c == d.nt - 1) {   // this chunk holds the row the QKV step writes
                     ptx::griddep_wait();
+                    TRACE(if (LLAMA_TRACE_ON && is_k) s_tr_release = trace_clock();)
                     waited = true;
                 }
                 const int row = (d.b * a.n_kv_heads + d.g) * a.kv_seq + d.c * kAttnChunk;
@@ -1210,6 +1221,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
+    TRACE(trace_cta(TR_ATTN_DEC, tr0, s_tr_release);)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1274,6 +1286,8 @@ TcArgs make_args(const AttnArgs& a) {
 }
 
 }  // namespace
+
+LLAMA_TRACE_UNIT(attn_tc)
 
 bool attention_tc_supported(int n_heads, int n_kv_heads, int head_dim) {
     const int n_rep = n_heads / n_kv_heads;

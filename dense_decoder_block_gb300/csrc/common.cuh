@@ -136,4 +136,74 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// ---------------------------------------------------------------- per-CTA timeline (trace builds)
+// In a library built with LLAMA_TRACE, while llama_trace_begin is in effect each
+// CTA of the block's step kernels writes one record when its thread 0 finishes:
+// {kernel | smid << 16 | cta << 32, %globaltimer at the CTA's start, after its
+// grid-dependency wait (0 where the recording thread does not wait), at thread
+// 0's end}.  In the product build every hook below compiles to nothing.  The
+// control word lives in each translation unit's constant bank (no relocatable
+// device code), so every unit with traced kernels has a setter (LLAMA_TRACE_UNIT)
+// and llama_trace_begin sets them all.
+enum TraceKernel : unsigned int {
+    TR_RMSNORM = 1, TR_GEMM_WS = 2, TR_GEMM_TT = 3, TR_REDUCE_QKV = 4, TR_REDUCE_RESID = 5, TR_REDUCE_SWIGLU = 6,
+    TR_REDUCE_RESID_NORM = 7, TR_ATTN_DEC = 8, TR_ATTN_COMBINE = 9, TR_ATTN_PF = 10, TR_ROPE = 11, TR_ATTN_WIDE = 12,
+};
+struct TraceCtl {
+    unsigned long long* recs;   // [capacity][4]
+    unsigned int* count;        // records claimed (may exceed capacity: the extra ones are dropped)
+    unsigned int capacity;
+};
+__device__ __forceinline__ unsigned long long trace_clock() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// TRACE(statement): the statement in trace builds, nothing in the product build
+#ifdef LLAMA_TRACE
+#define TRACE(...) __VA_ARGS__
+#else
+#define TRACE(...)
+#endif
+#ifdef LLAMA_TRACE
+static __constant__ TraceCtl g_trace;
+#define LLAMA_TRACE_ON (g_trace.recs != nullptr)
+#define LLAMA_TRACE_UNIT(name)                                                  \
+    cudaError_t trace_set_##name(const TraceCtl& c) {                           \
+        return cudaMemcpyToSymbol(g_trace, &c, sizeof(c));                      \
+    }
+#else
+#define LLAMA_TRACE_ON false
+#define LLAMA_TRACE_UNIT(name)                                                  \
+    cudaError_t trace_set_##name(const TraceCtl&) { return cudaErrorNotSupported; }
+#endif
+// %globaltimer for thread 0 while tracing is on, else 0 (no timer read)
+__device__ __forceinline__ unsigned long long trace_stamp() {
+    return (LLAMA_TRACE_ON && threadIdx.x == 0) ? trace_clock() : 0ull;
+}
+// thread 0 of the CTA, at its end: `kernel` is a TraceKernel, optionally with the
+// epilogue kind in bits 8..15
+__device__ __forceinline__ void trace_cta(unsigned int kernel, unsigned long long t_start,
+                                          unsigned long long t_release) {
+#ifdef LLAMA_TRACE
+    if (threadIdx.x != 0 || !LLAMA_TRACE_ON) return;
+    const TraceCtl c = g_trace;
+    const unsigned int i = atomicAdd(c.count, 1u);
+    if (i >= c.capacity) return;
+    unsigned int smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const unsigned long long cta =
+        blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z);
+    unsigned long long* r = c.recs + 4ull * i;
+    r[0] = (unsigned long long)(kernel & 0xffffu) | ((unsigned long long)(smid & 0xffffu) << 16) | (cta << 32);
+    r[1] = t_start;
+    r[2] = t_release;
+    r[3] = trace_clock();
+#else
+    (void)kernel;
+    (void)t_start;
+    (void)t_release;
+#endif
+}
+
 }  // namespace llama

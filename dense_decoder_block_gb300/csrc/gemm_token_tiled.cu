@@ -5,6 +5,8 @@
 
 namespace llama {
 
+LLAMA_TRACE_UNIT(gemm_tt)
+
 template <int BN, bool DUAL, int EPI>
 static cudaError_t run_tt(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0, const CUtensorMap& a1,
                           const CUtensorMap& a2, const bf16* x, cudaStream_t s) {

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
     // Accumulator lane = token, columns 0..127 gate, 128..255 up.
     constexpr uint32_t IDESC = DUAL ? ptx::idesc_bf16_f32(128, 2 * BN) : ptx::idesc_bf16_f32(128, BN);
 
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
@@ -72,6 +73,8 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
     uint64_t* tfull = empty + C::STAGES;
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = (uint32_t*)(tempty + 2);
+    // trace builds: when the producer's wait returned
+    TRACE(unsigned long long* tr_release = (unsigned long long*)(tempty + 3);)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total_kb = a.K / kBlockK;
@@ -112,6 +115,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
         for (int i = 0; i < C::STAGES; ++i) { ptx::mbar_init(&full[i], 1); ptx::mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; ++i) { ptx::mbar_init(&tfull[i], 1); ptx::mbar_init(&tempty[i], C::EPI_WARPS); }
         ptx::fence_mbar_init();
+        TRACE(*tr_release = 0;)
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -165,6 +169,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                                 // The weights do not depend on the previous kernel: the first stages
                                 // of them are in flight before waiting for it; then the activations.
                                 ptx::griddep_wait();
+                                TRACE(if (LLAMA_TRACE_ON) *tr_release = trace_clock();)
                                 ptx::griddep_launch_dependents();
                                 for (int j = 0; j <= it; ++j) load_b_of(j);
                                 waited = true;
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                 }
                 if (!waited && ok) {   // fewer k-blocks than stages in total
                     ptx::griddep_wait();
+                    TRACE(if (LLAMA_TRACE_ON) *tr_release = trace_clock();)
                     ptx::griddep_launch_dependents();
                     for (int j = 0; j < it; ++j) load_b_of(j);
                 }
@@ -290,6 +296,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    TRACE(trace_cta(TR_GEMM_TT | (EPI << 8), tr0, *tr_release);)
 }
 
 }  // namespace llama

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr int CPT = C::CPT;
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(128, BN);
 
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
@@ -46,6 +47,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = empty + C::STAGES;
     uint64_t* tempty = tfull + 2;
     uint32_t* tmem_holder = (uint32_t*)(tempty + 2);
+    // trace builds: when the MMA thread's wait returned
+    TRACE(unsigned long long* tr_release = (unsigned long long*)(tempty + 3);)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total_kb = a.K / kBlockK;
@@ -57,6 +60,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int i = 0; i < C::STAGES; ++i) { ptx::mbar_init(&full[i], 1); ptx::mbar_init(&empty[i], 1); }
         for (int i = 0; i < 2; ++i) { ptx::mbar_init(&tfull[i], 1); ptx::mbar_init(&tempty[i], 8); }
         ptx::fence_mbar_init();
+        TRACE(*tr_release = 0;)
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -124,6 +128,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // first the activations of the prefetched stages (see the producer)
             ptx::prefetch_tmap(&mB);
             ptx::griddep_wait();
+            TRACE(if (LLAMA_TRACE_ON) *tr_release = trace_clock();)
             ptx::griddep_launch_dependents();
             {
                 int n_iter = 0;
@@ -212,6 +217,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    TRACE(trace_cta(TR_GEMM_WS | (EPI << 8), tr0, *tr_release);)
 }
 
 }  // namespace llama

@@ -144,6 +144,14 @@ cudaError_t launch_rope_append_f32(const float* qkv_q, const float* qkv_k, const
 cudaError_t launch_embed(const int32_t* ids, int n, const void* w, int vocab, int d, void* x, int32_t* err,
                          cudaStream_t s);
 // ids[r] = argmax of logits row r, or *err when err is set and nonzero.
+// Per-CTA timeline: the control word of each translation unit with traced kernels.
+cudaError_t trace_set_norm(const TraceCtl& c);
+cudaError_t trace_set_gemm_ws(const TraceCtl& c);
+cudaError_t trace_set_gemm_tt(const TraceCtl& c);
+cudaError_t trace_set_reduce(const TraceCtl& c);
+cudaError_t trace_set_attn_tc(const TraceCtl& c);
+cudaError_t trace_set_attn_simt(const TraceCtl& c);
+
 // Failure-path self-test: a bounded wait that nothing satisfies (records LLAMA_ERR_DEVICE_TIMEOUT in *err).
 cudaError_t launch_expire_wait(int* err, unsigned long long budget_ns, cudaStream_t s);
 cudaError_t launch_argmax_rows(const float* logits, int rows, int vocab, int32_t* ids, const int* err,

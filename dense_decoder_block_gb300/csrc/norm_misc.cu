@@ -25,7 +25,9 @@ template <typename T, int EPT>
 __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ x, const T* __restrict__ g,
                                                           T* __restrict__ y, int d, float eps) {
     __shared__ float red[16 * 8];
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    TRACE(const unsigned long long tr1 = trace_stamp();)
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x, tid = threadIdx.x;
     const T* xr = x + (size_t)row * d;
@@ -67,6 +69,7 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ 
                 yr[i] = __fmul_rn(__fmul_rn(v, r), to_f(g[i]));
         }
     }
+    TRACE(trace_cta(TR_RMSNORM, tr0, tr1);)
 }
 
 template <typename T>
@@ -157,7 +160,9 @@ __global__ void __launch_bounds__(256) k_rope_inplace(bf16* __restrict__ q, bf16
                                                       const int* pos_dev, int max_pos,
                                                       const float* __restrict__ cos_tab,
                                                       const float* __restrict__ sin_tab, int* err) {
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    TRACE(const unsigned long long tr1 = trace_stamp();)
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int per_tok = (n_heads + n_kv_heads) * 16;   // 16 eight-element groups per 128-wide row
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -187,6 +192,7 @@ __global__ void __launch_bounds__(256) k_rope_inplace(bf16* __restrict__ q, bf16
         w[k] = *reinterpret_cast<const uint32_t*>(&o);
     }
     *p = u;
+    TRACE(trace_cta(TR_ROPE, tr0, tr1);)
 }
 
 template <typename T>
@@ -304,6 +310,8 @@ __global__ void k_expire_wait(int* err, unsigned long long budget_ns) {
 }
 
 }  // namespace
+
+LLAMA_TRACE_UNIT(norm)
 
 cudaError_t launch_rmsnorm(const void* x, const void* g, void* y, int rows, int d, float eps, int dtype,
                            cudaStream_t s) {

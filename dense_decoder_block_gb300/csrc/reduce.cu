@@ -19,9 +19,12 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ void griddep() {
+// returns the time the wait returned (for the optional timeline)
+__device__ __forceinline__ unsigned long long griddep() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    const unsigned long long t = trace_stamp();
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    return t;
 }
 
 // What a reduction reads before griddepcontrol.wait -- the position, the RoPE
@@ -32,20 +35,23 @@ __device__ __forceinline__ void griddep() {
 // block input, or h four launches before the last reduction).
 
 __global__ void __launch_bounds__(kThreads, 3) k_reduce_qkv(const ReduceArgs r) {
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
     const bool live = idx < r.M * F4;
     const int n = live ? idx / F4 : 0, f0 = live ? (idx - n * F4) * 4 : 0;
     Qkv4 p{};
     if (live) p = epi4_qkv_prepare(r.e, n, f0);
-    griddep();
+    TRACE(const unsigned long long tr1 =) griddep();
     if (!live) return;
     float4 s, unused;
     seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
     epi4_qkv_apply(p, s);
+    TRACE(trace_cta(TR_REDUCE_QKV, tr0, tr1);)
 }
 
 __global__ void __launch_bounds__(kThreads, 4) k_reduce_resid(const ReduceArgs r) {
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
     const bool live = idx < r.M * F4;
@@ -53,15 +59,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_resid(const ReduceArgs r
     const size_t off = (size_t)n * r.F + f0;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) x = load4_bf16(r.e.resid + off);
-    griddep();
+    TRACE(const unsigned long long tr1 =) griddep();
     if (!live) return;
     float4 s, unused;
     seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, off, 0, s, unused);
     epi4_resid(r.e, r.F, n, f0, x, s);
+    TRACE(trace_cta(TR_REDUCE_RESID, tr0, tr1);)
 }
 
 __global__ void __launch_bounds__(kThreads, 3) k_reduce_swiglu(const ReduceArgs r) {
-    griddep();
+    TRACE(const unsigned long long tr0 = trace_stamp();)
+    TRACE(const unsigned long long tr1 =) griddep();
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
     if (idx >= r.M * F4) return;
@@ -71,6 +79,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_reduce_swiglu(const ReduceArgs 
     float4 g, u;
     seg_sum4<true, 4>(r.partial, 2 * plane, r.n_segs, off, plane + off, g, u);
     epi4_swiglu(r.e, r.F, n, f0, g, u);
+    TRACE(trace_cta(TR_REDUCE_SWIGLU, tr0, tr1);)
 }
 
 // h = resid epilogue, then RMSNorm(h), one cluster of S CTAs per token row: CTA c
@@ -98,6 +107,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_resid_norm(const ReduceArgs
                                                                 bf16* __restrict__ hn, float eps) {
     __shared__ float red[8];
     __shared__ float slice_sum[S];
+    TRACE(const unsigned long long tr0 = trace_stamp();)
     const int c = (int)cluster_ctarank(), n = blockIdx.y, tid = threadIdx.x;
     const int d = r.F;
     const size_t plane = (size_t)r.M * r.F;
@@ -107,7 +117,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_resid_norm(const ReduceArgs
     const float x0 = __bfloat162float(__ldcg(r.e.resid + row + i0));
     const float x1 = __bfloat162float(__ldcg(r.e.resid + row + i1));
     const float g0 = __bfloat162float(gain[i0]), g1 = __bfloat162float(gain[i1]);
-    griddep();
+    TRACE(const unsigned long long tr1 =) griddep();
     float a0 = -0.f, a1 = -0.f;   // -0 + x == x: the sums equal ((s0 + s1) + s2) + ...
     for (int s0 = 0; s0 < r.n_segs; s0 += 8) {
         float w0[8], w1[8];
@@ -138,11 +148,14 @@ __global__ void __launch_bounds__(kThreads) k_reduce_resid_norm(const ReduceArgs
     const float scale = rms_scale(total, d, eps);
     hn[row + i0] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h0, scale)), g0));
     hn[row + i1] = __float2bfloat16_rn(__fmul_rn(bf16_round(__fmul_rn(h1, scale)), g1));
+    TRACE(trace_cta(TR_REDUCE_RESID_NORM, tr0, tr1);)
 }
 
 dim3 grid4(const ReduceArgs& r) { return dim3((unsigned)(((size_t)r.M * (r.F / 4) + kThreads - 1) / kThreads)); }
 
 }  // namespace
+
+LLAMA_TRACE_UNIT(reduce)
 
 cudaError_t launch_reduce(const ReduceArgs& r, int kind, cudaStream_t s) {
     if (r.M <= 0) return cudaSuccess;

@@ -203,6 +203,35 @@ int llama_block_decode_seqpos(llama_block blk, const void* x, int batch, const l
  * LLAMA_ERR_POS_RANGE). */
 int llama_block_poll_error(llama_block blk, void* stream);
 
+/* Per-CTA timeline of the block's kernels (RMSNorm, the projections, their
+ * reductions, RoPE, attention and its combine), in the trace build of the
+ * library (libllama_block_trace.so, the same sources compiled with
+ * LLAMA_TRACE); the product library returns LLAMA_ERR_UNSUPPORTED_DIMS from
+ * llama_trace_begin and carries no tracing code in its kernels.  Between
+ * llama_trace_begin and llama_trace_end every CTA of those kernels claims one
+ * record with an atomic
+ * increment of *count and, while the index is below `capacity`, writes four
+ * uint64 words at records[4 * index]:
+ *   [0] kernel id (bits 0..7: 1 RMSNorm, 2 weight-streaming projection, 3
+ *       token-tiled projection, 4..7 the QKV / residual / SwiGLU / residual +
+ *       RMSNorm reductions, 8 decode attention, 9 its combine, 10 prefill
+ *       attention, 11 RoPE, 12 wide-group decode attention; bits 8..15 the
+ *       projection's epilogue: 0 QKV, 1 residual, 2 SwiGLU, 4 logits),
+ *       bits 16..31 the SM, bits 32..63 the CTA's linear index;
+ *   [1] %globaltimer (ns) when the CTA started;
+ *   [2] when its grid-dependency wait returned (0 if that CTA's recording
+ *       thread does not wait);
+ *   [3] when the CTA's thread 0 finished.
+ * records (capacity x 32 bytes) and count (zeroed by the caller) are device
+ * memory owned by the caller and must stay valid until llama_trace_end.  The
+ * setting is process-wide and applies to kernels that run after the call
+ * (graph replays included); with it on, each CTA reads it from the constant
+ * bank at its start (a traced step runs about 3 us longer).  Returns LLAMA_OK,
+ * LLAMA_ERR_INVALID_ARG, LLAMA_ERR_CUDA or (product build)
+ * LLAMA_ERR_UNSUPPORTED_DIMS. */
+int llama_trace_begin(unsigned long long* records, unsigned int* count, unsigned int capacity);
+int llama_trace_end(void);
+
 /* Failure-path self-test.  Launches on `stream` one warp that waits, through the
  * same bounded mbarrier wait every tensor-core kernel of the library uses, on a
  * barrier nothing arrives on.  After budget_ns nanoseconds (0 or more than 2 s:
