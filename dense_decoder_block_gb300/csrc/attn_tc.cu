@@ -172,6 +172,64 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
                  : "memory");
 }
 
+// Eight K = 16 steps of one accumulator chain from a single asm block.  Step ks's
+// descriptors are step 0's plus the step's byte offset / 16 in the start-address
+// field (shared-memory addresses stay below 256 KB, so the 14-bit field never
+// carries: the same descriptors the per-step helpers build), the accumulate
+// predicate off for step 0 and on after.  The issuing thread shares its scheduler
+// with softmax and fold warps; this keeps its instructions per MMA few.
+//
+// Both operands K-major from shared memory in two 64-column sub-tiles (16 KB
+// apart): step ks at (ks / 4) * 16 KB + (ks % 4) * 32 bytes.
+__device__ __forceinline__ void umma8_ss_kmajor(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a<8>, b<8>;\n\t"
+        "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+        "add.s64 a2, %1, 4;\n\tadd.s64 b2, %2, 4;\n\t"
+        "add.s64 a3, %1, 6;\n\tadd.s64 b3, %2, 6;\n\t"
+        "add.s64 a4, %1, 1024;\n\tadd.s64 b4, %2, 1024;\n\t"
+        "add.s64 a5, %1, 1026;\n\tadd.s64 b5, %2, 1026;\n\t"
+        "add.s64 a6, %1, 1028;\n\tadd.s64 b6, %2, 1028;\n\t"
+        "add.s64 a7, %1, 1030;\n\tadd.s64 b7, %2, 1030;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, pt;\n\t"
+        "}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc)
+        : "memory");
+}
+// A from tensor memory (step ks 8 columns on: 16 bf16 per row), B MN-major from
+// shared memory (step ks 16 rows = 2048 bytes on).
+__device__ __forceinline__ void umma8_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 t<8>;\n\t.reg .b64 b<8>;\n\t"
+        "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+        "add.u32 t1, %1, 8;\n\tadd.s64 b1, %2, 128;\n\t"
+        "add.u32 t2, %1, 16;\n\tadd.s64 b2, %2, 256;\n\t"
+        "add.u32 t3, %1, 24;\n\tadd.s64 b3, %2, 384;\n\t"
+        "add.u32 t4, %1, 32;\n\tadd.s64 b4, %2, 512;\n\t"
+        "add.u32 t5, %1, 40;\n\tadd.s64 b5, %2, 640;\n\t"
+        "add.u32 t6, %1, 48;\n\tadd.s64 b6, %2, 768;\n\t"
+        "add.u32 t7, %1, 56;\n\tadd.s64 b7, %2, 896;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], b1, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], b2, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], b3, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t4], b4, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t5], b5, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t6], b6, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], b7, %3, pt;\n\t"
+        "}"
+        ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc)
+        : "memory");
+}
+
 // D += A . B with A (M = 128 rows x K = 16, bf16 pairs packed in 8 columns, row =
 // lane) read from tensor memory and B from shared memory.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -655,19 +713,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         } else if (warp == 1) {
             // ------------------------------------------------------------------ MMA issuer
             if (lane == 0) {
-                const uint32_t q_addr = ptx::smem_u32(sm + PF_OFF_Q);
+                const uint64_t q_desc = ptx::sw128_kmajor_desc(ptx::smem_u32(sm + PF_OFF_Q));
                 auto issue_s = [&](int i) -> bool {
                     const int k = i & 1;
                     if (!ptx::mbar_wait(&k_full[k], (i >> 1) & 1, err)) return false;
                     if (i >= 2 && !ptx::mbar_wait(&s_free[k], ((i >> 1) & 1) ^ 1, err)) return false;
                     ptx::tc_fence_after();
                     const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
-                        ptx::umma_bf16(tmem + PF_TM_S + k * 128, ptx::sw128_kmajor_desc(q_addr + off),
-                                       ptx::sw128_kmajor_desc(k_addr + off), IDESC_S, ks > 0 ? 1u : 0u);
-                    }
+                    umma8_ss_kmajor(tmem + PF_TM_S + k * 128, q_desc, ptx::sw128_kmajor_desc(k_addr), IDESC_S);
                     ptx::umma_commit(&s_full[k]);
                     ptx::umma_commit(&k_empty[k]);
                     return true;
@@ -682,10 +735,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err)) break;
                     ptx::tc_fence_after();
                     const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + k * 2 * kSub);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)   // P of keys 16ks.. in TMEM columns 8ks..
-                        umma_bf16_ts(tmem + PF_TM_OC + k * 128, tmem + PF_TM_S + k * 128 + ks * 8,
-                                     ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
+                    // P of keys 16ks.. in TMEM columns 8ks.., V rows 16ks..
+                    umma8_ts(tmem + PF_TM_OC + k * 128, tmem + PF_TM_S + k * 128, ptx::sw128_mnmajor_desc(v_addr, kSub),
+                             IDESC_PV);
                     ptx::umma_commit(&oc_full[k]);
                     ptx::umma_commit(&v_empty[k]);
                     if (i + 2 < n_iter) ok = issue_s(i + 2);
