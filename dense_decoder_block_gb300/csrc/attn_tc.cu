@@ -124,16 +124,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 //   l   = ((L0 + L1) + L2) + L3,  Lq = sum of p_j over keys 32q..32q+31 in key order
 // The P row goes to the two 64-key sub-tiles of the swizzled K-major P operand
 // (p_sub_stride bytes apart) at row `prow`.
-__device__ __forceinline__ float softmax_p(float s, float scale_log2, float m) {
-    return ex2(__fmaf_rn(s, scale_log2, -m));
-}
 template <int N>
 __device__ __forceinline__ void softmax_keys(const float* sv, int j0, int jmax, float scale_log2, float m,
                                              uint32_t* packed, float& lq) {
     const uint64_t c2 = pack2(scale_log2, scale_log2), nm2 = pack2(-m, -m);
 #pragma unroll
     for (int j = 0; j < N; j += 2) {
-        float x0, x1;   // fma(s, c, -m) for the pair, as softmax_p forms it
+        float x0, x1;   // fma(S_j, c, -m) for the pair
         unpack2(fma2(pack2(sv[j], sv[j + 1]), c2, nm2), x0, x1);
         const float p0 = (j0 + j <= jmax) ? ex2(x0) : 0.f;
         const float p1 = (j0 + j + 1 <= jmax) ? ex2(x1) : 0.f;
@@ -227,18 +224,6 @@ __device__ __forceinline__ void umma8_ts(uint32_t d, uint32_t a_tmem, uint64_t b
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], b7, %3, pt;\n\t"
         "}"
         ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc)
-        : "memory");
-}
-
-// D += A . B with A (M = 128 rows x K = 16, bf16 pairs packed in 8 columns, row =
-// lane) read from tensor memory and B from shared memory.
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
