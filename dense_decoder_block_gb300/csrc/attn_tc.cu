@@ -466,18 +466,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   warp 0       TMA: the Q tile once, then K chunks through a two-stage ring
 //   warp 2       TMA: V chunks through a two-stage ring (K(i+2) loads once S(i)
 //                has read K(i); V(i+2) once PV(i) has read V(i))
-//   warp 1       TMEM owner + MMA: PV(i) into O_c[i % 2] with P read from
-//                TMEM, then S(i+2) = Q K^T into the S buffer that chunk i used
-//                (S and O_c are both double-buffered in TMEM)
+//   warp 1       TMEM owner + MMA: PV(i) into O_c with P read from TMEM, then
+//                S(i+3) = Q K^T into the S buffer that chunk i used (three S
+//                buffers, one O_c)
 //   warps 4-11   softmax of every chunk, two threads per row: warps 4-7 take
 //                keys 0..63 and warps 8-11 keys 64..127 of the rows of their
 //                TMEM lane quarter, exchanging the row max and two quarter sums
 //                through shared memory; P (bf16 pairs) overwrites the first 64
 //                columns of the S row once both halves hold their scores, the
-//                row's (m, l) goes to columns 64, 65.  (One warpgroup per chunk
-//                on alternate chunks, thread = row, gave the same chunk time: it
-//                is set by the chain softmax -> PV -> fold -> next S, not by one
-//                warp's softmax.)
+//                row's (m, l) goes to columns 64, 65.
 //   warps 12-15  fold of every chunk into the running (O, M, L), thread = row,
 //                with the row's O in registers; then o = O * (1 / L)
 // Warp 3 only keeps the roles aligned to warpgroups.  A chunk that is wholly
@@ -498,7 +495,12 @@ constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
 constexpr int PF_OFF_BAR = PF_OFF_V + 4 * kSub;
 constexpr int PF_OFF_XCH = PF_OFF_BAR + 256;         // softmax halves' exchange: 4 x 128 floats
 constexpr int PF_SMEM_BYTES = PF_OFF_XCH + 2048 + 1024;
-constexpr int PF_TM_S = 0, PF_TM_OC = 256;   // S[parity] at 0 / 128, O_c[parity] at 256 / 384
+// S[i % 3] at columns 0 / 128 / 256, O_c at 384: three S buffers let S(i + 3) be
+// issued behind PV(i), so the softmax works up to two chunks ahead of the MMAs
+// that feed it; O_c needs one buffer, since the fold reads it before the softmax
+// of the next chunk has finished.
+constexpr int kPfSBufs = 3;
+constexpr int PF_TM_S = 0, PF_TM_OC = 384;
 // In S[parity], the softmax leaves P (bf16 pairs) in columns 0..63 and the row's
 // (m, l) in columns 64, 65.
 constexpr int PF_TM_ML = 64;
@@ -604,12 +606,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint64_t* k_empty = bars + 3;    // [2] MMA (after S) -> TMA
     uint64_t* v_full = bars + 5;     // [2] TMA -> MMA (and the softmax, before it zeroes rows)
     uint64_t* v_empty = bars + 7;    // [2] MMA (after PV) -> TMA
-    uint64_t* s_full = bars + 9;     // [2] MMA (after S) -> softmax
-    uint64_t* p_full = bars + 11;    // [2] softmax (P, m, l written) -> MMA, fold
-    uint64_t* s_free = bars + 13;    // [2] fold (m, l read) -> MMA
-    uint64_t* oc_full = bars + 15;   // [2] MMA (after PV) -> fold
-    uint64_t* oc_free = bars + 17;   // [2] fold (O_c read) -> MMA
-    uint32_t* tmem_holder = (uint32_t*)(bars + 19);
+    uint64_t* s_full = bars + 9;     // [3] MMA (after S) -> softmax
+    uint64_t* p_full = bars + 12;    // [3] softmax (P, m, l written) -> MMA, fold
+    uint64_t* s_free = bars + 15;    // [3] fold (m, l read) -> MMA
+    uint64_t* oc_full = bars + 18;   // MMA (after PV) -> fold
+    uint64_t* oc_free = bars + 19;   // fold (O_c read) -> MMA
+    uint32_t* tmem_holder = (uint32_t*)(bars + 20);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
@@ -637,12 +639,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ptx::mbar_init(&k_empty[i], 1);
             ptx::mbar_init(&v_full[i], 1);
             ptx::mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < kPfSBufs; ++i) {
             ptx::mbar_init(&s_full[i], 1);
             ptx::mbar_init(&p_full[i], 8);
             ptx::mbar_init(&s_free[i], 4);
-            ptx::mbar_init(&oc_full[i], 1);
-            ptx::mbar_init(&oc_free[i], 4);
         }
+        ptx::mbar_init(oc_full, 1);
+        ptx::mbar_init(oc_free, 4);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -699,33 +703,35 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             // ------------------------------------------------------------------ MMA issuer
             if (lane == 0) {
                 const uint64_t q_desc = ptx::sw128_kmajor_desc(ptx::smem_u32(sm + PF_OFF_Q));
+                // S(i) into S[i % 3]: K(i) landed, and the fold has read chunk i - 3's (m, l)
+                // from that buffer (PV(i - 3), which read its P, was issued before and the
+                // MMAs run in issue order)
                 auto issue_s = [&](int i) -> bool {
-                    const int k = i & 1;
+                    const int k = i & 1, sb = i % kPfSBufs;
                     if (!ptx::mbar_wait(&k_full[k], (i >> 1) & 1, err)) return false;
-                    if (i >= 2 && !ptx::mbar_wait(&s_free[k], ((i >> 1) & 1) ^ 1, err)) return false;
+                    if (i >= kPfSBufs && !ptx::mbar_wait(&s_free[sb], ((i / kPfSBufs) & 1) ^ 1, err)) return false;
                     ptx::tc_fence_after();
                     const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
-                    umma8_ss_kmajor(tmem + PF_TM_S + k * 128, q_desc, ptx::sw128_kmajor_desc(k_addr), IDESC_S);
-                    ptx::umma_commit(&s_full[k]);
+                    umma8_ss_kmajor(tmem + PF_TM_S + sb * 128, q_desc, ptx::sw128_kmajor_desc(k_addr), IDESC_S);
+                    ptx::umma_commit(&s_full[sb]);
                     ptx::umma_commit(&k_empty[k]);
                     return true;
                 };
                 bool ok = ptx::mbar_wait(q_full, 0, err);
-                if (ok) ok = issue_s(0);
-                if (ok && n_iter > 1) ok = issue_s(1);
+                for (int i = 0; i < kPfSBufs && i < n_iter && ok; ++i) ok = issue_s(i);
                 for (int i = 0; i < n_iter && ok; ++i) {
-                    const int k = i & 1;
-                    if (!ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err)) break;
-                    if (i >= 2 && !ptx::mbar_wait(&oc_free[k], ((i >> 1) & 1) ^ 1, err)) break;
+                    const int k = i & 1, sb = i % kPfSBufs;
+                    if (!ptx::mbar_wait(&p_full[sb], (i / kPfSBufs) & 1, err)) break;
+                    // O_c is overwritten once the fold has read chunk i - 1's
+                    if (i >= 1 && !ptx::mbar_wait(oc_free, (i - 1) & 1, err)) break;
                     if (!ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err)) break;
                     ptx::tc_fence_after();
                     const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + k * 2 * kSub);
                     // P of keys 16ks.. in TMEM columns 8ks.., V rows 16ks..
-                    umma8_ts(tmem + PF_TM_OC + k * 128, tmem + PF_TM_S + k * 128, ptx::sw128_mnmajor_desc(v_addr, kSub),
-                             IDESC_PV);
-                    ptx::umma_commit(&oc_full[k]);
+                    umma8_ts(tmem + PF_TM_OC, tmem + PF_TM_S + sb * 128, ptx::sw128_mnmajor_desc(v_addr, kSub), IDESC_PV);
+                    ptx::umma_commit(oc_full);
                     ptx::umma_commit(&v_empty[k]);
-                    if (i + 2 < n_iter) ok = issue_s(i + 2);
+                    if (i + kPfSBufs < n_iter) ok = issue_s(i + kPfSBufs);
                 }
             }
         }
@@ -742,14 +748,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         float* xch = reinterpret_cast<float*>(sm + PF_OFF_XCH);
         bool ok = true;
         for (int i = 0; i < n_iter; ++i) {
-            const int k = i & 1;
-            // s_full(i) also means PV(i - 2) -- issued before S(i) -- is done with P[k]
-            if (ok) ok = ptx::mbar_wait(&s_full[k], (i >> 1) & 1, err);
+            const int k = i & 1, sb = i % kPfSBufs;
+            // s_full(i) also means PV(i - 3) -- issued before S(i) -- is done with the P in S[sb]
+            if (ok) ok = ptx::mbar_wait(&s_full[sb], (i / kPfSBufs) & 1, err);
             ptx::tc_fence_after();
             const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
             float m;
             // both halves reach the two barriers inside on every chunk, whatever `ok` says
-            softmax_half_tmem(tmem + lane_addr + PF_TM_S + k * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, m);
+            softmax_half_tmem(tmem + lane_addr + PF_TM_S + sb * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, m);
             if (h == 0) {
                 // value rows past the last visible key of this tile are zeroed (they may hold
                 // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
@@ -768,7 +774,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&p_full[k]);
+            if (lane == 0) ptx::mbar_arrive(&p_full[sb]);
         }
     } else {
         // ------------------------------------------------------------------ fold + output
@@ -783,17 +789,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         bool started = false, ok = true;
 #pragma unroll 1
         for (int i = 0; i < n_iter; ++i) {
-            const int k = i & 1;
-            if (ok) ok = ptx::mbar_wait(&p_full[k], (i >> 1) & 1, err);
+            const int sb = i % kPfSBufs;
+            if (ok) ok = ptx::mbar_wait(&p_full[sb], (i / kPfSBufs) & 1, err);
             ptx::tc_fence_after();
             float ml[2];
-            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + k * 128 + PF_TM_ML, ml);
+            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + sb * 128 + PF_TM_ML, ml);
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s_free[k]);
+            if (lane == 0) ptx::mbar_arrive(&s_free[sb]);
             const float m = ml[0], l = ml[1];
-            if (ok) ok = ptx::mbar_wait(&oc_full[k], (i >> 1) & 1, err);
+            if (ok) ok = ptx::mbar_wait(oc_full, i & 1, err);
             ptx::tc_fence_after();
             // Per row: skip a chunk with no visible key, start from the first one, fold the
             // rest (the combine kernel's formula).  The TMEM loads are issued by the whole
@@ -811,16 +817,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 M = m;
                 L = l;
             }
-            const uint32_t oc_addr = tmem + lane_addr + PF_TM_OC + k * 128;
+            const uint32_t oc_addr = tmem + lane_addr + PF_TM_OC;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 float oc[32];
                 ptx::tmem_ld<32>(oc_addr + cb * 32, oc);
                 ptx::tmem_wait_ld();
-                if (cb == 3) {   // O_c[k] fully read: PV(i + 2) may overwrite it
+                if (cb == 3) {   // O_c fully read: PV(i + 1) may overwrite it
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&oc_free[k]);
+                    if (lane == 0) ptx::mbar_arrive(oc_free);
                 }
                 if (fold) {   // o = fma(o, alpha, oc * beta), two columns per instruction
                     const uint64_t a2 = pack2(alpha, alpha), b2 = pack2(beta, beta);
