@@ -176,19 +176,23 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
 // predicate off for step 0 and on after.  The issuing thread shares its scheduler
 // with softmax and fold warps; this keeps its instructions per MMA few.
 //
-// Both operands K-major from shared memory in two 64-column sub-tiles (16 KB
-// apart): step ks at (ks / 4) * 16 KB + (ks % 4) * 32 bytes.
-__device__ __forceinline__ void umma8_ss_kmajor(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+// Both operands from shared memory.  A is K-major in two 64-column sub-tiles
+// A_SUB16 x 16 bytes apart (step ks at (ks / 4) sub-tiles + (ks % 4) * 32 bytes);
+// B likewise with B_SUB16, or MN-major (B_MN: step ks 16 rows = 2048 bytes on).
+template <int A_SUB16, int B_SUB16, bool B_MN>
+__device__ __forceinline__ void umma8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+#define LLAMA_AOFF(ks) ((ks) / 4 * A_SUB16 + (ks) % 4 * 2)
+#define LLAMA_BOFF(ks) (B_MN ? (ks) * 128 : (ks) / 4 * B_SUB16 + (ks) % 4 * 2)
     asm volatile(
         "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a<8>, b<8>;\n\t"
         "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
-        "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
-        "add.s64 a2, %1, 4;\n\tadd.s64 b2, %2, 4;\n\t"
-        "add.s64 a3, %1, 6;\n\tadd.s64 b3, %2, 6;\n\t"
-        "add.s64 a4, %1, 1024;\n\tadd.s64 b4, %2, 1024;\n\t"
-        "add.s64 a5, %1, 1026;\n\tadd.s64 b5, %2, 1026;\n\t"
-        "add.s64 a6, %1, 1028;\n\tadd.s64 b6, %2, 1028;\n\t"
-        "add.s64 a7, %1, 1030;\n\tadd.s64 b7, %2, 1030;\n\t"
+        "add.s64 a1, %1, %4;\n\tadd.s64 b1, %2, %11;\n\t"
+        "add.s64 a2, %1, %5;\n\tadd.s64 b2, %2, %12;\n\t"
+        "add.s64 a3, %1, %6;\n\tadd.s64 b3, %2, %13;\n\t"
+        "add.s64 a4, %1, %7;\n\tadd.s64 b4, %2, %14;\n\t"
+        "add.s64 a5, %1, %8;\n\tadd.s64 b5, %2, %15;\n\t"
+        "add.s64 a6, %1, %9;\n\tadd.s64 b6, %2, %16;\n\t"
+        "add.s64 a7, %1, %10;\n\tadd.s64 b7, %2, %17;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, pt;\n\t"
@@ -197,9 +201,13 @@ __device__ __forceinline__ void umma8_ss_kmajor(uint32_t d, uint64_t a, uint64_t
         "tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, pt;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, pt;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, pt;\n\t"
-        "}"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc)
+        "}" ::"r"(d), "l"(a), "l"(b), "r"(idesc),
+        "n"(LLAMA_AOFF(1)), "n"(LLAMA_AOFF(2)), "n"(LLAMA_AOFF(3)), "n"(LLAMA_AOFF(4)), "n"(LLAMA_AOFF(5)),
+        "n"(LLAMA_AOFF(6)), "n"(LLAMA_AOFF(7)), "n"(LLAMA_BOFF(1)), "n"(LLAMA_BOFF(2)), "n"(LLAMA_BOFF(3)),
+        "n"(LLAMA_BOFF(4)), "n"(LLAMA_BOFF(5)), "n"(LLAMA_BOFF(6)), "n"(LLAMA_BOFF(7))
         : "memory");
+#undef LLAMA_AOFF
+#undef LLAMA_BOFF
 }
 // A from tensor memory (step ks 8 columns on: 16 bf16 per row), B MN-major from
 // shared memory (step ks 16 rows = 2048 bytes on).
@@ -712,7 +720,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (i >= kPfSBufs && !ptx::mbar_wait(&s_free[sb], ((i / kPfSBufs) & 1) ^ 1, err)) return false;
                     ptx::tc_fence_after();
                     const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
-                    umma8_ss_kmajor(tmem + PF_TM_S + sb * 128, q_desc, ptx::sw128_kmajor_desc(k_addr), IDESC_S);
+                    umma8_ss<kSub / 16, kSub / 16, false>(tmem + PF_TM_S + sb * 128, q_desc,
+                                                          ptx::sw128_kmajor_desc(k_addr), IDESC_S);
                     ptx::umma_commit(&s_full[sb]);
                     ptx::umma_commit(&k_empty[k]);
                     return true;
@@ -1117,10 +1126,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
                 const uint32_t p_addr = ptx::smem_u32(sm + D_OFF_P + slot * 2048);
                 if (!ptx::mbar_wait(&v_full[st], (j / kDecStagesV) & 1, err)) return false;
                 const uint32_t v_addr = ptx::smem_u32(sm + D_OFF_V + st * 2 * kSub);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    ptx::umma_bf16(tmem + slot * 128, sw128_kmajor_desc_rows8(p_addr + (ks >> 2) * 1024 + (ks & 3) * 32),
-                                   ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
+                umma8_ss<1024 / 16, 0, true>(tmem + slot * 128, sw128_kmajor_desc_rows8(p_addr),
+                                             ptx::sw128_mnmajor_desc(v_addr, kSub), IDESC_PV);
                 ptx::umma_commit(&o_full[slot]);
                 ptx::umma_commit(&v_empty[st]);
                 return true;
@@ -1133,11 +1140,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_attn_tc_dec(const __grid_con
                 ptx::tc_fence_after();
                 const uint32_t q_addr = ptx::smem_u32(sm + D_OFF_Q + slot * 2048);
                 const uint32_t k_addr = ptx::smem_u32(sm + D_OFF_K + st * 2 * kSub);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    ptx::umma_bf16(tmem + slot * 128, sw128_kmajor_desc_rows8(q_addr + (ks >> 2) * 1024 + (ks & 3) * 32),
-                                   ptx::sw128_kmajor_desc(k_addr + (ks >> 2) * kSub + (ks & 3) * 32), IDESC_S,
-                                   ks > 0 ? 1u : 0u);
+                umma8_ss<1024 / 16, kSub / 16, false>(tmem + slot * 128, sw128_kmajor_desc_rows8(q_addr),
+                                                      ptx::sw128_kmajor_desc(k_addr), IDESC_S);
                 ptx::umma_commit(&s_full[slot]);
                 ptx::umma_commit(&k_empty[st]);
                 if (i > 0) ok = issue_pv(i - 1);
