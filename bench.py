@@ -763,7 +763,7 @@ def timeline_stages(rec, order):
 
 def run_timeline(args, rank, world, device):
     """One replayed decode step (the default workload: 8B block, batch 32, pos 1000)
-    and one 2048-token prefill, each traced CTA by CTA (llama_trace_begin, in the
+    and one prefill of --tokens tokens (2048 by default), each traced CTA by CTA (llama_trace_begin, in the
     library's trace build): when each launch's first CTA starts, its last ends and
     its CTAs' durations -- from kernel start, not from the dependency release.  A
     traced step runs a few microseconds longer than the product build's."""
@@ -813,7 +813,7 @@ def run_timeline(args, rank, world, device):
     del graph, blk, kv, w
     torch.cuda.empty_cache()
 
-    T = 2048
+    T = args.tokens
     pinp = workloads.make_block_inputs(dims, 1, T, max_seq=T, weights=wts)
     w = {k: v.to(device) for k, v in pinp.weights.items()}
     g = {k: v.to(device) for k, v in pinp.gains.items()}
@@ -827,11 +827,13 @@ def run_timeline(args, rank, world, device):
     torch.cuda.synchronize(device)
     prefill_order = [("rmsnorm_1", 1), ("qkv", 3), ("rope", 11), ("attention", 10), ("o_proj", 3 | 1 << 8),
                      ("rmsnorm_2", 1), ("gate_up", 3 | 2 << 8), ("down", 3 | 1 << 8)]
+    if pblk.launch_count() > len(prefill_order):   # few tokens: the down projection split, then its reduction
+        prefill_order.append(("down_reduce", 5))
     with ddb.Trace(1 << 16, device) as tr:
         pblk.prefill(px, pkv, py, pws)
         torch.cuda.synchronize(device)
     assert pblk.poll_error() == 0
-    res["prefill_8b_t2048"] = timeline_stages(tr.records(), prefill_order)
+    res[f"prefill_8b_t{T}"] = timeline_stages(tr.records(), prefill_order)
     return res
 
 
@@ -988,7 +990,7 @@ def main():
                          "stack: 32 blocks + embedding + LM head, prefill then greedy decode; survey: one call of "
                          "each other kernel family, for a per-kernel profile; timeline: one decode step and one "
                          "prefill traced CTA by CTA")
-    ap.add_argument("--tokens", type=int, default=2048, help="prefill tokens (with --workload prefill)")
+    ap.add_argument("--tokens", type=int, default=2048, help="prefill tokens (with --workload prefill or timeline)")
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     args = ap.parse_args()

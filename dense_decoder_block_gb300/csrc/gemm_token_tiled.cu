@@ -46,12 +46,13 @@ static cudaError_t dispatch_tt(const GemmProblem& p, const GemmKArgs& ka, const 
 }
 
 // Token-block width of a single-accumulator projection: 256 (the higher
-// arithmetic intensity per loaded byte) unless 128-token tiles give a clearly
-// shorter schedule -- waves of tiles over the SMs times the tile's MMA length,
-// at least 20% shorter -- as when 256-token tiles would leave SMs idle (few
-// tokens); a few percent of span does not pay for the lower intensity (QKV at
-// 8192 tokens measured 1001 TFLOP/s at 128 against 1226 at 256).  The
-// per-element result does not depend on the width.
+// arithmetic intensity per loaded byte) unless 192- or 128-token tiles give a
+// clearly shorter schedule -- waves of tiles over the SMs times the tile's MMA
+// length, at least 20% shorter -- as when 256-token tiles would leave SMs idle
+// (few tokens: QKV at 512 tokens has 96 tiles of 256 for 152 SMs, 144 of 192);
+// a few percent of span does not pay for the lower intensity (QKV at 8192
+// tokens measured 1001 TFLOP/s at 128 against 1226 at 256).  The per-element
+// result does not depend on the width.
 static int tt_width(const GemmProblem& p) {
     const long n_sm = device_sm_count();
     const long ft = p.F / kTileF;
@@ -59,7 +60,10 @@ static int tt_width(const GemmProblem& p) {
         const long tiles = ft * ((p.M + bn - 1) / bn);
         return ((tiles + n_sm - 1) / n_sm) * bn;
     };
-    return 5 * span(128) <= 4 * span(256) ? 128 : 256;
+    const long s256 = span(256), s192 = span(192), s128 = span(128);
+    if (5 * s128 <= 4 * s256 && s128 <= s192) return 128;
+    if (5 * s192 <= 4 * s256) return 192;
+    return 256;
 }
 
 cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const CUtensorMap& a0,
@@ -69,7 +73,11 @@ cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const 
         return run_tt<128, true, EPI_SWIGLU>(p, ka, a0, a1, a2, x, s);
     }
     if (ka.split) return dispatch_tt<256>(p, ka, a0, a1, a2, x, s);
-    return tt_width(p) == 128 ? dispatch_tt<128>(p, ka, a0, a1, a2, x, s) : dispatch_tt<256>(p, ka, a0, a1, a2, x, s);
+    switch (tt_width(p)) {
+        case 128: return dispatch_tt<128>(p, ka, a0, a1, a2, x, s);
+        case 192: return dispatch_tt<192>(p, ka, a0, a1, a2, x, s);
+        default: return dispatch_tt<256>(p, ka, a0, a1, a2, x, s);
+    }
 }
 
 }  // namespace llama
