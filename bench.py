@@ -828,6 +828,7 @@ def run_timeline(args, rank, world, device):
     prefill_order = [("rmsnorm_1", 1), ("qkv", 3), ("rope", 11), ("attention", 10), ("o_proj", 3 | 1 << 8),
                      ("rmsnorm_2", 1), ("gate_up", 3 | 2 << 8), ("down", 3 | 1 << 8)]
     if pblk.launch_count() > len(prefill_order):   # few tokens: the down projection split, then its reduction
+        prefill_order[-1] = ("down", 3 | 1 << 8 | 1 << 12)
         prefill_order.append(("down_reduce", 5))
     with ddb.Trace(1 << 16, device) as tr:
         pblk.prefill(px, pkv, py, pws)

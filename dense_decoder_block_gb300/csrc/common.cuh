@@ -182,7 +182,7 @@ __device__ __forceinline__ unsigned long long trace_stamp() {
     return (LLAMA_TRACE_ON && threadIdx.x == 0) ? trace_clock() : 0ull;
 }
 // thread 0 of the CTA, at its end: `kernel` is a TraceKernel, optionally with the
-// epilogue kind in bits 8..15
+// epilogue kind in bits 8..11 and bit 12 for a split token-tiled projection
 __device__ __forceinline__ void trace_cta(unsigned int kernel, unsigned long long t_start,
                                           unsigned long long t_release) {
 #ifdef LLAMA_TRACE

@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
-    TRACE(trace_cta(TR_GEMM_TT | (EPI << 8), tr0, *tr_release);)
+    TRACE(trace_cta(TR_GEMM_TT | (EPI << 8) | (a.split ? 1u << 12 : 0u), tr0, *tr_release);)
 }
 
 }  // namespace llama

@@ -215,8 +215,9 @@ int llama_block_poll_error(llama_block blk, void* stream);
  *   [0] kernel id (bits 0..7: 1 RMSNorm, 2 weight-streaming projection, 3
  *       token-tiled projection, 4..7 the QKV / residual / SwiGLU / residual +
  *       RMSNorm reductions, 8 decode attention, 9 its combine, 10 prefill
- *       attention, 11 RoPE, 12 wide-group decode attention; bits 8..15 the
- *       projection's epilogue: 0 QKV, 1 residual, 2 SwiGLU, 4 logits),
+ *       attention, 11 RoPE, 12 wide-group decode attention; bits 8..11 the
+ *       projection's epilogue: 0 QKV, 1 residual, 2 SwiGLU, 4 logits; bit 12
+ *       a token-tiled projection whose K-segments run on separate CTAs),
  *       bits 16..31 the SM, bits 32..63 the CTA's linear index;
  *   [1] %globaltimer (ns) when the CTA started;
  *   [2] when its grid-dependency wait returned (0 if that CTA's recording
