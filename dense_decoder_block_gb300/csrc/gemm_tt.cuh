@@ -210,16 +210,10 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                             ptx::tc_fence_after();
                             const uint32_t sa = ptx::smem_u32(smem + stage * C::STAGE_BYTES);
                             const uint32_t sb = sa + NACC * kABytes;
-#pragma unroll
-                            for (int k = 0; k < kBlockK / 16; ++k) {
-                                const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                                if (DUAL)   // A = tokens, B = gate rows then up rows
-                                    ptx::umma_bf16(d, ptx::sw128_kmajor_desc(sb + 32 * k), ptx::sw128_kmajor_desc(sa + 32 * k),
-                                                   IDESC, accum);
-                                else        // A = weights, B = tokens
-                                    ptx::umma_bf16(d, ptx::sw128_kmajor_desc(sa + 32 * k), ptx::sw128_kmajor_desc(sb + 32 * k),
-                                                   IDESC, accum);
-                            }
+                            if (DUAL)   // A = tokens, B = gate rows then up rows
+                                ptx::umma_kblock(d, ptx::sw128_kmajor_desc(sb), ptx::sw128_kmajor_desc(sa), IDESC, kb > kb0);
+                            else        // A = weights, B = tokens
+                                ptx::umma_kblock(d, ptx::sw128_kmajor_desc(sa), ptx::sw128_kmajor_desc(sb), IDESC, kb > kb0);
                             ptx::umma_commit(&empty[stage]);
                             if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
                         }

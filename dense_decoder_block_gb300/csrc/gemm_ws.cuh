@@ -153,13 +153,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t sa = ptx::smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t sb = sa + NACC * kABytes;
-#pragma unroll
-                    for (int k = 0; k < kBlockK / 16; ++k) {
-                        const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                        const uint64_t bdesc = ptx::sw128_kmajor_desc(sb + 32 * k);
-                        ptx::umma_bf16(d, ptx::sw128_kmajor_desc(sa + 32 * k), bdesc, IDESC, accum);
-                        if (DUAL) ptx::umma_bf16(d + BN, ptx::sw128_kmajor_desc(sa + kABytes + 32 * k), bdesc, IDESC, accum);
-                    }
+                    const uint64_t bdesc = ptx::sw128_kmajor_desc(sb);
+                    ptx::umma_kblock(d, ptx::sw128_kmajor_desc(sa), bdesc, IDESC, kb > kb0);
+                    if (DUAL) ptx::umma_kblock(d + BN, ptx::sw128_kmajor_desc(sa + kABytes), bdesc, IDESC, kb > kb0);
                     ptx::umma_commit(&empty[stage]);
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
                 }

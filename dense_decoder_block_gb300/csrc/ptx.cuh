@@ -158,6 +158,29 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 // D[tmem] (+)= A[smem] * B[smem]^T, both K-major bf16, fp32 accumulate.
+// The four K = 16 steps of one 64-element k-block of K-major operands with
+// 128-byte swizzled rows, from one asm block: step k starts 32 bytes on, which is
+// +2 in the start-address field of both descriptors (shared-memory addresses stay
+// below 256 KB, so the field never carries: the same descriptors as
+// sw128_kmajor_desc(addr + 32 k)).  Step 0 accumulates when accumulate_first is
+// non-zero, steps 1..3 always.  Few instructions per MMA for the issuing thread.
+__device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate_first) {
+    asm volatile(
+        "{\n\t.reg .pred p0, pt;\n\t.reg .b64 a<4>, b<4>;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+        "add.s64 a2, %1, 4;\n\tadd.s64 b2, %2, 4;\n\t"
+        "add.s64 a3, %1, 6;\n\tadd.s64 b3, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, pt;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate_first)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(
