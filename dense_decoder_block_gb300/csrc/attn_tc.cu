@@ -382,22 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ptx::mbar_wait(&kv_full[st], (i >> 1) & 1, err)) break;
                 if (i > 0 && !ptx::mbar_wait(s_empty, (i - 1) & 1, err)) break;
                 ptx::tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
-                    ptx::umma_bf16(tmem + TM_S, ptx::sw128_kmajor_desc(q_addr + off),
-                                   ptx::sw128_kmajor_desc(k_addr + off), IDESC_S, ks > 0 ? 1u : 0u);
-                }
+                umma8_ss<kSub / 16, kSub / 16, false>(tmem + TM_S, ptx::sw128_kmajor_desc(q_addr),
+                                                      ptx::sw128_kmajor_desc(k_addr), IDESC_S);
                 ptx::umma_commit(s_full);
                 if (!ptx::mbar_wait(p_full, i & 1, err)) break;
                 if (i > 0 && !ptx::mbar_wait(oc_empty, (i - 1) & 1, err)) break;
                 ptx::tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t aoff = (ks >> 2) * kSub + (ks & 3) * 32;
-                    ptx::umma_bf16(tmem + TM_OC, ptx::sw128_kmajor_desc(p_addr + aoff),
-                                   ptx::sw128_mnmajor_desc(v_addr + ks * 2048, kSub), IDESC_PV, ks > 0 ? 1u : 0u);
-                }
+                umma8_ss<kSub / 16, 0, true>(tmem + TM_OC, ptx::sw128_kmajor_desc(p_addr),
+                                             ptx::sw128_mnmajor_desc(v_addr, kSub), IDESC_PV);
                 ptx::umma_commit(o_full);
                 ptx::umma_commit(&kv_empty[st]);
             }
