@@ -575,13 +575,11 @@ extern "C" int llama_block_decode_seqpos(llama_block b, const void* x, int batch
     if (!x || !y || !pos_seq || !aligned16(x) || !aligned16(y))
         return fail(b, LLAMA_ERR_INVALID_ARG, "x / y / pos_seq null or x / y not 16-byte aligned");
     const auto& d = b->dims;
-    // The per-sequence positions reach the QKV reduction (RoPE, cache row), the
-    // weight-streaming decode attention and the combine: bf16, up to 8 query heads per
-    // KV head, a QKV projection with a reduction step (more than one K-segment), at
-    // most 32 sequences (the weight-streaming schedule).
+    // The per-sequence positions reach the QKV projection's epilogue (RoPE, cache
+    // row), the weight-streaming decode attention and the combine: bf16, up to 8
+    // query heads per KV head, at most 32 sequences (the weight-streaming schedule).
     if (d.dtype != LLAMA_BF16 || !attention_tc_supported(d.n_heads, d.n_kv_heads, d.head_dim) ||
-        d.n_heads / d.n_kv_heads > 8 || batch > 32 ||
-        !gemm_needs_reduce(problem_qkv(b, batch, nullptr), PATH_AUTO))
+        d.n_heads / d.n_kv_heads > 8 || batch > 32)
         return fail(b, LLAMA_ERR_UNSUPPORTED_DIMS, "per-sequence positions need the bf16 weight-streaming decode path");
     int rc = check_kv(b, kv, batch, 0);
     if (rc != LLAMA_OK) return rc;

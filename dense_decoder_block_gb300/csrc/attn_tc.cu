@@ -506,12 +506,6 @@ constexpr int PF_TM_S = 0, PF_TM_OC = 384;
 constexpr int PF_TM_ML = 64;
 static_assert(PF_SMEM_BYTES <= 232448, "shared memory per CTA");
 
-// Barrier of `n` threads (whole warps) on hardware barrier `id` (1..15; 0 is
-// __syncthreads).  Every participating warp must reach it the same number of times.
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // Prefill softmax of one query row over one 128-key chunk, the keys split over
 // two threads (two warps of the same TMEM lane quarter): half h holds keys
 // 64h .. 64h+63 of the row's S in registers.  It computes exactly the canonical
@@ -548,7 +542,7 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
         mx = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
     }
     xch[h * 128 + row] = mx;
-    named_bar_sync(bar, 64);   // both halves' maxima written, both S halves read
+    ptx::named_bar_sync(bar, 64);   // both halves' maxima written, both S halves read
     const float m = __fmul_rn(fmaxf(xch[row], xch[128 + row]), scale_log2);
     const float m_use = (jmax >= 0) ? m : 0.f;   // a row with no visible key: every p is 0
     if (!full) {
@@ -585,7 +579,7 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
         xch[256 + row] = lq[0];
         xch[384 + row] = lq[1];
     }
-    named_bar_sync(bar, 64);   // L2, L3 written; the maxima read
+    ptx::named_bar_sync(bar, 64);   // L2, L3 written; the maxima read
     if (h == 0) {
         const float l = __fadd_rn(__fadd_rn(__fadd_rn(lq[0], lq[1]), xch[256 + row]), xch[384 + row]);
         ptx::tmem_st2(s_taddr + PF_TM_ML, m, l);

@@ -133,6 +133,10 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
         else { kind = 2; head = tile - a.q_tiles - a.k_tiles; }
         const int T = e.tokens_per_seq;
         const int base = e.pos_dev ? *e.pos_dev : e.start_pos;
+        // sequence bb at index tt; with per-sequence positions (T = 1) sequence bb
+        // is token bb, read only for tokens of the call
+        const int* ps = e.pos_seq;
+        auto pos_at = [&](int bb, int tt) { return ps ? (bb < a.M ? ps[bb] : 0) : base + tt; };
         const int i = row >> 1;
         const bool rope = kind < 2 && !e.rope_later;   // warp-uniform
         // token n0 + j = (sequence b, index t), advanced column by column
@@ -141,7 +145,7 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
         bf16* qp = e.out + (size_t)n0 * q_stride + head * 128 + row;   // kind 0
         bf16* cp = ((kind == 1) ? e.kc : e.vc) + (size_t)head * e.kv_seq * 128 + row;   // kinds 1, 2
         const size_t seq_stride = (size_t)e.n_kv_heads * e.kv_seq * 128;
-        if (!rope && base >= 0 && base + T <= e.max_pos) {
+        if (!rope && !ps && base >= 0 && base + T <= e.max_pos) {
             // Every position of the call is valid and nothing is rotated here: short
             // straight-line stores (bf16(bf16_round(x)) == bf16(x)).  The general
             // loop below would keep a large unrolled body in the instruction cache.
@@ -167,7 +171,7 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
                 int bb = b, tt = t;
 #pragma unroll
                 for (int j = 0; j < CH; ++j) {
-                    const int pos = base + tt;
+                    const int pos = pos_at(bb, tt);
                     const int pc = (pos >= 0 && pos < e.max_pos) ? pos : 0;
                     cs[j] = __ldg(e.cos_tab + (size_t)pc * kRopeMaxPairs + i);
                     sn[j] = __ldg(e.sin_tab + (size_t)pc * kRopeMaxPairs + i);
@@ -176,7 +180,7 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
             }
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
-                const int pos = base + t;
+                const int pos = pos_at(b, t);
                 const bool pos_ok = (pos >= 0) && (pos < e.max_pos);
                 float v = bf16_round(acc[c0 + j]);
                 if (rope) {

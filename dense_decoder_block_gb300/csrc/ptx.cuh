@@ -280,6 +280,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// Barrier of `n` threads (whole warps) on hardware barrier `id` (1..15; 0 is
+// __syncthreads).  Every participating warp must reach it the same number of times.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (TMA, tensor core) once the threads have synchronised.
 __device__ __forceinline__ void fence_proxy_async_smem() {

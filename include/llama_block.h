@@ -191,8 +191,7 @@ int llama_block_decode_devpos(llama_block blk, const void* x, int batch, const l
  * bit, what llama_block_decode at that position gives for it.  Each value must lie
  * in [0, max_seq): otherwise the kernels record LLAMA_ERR_POS_RANGE in the error
  * word, write no cache row and leave y undefined.  Supported for bf16 handles
- * with at most 8 query heads per KV head, batch <= 32, and a QKV projection with
- * more than one K-segment (true for the 8B and 70B shapes); otherwise
+ * with at most 8 query heads per KV head and batch <= 32; otherwise
  * LLAMA_ERR_UNSUPPORTED_DIMS. */
 int llama_block_decode_seqpos(llama_block blk, const void* x, int batch, const llama_kv_cache* kv,
                               const int32_t* pos_seq, void* y, void* workspace, size_t workspace_bytes,

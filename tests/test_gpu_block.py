@@ -361,15 +361,22 @@ def test_host_mapped_x_and_y_match_device_buffers():
         ddb.HostMapped(torch.empty(4))   # not pinned
 
 
-def test_decode_per_sequence_positions_bit_identical_to_prefill():
-    """One decode step with a position per sequence (chunk counts 1, 1, 2, 2 and 3,
-    positions on both sides of chunk edges): every sequence's output row and new
-    cache row equal the prefill rows at its position bit for bit, cache rows past
-    each position are left alone, and an out-of-range position is reported."""
-    pos = [5, 127, 128, 257, 300]
+# 64 query and 32 KV heads: 128 QKV feature tiles, which the decode projection
+# streams in a single K-segment (its epilogue in the projection kernel)
+ONESEG = workloads.BlockDims(d_model=8192, n_heads=64, n_kv_heads=32, head_dim=128, d_ff=1024)
+
+
+@pytest.mark.parametrize("dims,pos", [(MID, [5, 127, 128, 257, 300]), (ONESEG, [3, 130])],
+                         ids=["mid-segment-sums", "one-segment-qkv"])
+def test_decode_per_sequence_positions_bit_identical_to_prefill(dims, pos):
+    """One decode step with a position per sequence (MID: chunk counts 1, 1, 2, 2
+    and 3, positions on both sides of chunk edges; its QKV projection adds two
+    K-segments, ONESEG's streams one): every sequence's output row and new cache
+    row equal the prefill rows at its position bit for bit, cache rows past each
+    position are left alone, and an out-of-range position is reported."""
     B, T_all = len(pos), max(pos) + 1
     max_seq = T_all + 4
-    inp = workloads.make_block_inputs(MID, B, T_all, max_seq=max_seq)
+    inp = workloads.make_block_inputs(dims, B, T_all, max_seq=max_seq)
     blk, ddb = gpu_block(inp, max_seq)
     dev = torch.device("cuda:0")
     kc_pf, vc_pf = inp.k_cache.to(dev), inp.v_cache.to(dev)
@@ -396,10 +403,10 @@ def test_decode_per_sequence_positions_bit_identical_to_prefill():
     x64 = workloads.to_numpy64(inp.x)
     y_ex, k_ex, v_ex = [], [], []
     for b, p in enumerate(pos):
-        kr = np.zeros((1, MID.n_kv_heads, p + 1, MID.head_dim))
+        kr = np.zeros((1, dims.n_kv_heads, p + 1, dims.head_dim))
         vr = np.zeros_like(kr)
         tr = {}
-        ob.block_forward(x64[b:b + 1, :p + 1], w, g, MID, kr, vr, 0, rnd_for(inp.dtype), out_rows=[p], trace=tr)
+        ob.block_forward(x64[b:b + 1, :p + 1], w, g, dims, kr, vr, 0, rnd_for(inp.dtype), out_rows=[p], trace=tr)
         y_ex.append(tr["y_exact"][0, 0])
         k_ex.append(tr["k_exact"][0, :, p])
         v_ex.append(tr["v_exact"][0, :, p])
@@ -409,7 +416,7 @@ def test_decode_per_sequence_positions_bit_identical_to_prefill():
     check_bf16_output(workloads.to_numpy64(torch.stack([vc[b, :, p] for b, p in enumerate(pos)])), np.stack(v_ex),
                       what="per-sequence decode v rows")
     # a position outside the cache is recorded by the kernels
-    bad = torch.tensor([5, 127, max_seq, 257, 300], dtype=torch.int32, device=dev)
+    bad = torch.tensor([max_seq] + pos[1:], dtype=torch.int32, device=dev)
     blk.decode_seqpos(x_dec, kv, bad, y, blk.workspace(B, 1))
     assert blk.poll_error() == ddb.LLAMA_ERR_POS_RANGE
     assert blk.poll_error() == 0
