@@ -273,9 +273,11 @@ __global__ void __launch_bounds__(32) k_attn_decode_combine(const AttnK a) {
     const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
     // The position is set before the step, never by the kernels this one overlaps.
     const int pos = a.pos_seq ? a.pos_seq[b] : base_position(a);
+    // The O projection after this kernel reads only its weights before its own wait:
+    // it may launch at once and take the SMs as the attention CTAs leave them.
+    if (threadIdx.x == 0) ptx_launch_dependents();
     ptx_wait();
     TRACE(const unsigned long long tr1 = trace_stamp();)
-    if (threadIdx.x == 0) ptx_launch_dependents();
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int g = h / n_rep, r = h % n_rep;
     if (pos < 0 || pos >= a.max_pos) return;

@@ -111,15 +111,19 @@ __device__ __forceinline__ float rms_sumsq_slices(const float* v, float* red /* 
 
 // Launch with programmatic stream serialization: the kernel may begin while the
 // previous kernel on the stream drains.  Every kernel of the library calls
-// griddepcontrol.wait before it reads anything an earlier kernel wrote, and lets
-// its own dependents start (griddepcontrol.launch_dependents) only after that
-// wait: so when a kernel starts, the kernel two places earlier and everything
-// before it have completed, and only the immediately preceding kernel may still
-// be running.  Reading data that predecessor did not write before the wait
-// (weights, older KV-cache rows) is therefore safe.  A kernel that allocates
-// tensor memory also triggers only after its allocation: a dependent CTA that
-// started earlier on the same SM could otherwise hold the columns while it
-// waits for this grid.
+// griddepcontrol.wait before it reads anything an earlier kernel wrote; when the
+// wait returns, every earlier kernel has completed (none completes before its own
+// wait returns).  The projection and attention kernels let their dependents start
+// (griddepcontrol.launch_dependents) only after that wait, so a kernel that
+// follows one of them starts only once everything two places back has completed:
+// the reductions read positions, gains and residuals before their wait on that
+// ground.  The row-wise kernels (RMSNorm, RoPE, the segment reductions, the
+// attention combine) trigger before their wait: the kernel after each (a
+// projection or attention) reads only weights, positions and older KV-cache rows
+// before its own wait, none of which a kernel still running writes.  A kernel
+// that allocates tensor memory triggers only after its allocation: a dependent
+// CTA that started earlier on the same SM could otherwise hold the columns while
+// it waits for this grid.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args&&... args) {

@@ -26,9 +26,10 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ 
                                                           T* __restrict__ y, int d, float eps) {
     __shared__ float red[16 * 8];
     TRACE(const unsigned long long tr0 = trace_stamp();)
+    // the projection after RMSNorm reads only its weights before its own wait
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     TRACE(const unsigned long long tr1 = trace_stamp();)
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x, tid = threadIdx.x;
     const T* xr = x + (size_t)row * d;
     T* yr = y + (size_t)row * d;
@@ -161,9 +162,10 @@ __global__ void __launch_bounds__(256) k_rope_inplace(bf16* __restrict__ q, bf16
                                                       const float* __restrict__ cos_tab,
                                                       const float* __restrict__ sin_tab, int* err) {
     TRACE(const unsigned long long tr0 = trace_stamp();)
+    // the prefill attention after RoPE reads nothing before its own wait
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     TRACE(const unsigned long long tr1 = trace_stamp();)
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int per_tok = (n_heads + n_kv_heads) * 16;   // 16 eight-element groups per 128-wide row
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)M * per_tok) return;

@@ -19,18 +19,21 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// returns the time the wait returned (for the optional timeline)
+// Lets the next kernel launch, then waits for the projection.  The trigger comes
+// before the wait: what follows a reduction (attention, a projection, RMSNorm)
+// reads nothing before its own wait that a kernel still running may write, and its
+// CTAs take the SMs as the projection's CTAs leave them instead of after this
+// kernel's release.  Returns the time the wait returned (for the optional timeline).
 __device__ __forceinline__ unsigned long long griddep() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const unsigned long long t = trace_stamp();
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    return t;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    return trace_stamp();
 }
 
 // What a reduction reads before griddepcontrol.wait -- the position, the RoPE
 // tables, gains and the residual input -- is never written by the kernel it
-// overlaps: a kernel of this chain starts only after its predecessor passed its
-// own wait, so everything two or more launches back is complete and visible.
+// overlaps: a reduction starts only after its projection passed its own wait, so
+// everything two or more launches back is complete and visible.
 // The residual of each reduction is produced at least two launches earlier (the
 // block input, or h four launches before the last reduction).
 
