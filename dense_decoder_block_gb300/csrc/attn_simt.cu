@@ -315,6 +315,14 @@ AttnK make_k(const AttnArgs& a) {
 }
 
 template <typename T, int DH>
+cudaError_t combine_launch(const AttnK& k, cudaStream_t s) {
+    auto kern = k_attn_decode_combine<T, DH>;
+    cudaError_t r = kernel_setup_once((const void*)kern, setup_prefer_shared);
+    if (r != cudaSuccess) return r;
+    return launch_pdl(kern, dim3(k.n_heads, k.batch), dim3(32), 0, s, k);
+}
+
+template <typename T, int DH>
 cudaError_t prefill_impl(const AttnArgs& a, cudaStream_t s) {
     AttnK k = make_k(a);
     const int n_rep = a.n_heads / a.n_kv_heads;
@@ -339,12 +347,12 @@ cudaError_t decode_impl(const AttnArgs& a, cudaStream_t s) {
     dim3 grid(a.n_chunks, a.n_kv_heads, a.batch);
     r = launch_pdl(kern, grid, dim3(kThreads), sm, s, k);
     if (r != cudaSuccess) return r;
-    return launch_pdl(k_attn_decode_combine<T, DH>, dim3(a.n_heads, a.batch), dim3(32), 0, s, k);
+    return combine_launch<T, DH>(k, s);
 }
 
 template <typename T, int DH>
 cudaError_t combine_impl(const AttnArgs& a, cudaStream_t s) {
-    return launch_pdl(k_attn_decode_combine<T, DH>, dim3(a.n_heads, a.batch), dim3(32), 0, s, make_k(a));
+    return combine_launch<T, DH>(make_k(a), s);
 }
 
 }  // namespace

@@ -122,6 +122,10 @@ cudaError_t kernel_setup_once(const void* kern, cudaError_t (*setup)(const void*
     return e;
 }
 
+cudaError_t setup_prefer_shared(const void* kern) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
 bool gemm_tt_split(const GemmProblem& p, int path) {
     // A token-tiled projection whose 256-token tiles would keep under 70% of the SMs
     // busy runs its K-segments on separate CTAs (split mode of gemm_tt.cuh) and

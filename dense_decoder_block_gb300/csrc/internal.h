@@ -71,6 +71,10 @@ int device_sm_count();
 // set -- under a process-wide lock, so concurrent first calls do not race.  A
 // failed setup is not recorded and runs again on the next call.
 cudaError_t kernel_setup_once(const void* kern, cudaError_t (*setup)(const void* kern));
+// Setup of a row-wise kernel that uses little or no shared memory: prefer the
+// largest shared-memory carveout, so that an SM running its CTAs can take the CTAs
+// of the projection or attention launched behind it without reconfiguring.
+cudaError_t setup_prefer_shared(const void* kern);
 
 cudaError_t launch_gemm(const GemmProblem& p, const GemmEpi& e, int path, float* partial, cudaStream_t s);
 

@@ -73,21 +73,28 @@ __global__ void __launch_bounds__(kNormThreads) k_rmsnorm(const T* __restrict__ 
     TRACE(trace_cta(TR_RMSNORM, tr0, tr1);)
 }
 
+template <typename K, typename... Args>
+cudaError_t launch_small(K kern, dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+    cudaError_t r = kernel_setup_once((const void*)kern, setup_prefer_shared);
+    if (r != cudaSuccess) return r;
+    return launch_pdl(kern, grid, block, 0, s, args...);
+}
+
 template <typename T>
 cudaError_t rmsnorm_dispatch(const T* x, const T* g, T* y, int rows, int d, float eps, cudaStream_t s) {
     const dim3 grid(rows), block(kNormThreads);
     if (d % kNormThreads == 0) {
         switch (d / kNormThreads) {
-            case 1: return launch_pdl(k_rmsnorm<T, 1>, grid, block, 0, s, x, g, y, d, eps);
-            case 2: return launch_pdl(k_rmsnorm<T, 2>, grid, block, 0, s, x, g, y, d, eps);
-            case 4: return launch_pdl(k_rmsnorm<T, 4>, grid, block, 0, s, x, g, y, d, eps);
-            case 8: return launch_pdl(k_rmsnorm<T, 8>, grid, block, 0, s, x, g, y, d, eps);
-            case 16: return launch_pdl(k_rmsnorm<T, 16>, grid, block, 0, s, x, g, y, d, eps);
-            case 32: return launch_pdl(k_rmsnorm<T, 32>, grid, block, 0, s, x, g, y, d, eps);
+            case 1: return launch_small(k_rmsnorm<T, 1>, grid, block, s, x, g, y, d, eps);
+            case 2: return launch_small(k_rmsnorm<T, 2>, grid, block, s, x, g, y, d, eps);
+            case 4: return launch_small(k_rmsnorm<T, 4>, grid, block, s, x, g, y, d, eps);
+            case 8: return launch_small(k_rmsnorm<T, 8>, grid, block, s, x, g, y, d, eps);
+            case 16: return launch_small(k_rmsnorm<T, 16>, grid, block, s, x, g, y, d, eps);
+            case 32: return launch_small(k_rmsnorm<T, 32>, grid, block, s, x, g, y, d, eps);
             default: break;
         }
     }
-    return launch_pdl(k_rmsnorm<T, 0>, grid, block, 0, s, x, g, y, d, eps);
+    return launch_small(k_rmsnorm<T, 0>, grid, block, s, x, g, y, d, eps);
 }
 
 // fp32 projection: one thread per output, ascending K (the same order for any M).
@@ -346,7 +353,7 @@ cudaError_t launch_rope_inplace(void* q, void* kc, int M, int T, int n_heads, in
     if (M <= 0) return cudaSuccess;
     const long long threads = (long long)M * (n_heads + n_kv_heads) * 16;
     const dim3 grid((unsigned)((threads + 255) / 256));
-    return launch_pdl(k_rope_inplace, grid, dim3(256), 0, s, (bf16*)q, (bf16*)kc, M, T, n_heads, n_kv_heads,
+    return launch_small(k_rope_inplace, grid, dim3(256), s, (bf16*)q, (bf16*)kc, M, T, n_heads, n_kv_heads,
                       kv_seq, start_pos, pos_dev, max_pos, cos_tab, sin_tab, err);
 }
 

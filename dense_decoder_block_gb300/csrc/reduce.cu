@@ -37,7 +37,10 @@ __device__ __forceinline__ unsigned long long griddep() {
 // The residual of each reduction is produced at least two launches earlier (the
 // block input, or h four launches before the last reduction).
 
-__global__ void __launch_bounds__(kThreads, 3) k_reduce_qkv(const ReduceArgs r) {
+// At most 48 registers (five CTAs' worth per SM): two of its CTAs fit beside a
+// CTA of the QKV projection, so all of them start while the projection runs and
+// the attention kernel behind them can launch before the projection ends.
+__global__ void __launch_bounds__(kThreads, 5) k_reduce_qkv(const ReduceArgs r) {
     TRACE(const unsigned long long tr0 = trace_stamp();)
     const int F4 = r.F / 4;
     const int idx = blockIdx.x * kThreads + threadIdx.x;
@@ -48,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_reduce_qkv(const ReduceArgs r) 
     TRACE(const unsigned long long tr1 =) griddep();
     if (!live) return;
     float4 s, unused;
-    seg_sum4<false, 8>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
+    seg_sum4<false, 4>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
     epi4_qkv_apply(p, s);
     TRACE(trace_cta(TR_REDUCE_QKV, tr0, tr1);)
 }
@@ -163,12 +166,12 @@ LLAMA_TRACE_UNIT(reduce)
 cudaError_t launch_reduce(const ReduceArgs& r, int kind, cudaStream_t s) {
     if (r.M <= 0) return cudaSuccess;
     if (r.F % 4) return cudaErrorInvalidValue;
-    switch (kind) {
-        case EPI_QKV: return launch_pdl(k_reduce_qkv, grid4(r), dim3(kThreads), 0, s, r);
-        case EPI_RESID: return launch_pdl(k_reduce_resid, grid4(r), dim3(kThreads), 0, s, r);
-        case EPI_SWIGLU: return launch_pdl(k_reduce_swiglu, grid4(r), dim3(kThreads), 0, s, r);
-        default: return cudaErrorInvalidValue;
-    }
+    auto kern = kind == EPI_QKV ? k_reduce_qkv : kind == EPI_RESID ? k_reduce_resid : kind == EPI_SWIGLU ? k_reduce_swiglu
+                                                                                                     : nullptr;
+    if (!kern) return cudaErrorInvalidValue;
+    cudaError_t e = kernel_setup_once((const void*)kern, setup_prefer_shared);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, grid4(r), dim3(kThreads), 0, s, r);
 }
 
 // The widths whose k_rmsnorm uses the slice definition (d / 256 in {4, 8, 16, 32}).
@@ -179,12 +182,12 @@ bool reduce_resid_norm_supported(int d) {
 template <int S>
 static cudaError_t launch_resid_norm(const ReduceArgs& r, const void* gain, void* hn, float eps, cudaStream_t s) {
     auto kern = k_reduce_resid_norm<S>;
-    if (S > 8) {
-        cudaError_t e = kernel_setup_once((const void*)kern, [](const void* k) {
-            return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        });
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = kernel_setup_once((const void*)kern, [](const void* k) {
+        cudaError_t r = setup_prefer_shared(k);
+        if (r == cudaSuccess && S > 8) r = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, r.M);
     cfg.blockDim = dim3(kThreads);
