@@ -121,10 +121,11 @@ __device__ __forceinline__ void epi_swiglu_row(bf16* dst, const float (&g)[CPT],
 // the arithmetic is epi_store's.
 template <int EPI, int CPT>
 __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int row, int n0, const float (&acc)[CPT],
-                                               const float (&acc_up)[CPT]) {
+                                               const float (&acc_up)[CPT], int n_cols = CPT) {
     const GemmEpi& e = a.e;
     const int f = tile * kTileF + row;
-    const int n_valid = a.M - n0;   // columns j < n_valid are tokens of the call
+    // columns j < n_valid are tokens of the call (and of this thread's n_cols)
+    const int n_valid = min(a.M - n0, n_cols);
     if constexpr (EPI == EPI_QKV) {
         constexpr int CH = CPT < 4 ? CPT : 4;
         int kind, head;
@@ -215,7 +216,7 @@ __device__ __forceinline__ void epi_store_cols(const GemmKArgs& a, int tile, int
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) epi_store<EPI>(a, tile, row, n0 + j, acc[j], acc_up[j], n0 + j < a.M);
+        for (int j = 0; j < CPT; ++j) epi_store<EPI>(a, tile, row, n0 + j, acc[j], acc_up[j], j < n_valid);
     }
 }
 

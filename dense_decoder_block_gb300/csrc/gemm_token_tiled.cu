@@ -51,7 +51,11 @@ static cudaError_t dispatch_tt(const GemmProblem& p, const GemmKArgs& ka, const 
 // length, at least 20% shorter -- as when 256-token tiles would leave SMs idle
 // (few tokens: QKV at 512 tokens has 96 tiles of 256 for 152 SMs, 144 of 192);
 // a few percent of span does not pay for the lower intensity (QKV at 8192
-// tokens measured 1001 TFLOP/s at 128 against 1226 at 256).  The per-element
+// tokens measured 1001 TFLOP/s at 128 against 1226 at 256).  240-token tiles
+// load nearly as much per MMA as 256 and are taken whenever their schedule is
+// shorter at all: at 2048 tokens the 32 feature tiles of O and down make 288
+// tiles of 240 (two waves of 152 SMs, span 480) against 256 of 256 (span 512),
+// and QKV's 48 make three waves either way (720 against 768).  The per-element
 // result does not depend on the width.
 static int tt_width(const GemmProblem& p) {
     const long n_sm = device_sm_count();
@@ -60,9 +64,10 @@ static int tt_width(const GemmProblem& p) {
         const long tiles = ft * ((p.M + bn - 1) / bn);
         return ((tiles + n_sm - 1) / n_sm) * bn;
     };
-    const long s256 = span(256), s192 = span(192), s128 = span(128);
-    if (5 * s128 <= 4 * s256 && s128 <= s192) return 128;
-    if (5 * s192 <= 4 * s256) return 192;
+    const long s256 = span(256), s240 = span(240), s192 = span(192), s128 = span(128);
+    if (5 * s128 <= 4 * s256 && s128 <= s192 && s128 < s240) return 128;
+    if (5 * s192 <= 4 * s256 && s192 < s240) return 192;
+    if (s240 < s256) return 240;
     return 256;
 }
 
@@ -76,6 +81,7 @@ cudaError_t launch_token_tiled(const GemmProblem& p, const GemmKArgs& ka, const 
     switch (tt_width(p)) {
         case 128: return dispatch_tt<128>(p, ka, a0, a1, a2, x, s);
         case 192: return dispatch_tt<192>(p, ka, a0, a1, a2, x, s);
+        case 240: return dispatch_tt<240>(p, ka, a0, a1, a2, x, s);
         default: return dispatch_tt<256>(p, ka, a0, a1, a2, x, s);
     }
 }

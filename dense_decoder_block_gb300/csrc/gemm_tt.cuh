@@ -3,7 +3,8 @@
 // Same arithmetic as the weight-streaming kernel (gemm_ws.cuh): per output, one
 // tcgen05.mma chain per K-segment of seg_kb k-blocks, segment results added in
 // ascending fp32 order.  Here one CTA per SM walks output tiles of 128 features
-// x BN tokens (BN = 256; 128 with the gate/up pair); for every tile it runs the
+// x BN tokens (BN = 256, 240, 192 or 128 as the host picks; 128 with the gate/up
+// pair); for every tile it runs the
 // segments' chains into two alternating TMEM buffers while sixteen epilogue
 // warps (four per TMEM lane quarter, each owning a quarter of the columns) keep
 // the running sums in registers; after a tile's last segment they apply the
@@ -39,16 +40,21 @@ struct TtCfg {
     static constexpr int STAGE_BYTES = NACC * kABytes + B_BYTES;
     static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
-    static constexpr int ACC_COLS = NACC * BN;                 // one TMEM buffer
+    // TMEM columns per accumulator and the epilogue's column split: a 240-token tile
+    // keeps the 256-column layout (its MMA writes columns 0..239; the last column
+    // group's threads store 48 of their 64)
+    static constexpr int NCOLS = BN == 240 ? 256 : BN;
+    static constexpr int ACC_COLS = NACC * NCOLS;              // one TMEM buffer
     static constexpr int TMEM_COLS = 512;                      // two buffers
     static constexpr int EPI_WARPS = 16;
-    static constexpr int CPT = BN / 4;                         // columns per thread per accumulator
+    static constexpr int CPT = NCOLS / 4;                      // columns per thread per accumulator
     static constexpr int THREADS = 128 + 32 * EPI_WARPS;       // warpgroup 0 + four epilogue warpgroups
     static constexpr int REGS_CTRL = 56;                       // warpgroup 0 after the split
     static constexpr int REGS_EPI = 104;                       // epilogue warpgroups after the split
     static constexpr int REGS_NEEDED = 128 * REGS_CTRL + 32 * EPI_WARPS * REGS_EPI;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
     static_assert(2 * ACC_COLS <= 512, "two TMEM buffers");
+    static_assert(BN % 16 == 0 && BN <= NCOLS && NCOLS % 64 == 0, "MMA N and the epilogue's 16-column loads");
 };
 
 template <int BN, bool DUAL, int EPI>
@@ -253,7 +259,8 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < CPT / CH; ++c) {
                         float tmp[CH];
-                        ptx::tmem_ld<CH>(tmem_base + lane_addr + buf * C::ACC_COLS + ac * BN + cg * CPT + c * CH, tmp);
+                        ptx::tmem_ld<CH>(tmem_base + lane_addr + buf * C::ACC_COLS + ac * C::NCOLS + cg * CPT + c * CH,
+                                         tmp);
                         ptx::tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < CH; ++j) acc[ac][c * CH + j] = __fadd_rn(acc[ac][c * CH + j], tmp[j]);
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                     float* dst = a.partial + ((size_t)wseg * a.M + n0) * a.F + f;
 #pragma unroll
                     for (int j = 0; j < CPT; ++j)
-                        if (n0 + j < a.M) dst[(size_t)j * a.F] = acc[0][j];
+                        if (n0 + j < a.M && cg * CPT + j < BN) dst[(size_t)j * a.F] = acc[0][j];
                 }
             } else if (ok) {
                 if constexpr (DUAL) {
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(TtCfg<BN, DUAL>::THREADS, 1)
                     const int tok = n * BN + row;
                     if (tok < a.M) epi_swiglu_row<CPT>(a.e.out + (size_t)tok * a.F + m * kTileF + cg * CPT, acc[0], acc[1]);
                 } else {
-                    epi_store_cols<EPI, CPT>(a, m, row, n * BN + cg * CPT, acc[0], acc[NACC - 1]);
+                    epi_store_cols<EPI, CPT>(a, m, row, n * BN + cg * CPT, acc[0], acc[NACC - 1], BN - cg * CPT);
                 }
             }
         }
