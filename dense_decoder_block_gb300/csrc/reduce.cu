@@ -10,6 +10,8 @@
 //   swiglu: u = bf16(bf16(silu(bf16(gate))) * bf16(up))
 //   resid + RMSNorm: h as resid, then hn = RMSNorm(h) with the 256-thread tree
 // All loads of one output are issued before its additions (one round trip).
+#include <algorithm>
+
 #include "internal.h"
 #include "reduce_epi.cuh"
 
@@ -37,22 +39,37 @@ __device__ __forceinline__ unsigned long long griddep() {
 // The residual of each reduction is produced at least two launches earlier (the
 // block input, or h four launches before the last reduction).
 
-// At most 48 registers (five CTAs' worth per SM): two of its CTAs fit beside a
-// CTA of the QKV projection, so all of them start while the projection runs and
-// the attention kernel behind them can launch before the projection ends.
-__global__ void __launch_bounds__(kThreads, 5) k_reduce_qkv(const ReduceArgs r) {
+// 320 threads of at most 48 registers (15,360 per CTA), one item per thread and a
+// grid of at most one CTA per SM (threads loop over the items beyond 320 per SM):
+// every CTA fits beside a CTA of the QKV projection, so all of them start while the
+// projection runs and the attention kernel behind them launches before the
+// projection ends, and an attention CTA (192 threads x 256 registers, 49,152) fits
+// beside the one reduction CTA of an SM, so the attention streams its older K/V
+// chunks while the reduction runs.
+constexpr int kQkvThreads = 320;
+
+__global__ void __launch_bounds__(kQkvThreads, 4) k_reduce_qkv(const ReduceArgs r) {
     TRACE(const unsigned long long tr0 = trace_stamp();)
     const int F4 = r.F / 4;
-    const int idx = blockIdx.x * kThreads + threadIdx.x;
-    const bool live = idx < r.M * F4;
-    const int n = live ? idx / F4 : 0, f0 = live ? (idx - n * F4) * 4 : 0;
+    const int n_items = r.M * F4;
+    int idx = blockIdx.x * kQkvThreads + threadIdx.x;
+    bool live = idx < n_items;
+    int n = live ? idx / F4 : 0, f0 = live ? (idx - n * F4) * 4 : 0;
     Qkv4 p{};
     if (live) p = epi4_qkv_prepare(r.e, n, f0);
     TRACE(const unsigned long long tr1 =) griddep();
-    if (!live) return;
-    float4 s, unused;
-    seg_sum4<false, 4>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
-    epi4_qkv_apply(p, s);
+    while (live) {
+        float4 s, unused;
+        seg_sum4<false, 4>(r.partial, (size_t)r.M * r.F, r.n_segs, (size_t)n * r.F + f0, 0, s, unused);
+        epi4_qkv_apply(p, s);
+        idx += gridDim.x * kQkvThreads;
+        live = idx < n_items;
+        if (live) {
+            n = idx / F4;
+            f0 = (idx - n * F4) * 4;
+            p = epi4_qkv_prepare(r.e, n, f0);
+        }
+    }
     TRACE(trace_cta(TR_REDUCE_QKV, tr0, tr1);)
 }
 
@@ -171,6 +188,10 @@ cudaError_t launch_reduce(const ReduceArgs& r, int kind, cudaStream_t s) {
     if (!kern) return cudaErrorInvalidValue;
     cudaError_t e = kernel_setup_once((const void*)kern, setup_prefer_shared);
     if (e != cudaSuccess) return e;
+    if (kind == EPI_QKV) {   // one item per thread, at most one CTA per SM
+        const long need = ((long)r.M * (r.F / 4) + kQkvThreads - 1) / kQkvThreads;
+        return launch_pdl(kern, dim3((unsigned)std::min(need, (long)device_sm_count())), dim3(kQkvThreads), 0, s, r);
+    }
     return launch_pdl(kern, grid4(r), dim3(kThreads), 0, s, r);
 }
 
