@@ -462,8 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ----------------------------------------------------------------------------- prefill
 // Pipelined prefill attention.  Same unit (one 128-row query tile of a KV group,
 // its chunks in ascending order) and the same arithmetic as above, split over
-// roles that overlap:
-//   warp 0       TMA: the Q tile once, then K chunks through a two-stage ring
+// roles that overlap.  The kernel is persistent (at most one CTA per SM, each
+// walking its tiles in turn) and every role counts the chunks of all its CTA's
+// tiles in one sequence, so one tile's first copies and S MMAs overlap the
+// previous tile's last softmax, fold and output store:
+//   warp 0       TMA: each tile's Q (two buffers, the next tile's loading while
+//                this one's S MMAs run), then its K chunks through a two-stage ring
 //   warp 2       TMA: V chunks through a two-stage ring (K(i+2) loads once S(i)
 //                has read K(i); V(i+2) once PV(i) has read V(i))
 //   warp 1       TMEM owner + MMA: PV(i) into O_c with P read from TMEM, then
@@ -489,8 +493,8 @@ constexpr int kPfRegsSoftmax = 112;
 constexpr int kPfRegsFold = 232;
 constexpr int kPfRegsNeeded = 128 * kPfRegsCtrl + 256 * kPfRegsSoftmax + 128 * kPfRegsFold;
 static_assert(kPfRegsNeeded <= 128 * kPfThreads, "register split exceeds the launch allocation");
-constexpr int PF_OFF_Q = 0;                          // Q: 2 sub-tiles
-constexpr int PF_OFF_K = 2 * kSub;                   // [stage] K: 2 sub-tiles
+constexpr int PF_OFF_Q = 0;                          // [buffer] Q: 2 sub-tiles
+constexpr int PF_OFF_K = 4 * kSub;                   // [stage] K: 2 sub-tiles
 constexpr int PF_OFF_V = PF_OFF_K + 4 * kSub;        // [stage] V: 2 sub-tiles
 constexpr int PF_OFF_BAR = PF_OFF_V + 4 * kSub;
 constexpr int PF_OFF_XCH = PF_OFF_BAR + 256;         // softmax halves' exchange: 4 x 128 floats
@@ -588,6 +592,33 @@ __device__ __forceinline__ void softmax_half_tmem(uint32_t s_taddr, int h, int r
     m_out = m;
 }
 
+// The tiles of a launch: tile L is KV group bg = L % n_bg (sequence bg / n_kv_heads,
+// KV head bg % n_kv_heads) and query tile y = L / n_bg counted from the last, so
+// lower L are longer (causal: later tokens see more chunks).  CTA c takes its
+// tiles in rounds, c in round 0, then from the other end of the next round
+// (G - 1 - c), and so on (snake order): every pair of rounds gives each CTA a long
+// tile and a short one.
+struct PfTile {
+    int b, g, t0, t_last, kv_last, n_iter;
+};
+__device__ __forceinline__ int pf_tile_index(int j, int n_ctas) {
+    const int c = (j & 1) ? (n_ctas - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    return j * n_ctas + c;
+}
+__device__ __forceinline__ PfTile pf_tile(const TcArgs& a, int L, int base) {
+    const int n_bg = a.batch * a.n_kv_heads;
+    const int n_qt = (a.tokens + a.tq - 1) / a.tq;
+    const int bg = L % n_bg, y = L / n_bg;
+    PfTile t;
+    t.g = bg % a.n_kv_heads;
+    t.b = bg / a.n_kv_heads;
+    t.t0 = (n_qt - 1 - y) * a.tq;
+    t.t_last = min(t.t0 + a.tq, a.tokens) - 1;
+    t.kv_last = base + t.t_last;
+    t.n_iter = t.kv_last / kAttnChunk + 1;
+    return t;
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1)
     k_attn_pf(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
               const __grid_constant__ CUtensorMap mV, const TcArgs a) {
@@ -595,40 +626,41 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(sm + PF_OFF_BAR);
-    uint64_t* q_full = bars + 0;
-    uint64_t* k_full = bars + 1;     // [2] TMA -> MMA
-    uint64_t* k_empty = bars + 3;    // [2] MMA (after S) -> TMA
-    uint64_t* v_full = bars + 5;     // [2] TMA -> MMA (and the softmax, before it zeroes rows)
-    uint64_t* v_empty = bars + 7;    // [2] MMA (after PV) -> TMA
-    uint64_t* s_full = bars + 9;     // [3] MMA (after S) -> softmax
-    uint64_t* p_full = bars + 12;    // [3] softmax (P, m, l written) -> MMA, fold
-    uint64_t* s_free = bars + 15;    // [3] fold (m, l read) -> MMA
-    uint64_t* oc_full = bars + 18;   // MMA (after PV) -> fold
-    uint64_t* oc_free = bars + 19;   // fold (O_c read) -> MMA
-    uint32_t* tmem_holder = (uint32_t*)(bars + 20);
+    uint64_t* q_full = bars + 0;     // [2] TMA -> MMA (the Q tile of this CTA's tile j in buffer j % 2)
+    uint64_t* q_empty = bars + 2;    // [2] MMA (after the tile's last S) -> TMA
+    uint64_t* k_full = bars + 4;     // [2] TMA -> MMA
+    uint64_t* k_empty = bars + 6;    // [2] MMA (after S) -> TMA
+    uint64_t* v_full = bars + 8;     // [2] TMA -> MMA (and the softmax, before it zeroes rows)
+    uint64_t* v_empty = bars + 10;   // [2] MMA (after PV) -> TMA
+    uint64_t* s_full = bars + 12;    // [3] MMA (after S) -> softmax
+    uint64_t* p_full = bars + 15;    // [3] softmax (P, m, l written) -> MMA, fold
+    uint64_t* s_free = bars + 18;    // [3] fold (m, l read) -> MMA
+    uint64_t* oc_full = bars + 21;   // MMA (after PV) -> fold
+    uint64_t* oc_free = bars + 22;   // fold (O_c read) -> MMA
+    uint32_t* tmem_holder = (uint32_t*)(bars + 23);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_wait();   // q and the cache rows come from the projection kernels
     TRACE(const unsigned long long tr1 = trace_stamp();)
 
-    // blockIdx.x = (sequence, KV head), blockIdx.y = query tile from the last: CTAs are
-    // dispatched in linear order, so every group's longest tiles go first
-    const int g = blockIdx.x % a.n_kv_heads, b = blockIdx.x / a.n_kv_heads;
+    // Persistent: this CTA walks tiles j = 0, 1, ... (pf_tile_index) while in range.
+    // Every ring and buffer below counts the chunks of all its tiles in one sequence
+    // (gi), so a tile's first loads and S MMAs go out while the previous tile's last
+    // chunks are still in the softmax and the fold.
     const int n_rep = a.n_heads / a.n_kv_heads;
     const int base = a.pos_dev ? *a.pos_dev : a.start_pos;
-    const int t0 = (gridDim.y - 1 - blockIdx.y) * a.tq;
-    const int t_last = min(t0 + a.tq, a.tokens) - 1;
-    if (base < 0 || base + t_last >= a.max_pos) {
-        if (threadIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
+    if (base < 0 || base + a.tokens - 1 >= a.max_pos) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) record_error(a.err, LLAMA_ERR_POS_RANGE);
         return;
     }
-    const int kv_last = base + t_last;
-    const int n_iter = kv_last / kAttnChunk + 1;
+    const int n_tiles = a.batch * a.n_kv_heads * ((a.tokens + a.tq - 1) / a.tq);
+    const int G = gridDim.x;
     int* err = a.err;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(q_full, 1);
         for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&q_full[i], 1);
+            ptx::mbar_init(&q_empty[i], 1);
             ptx::mbar_init(&k_full[i], 1);
             ptx::mbar_init(&k_empty[i], 1);
             ptx::mbar_init(&v_full[i], 1);
@@ -666,67 +698,95 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 uint64_t* empty = is_k ? k_empty : v_empty;
                 uint8_t* ring = sm + (is_k ? PF_OFF_K : PF_OFF_V);
                 ptx::prefetch_tmap(map);
-                if (is_k) {
-                    ptx::prefetch_tmap(&mQ);
-                    ptx::mbar_arrive_expect_tx(q_full, 2 * kSub);
-                    for (int half = 0; half < 2; ++half)
-                        asm volatile(
-                            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(ptx::smem_u32(sm + PF_OFF_Q + half * kSub)),
-                            "l"(reinterpret_cast<uint64_t>(&mQ)), "r"(ptx::smem_u32(q_full)), "r"(half * 64),
-                            "r"(g * n_rep), "r"(b * a.tokens + t0)
-                            : "memory");
-                }
-                const int head_row0 = (b * a.n_kv_heads + g) * a.kv_seq;
-                int issued = 0;
-                for (int i = 0; i < n_iter; ++i, ++issued) {
-                    const int st = i & 1;
-                    if (i >= 2 && !ptx::mbar_wait(&empty[st], ((i >> 1) & 1) ^ 1, err)) break;
-                    uint8_t* dst = ring + st * 2 * kSub;
-                    const int row = head_row0 + i * kAttnChunk;
-                    ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
-                    ptx::tma_load_2d(dst, map, &full[st], 0, row);
-                    ptx::tma_load_2d(dst + kSub, map, &full[st], 64, row);
+                if (is_k) ptx::prefetch_tmap(&mQ);
+                int gi = 0, n_q = 0;   // chunks and Q tiles issued
+                bool ok = true;
+                for (int j = 0; ok; ++j) {
+                    const int L = pf_tile_index(j, G);
+                    if (L >= n_tiles) break;
+                    const PfTile t = pf_tile(a, L, base);
+                    if (is_k) {
+                        // Q of tile j into buffer j % 2 once tile j - 2's S MMAs are done with it
+                        const int qb = j & 1;
+                        if (j >= 2 && !ptx::mbar_wait(&q_empty[qb], ((j >> 1) - 1) & 1, err)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&q_full[qb], 2 * kSub);
+                        for (int half = 0; half < 2; ++half)
+                            asm volatile(
+                                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+                                    ptx::smem_u32(sm + PF_OFF_Q + qb * 2 * kSub + half * kSub)),
+                                "l"(reinterpret_cast<uint64_t>(&mQ)), "r"(ptx::smem_u32(&q_full[qb])), "r"(half * 64),
+                                "r"(t.g * n_rep), "r"(t.b * a.tokens + t.t0)
+                                : "memory");
+                        ++n_q;
+                    }
+                    const int head_row0 = (t.b * a.n_kv_heads + t.g) * a.kv_seq;
+                    for (int i = 0; i < t.n_iter; ++i, ++gi) {
+                        const int st = gi & 1;
+                        if (gi >= 2 && !ptx::mbar_wait(&empty[st], ((gi >> 1) & 1) ^ 1, err)) { ok = false; break; }
+                        uint8_t* dst = ring + st * 2 * kSub;
+                        const int row = head_row0 + i * kAttnChunk;
+                        ptx::mbar_arrive_expect_tx(&full[st], 2 * kSub);
+                        ptx::tma_load_2d(dst, map, &full[st], 0, row);
+                        ptx::tma_load_2d(dst + kSub, map, &full[st], 64, row);
+                    }
                 }
                 // no copy may still be landing when the CTA exits (it has landed already
                 // unless a wait above gave up)
-                if (is_k) ptx::mbar_wait_drain(q_full, 0);
-                for (int i = max(0, issued - 2); i < issued; ++i) ptx::mbar_wait_drain(&full[i & 1], (i >> 1) & 1);
+                for (int j = max(0, n_q - 2); j < n_q; ++j) ptx::mbar_wait_drain(&q_full[j & 1], (j >> 1) & 1);
+                for (int i = max(0, gi - 2); i < gi; ++i) ptx::mbar_wait_drain(&full[i & 1], (i >> 1) & 1);
             }
         } else if (warp == 1) {
             // ------------------------------------------------------------------ MMA issuer
             if (lane == 0) {
-                const uint64_t q_desc = ptx::sw128_kmajor_desc(ptx::smem_u32(sm + PF_OFF_Q));
-                // S(i) into S[i % 3]: K(i) landed, and the fold has read chunk i - 3's (m, l)
-                // from that buffer (PV(i - 3), which read its P, was issued before and the
-                // MMAs run in issue order)
-                auto issue_s = [&](int i) -> bool {
-                    const int k = i & 1, sb = i % kPfSBufs;
-                    if (!ptx::mbar_wait(&k_full[k], (i >> 1) & 1, err)) return false;
-                    if (i >= kPfSBufs && !ptx::mbar_wait(&s_free[sb], ((i / kPfSBufs) & 1) ^ 1, err)) return false;
+                int n_total = 0;   // chunks of all this CTA's tiles
+                for (int j = 0;; ++j) {
+                    const int L = pf_tile_index(j, G);
+                    if (L >= n_tiles) break;
+                    n_total += pf_tile(a, L, base).n_iter;
+                }
+                // S(gi) into S[gi % 3]: Q of its tile landed (at the tile's first chunk),
+                // K(gi) landed, and the fold has read chunk gi - 3's (m, l) from that buffer
+                // (PV(gi - 3), which read its P, was issued before and the MMAs run in issue
+                // order).  After a tile's last S its Q buffer is released.
+                int s_j = 0, s_i = 0, s_n = 0;   // tile and chunk of the next S
+                if (n_total > 0) s_n = pf_tile(a, pf_tile_index(0, G), base).n_iter;
+                auto issue_s = [&](int gi) -> bool {
+                    const int k = gi & 1, sb = gi % kPfSBufs, qb = s_j & 1;
+                    if (s_i == 0 && !ptx::mbar_wait(&q_full[qb], (s_j >> 1) & 1, err)) return false;
+                    if (!ptx::mbar_wait(&k_full[k], (gi >> 1) & 1, err)) return false;
+                    if (gi >= kPfSBufs && !ptx::mbar_wait(&s_free[sb], ((gi / kPfSBufs) & 1) ^ 1, err)) return false;
                     ptx::tc_fence_after();
+                    const uint64_t q_desc = ptx::sw128_kmajor_desc(ptx::smem_u32(sm + PF_OFF_Q + qb * 2 * kSub));
                     const uint32_t k_addr = ptx::smem_u32(sm + PF_OFF_K + k * 2 * kSub);
                     umma8_ss<kSub / 16, kSub / 16, false>(tmem + PF_TM_S + sb * 128, q_desc,
                                                           ptx::sw128_kmajor_desc(k_addr), IDESC_S);
                     ptx::umma_commit(&s_full[sb]);
                     ptx::umma_commit(&k_empty[k]);
+                    if (++s_i == s_n) {
+                        ptx::umma_commit(&q_empty[qb]);
+                        ++s_j;
+                        s_i = 0;
+                        const int L = pf_tile_index(s_j, G);
+                        s_n = L < n_tiles ? pf_tile(a, L, base).n_iter : 0;
+                    }
                     return true;
                 };
-                bool ok = ptx::mbar_wait(q_full, 0, err);
-                for (int i = 0; i < kPfSBufs && i < n_iter && ok; ++i) ok = issue_s(i);
-                for (int i = 0; i < n_iter && ok; ++i) {
-                    const int k = i & 1, sb = i % kPfSBufs;
-                    if (!ptx::mbar_wait(&p_full[sb], (i / kPfSBufs) & 1, err)) break;
-                    // O_c is overwritten once the fold has read chunk i - 1's
-                    if (i >= 1 && !ptx::mbar_wait(oc_free, (i - 1) & 1, err)) break;
-                    if (!ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err)) break;
+                bool ok = true;
+                for (int gi = 0; gi < kPfSBufs && gi < n_total && ok; ++gi) ok = issue_s(gi);
+                for (int gi = 0; gi < n_total && ok; ++gi) {
+                    const int k = gi & 1, sb = gi % kPfSBufs;
+                    if (!ptx::mbar_wait(&p_full[sb], (gi / kPfSBufs) & 1, err)) break;
+                    // O_c is overwritten once the fold has read chunk gi - 1's
+                    if (gi >= 1 && !ptx::mbar_wait(oc_free, (gi - 1) & 1, err)) break;
+                    if (!ptx::mbar_wait(&v_full[k], (gi >> 1) & 1, err)) break;
                     ptx::tc_fence_after();
                     const uint32_t v_addr = ptx::smem_u32(sm + PF_OFF_V + k * 2 * kSub);
                     // P of keys 16ks.. in TMEM columns 8ks.., V rows 16ks..
                     umma8_ts(tmem + PF_TM_OC, tmem + PF_TM_S + sb * 128, ptx::sw128_mnmajor_desc(v_addr, kSub), IDESC_PV);
                     ptx::umma_commit(oc_full);
                     ptx::umma_commit(&v_empty[k]);
-                    if (i + kPfSBufs < n_iter) ok = issue_s(i + kPfSBufs);
+                    if (gi + kPfSBufs < n_total) ok = issue_s(gi + kPfSBufs);
                 }
             }
         }
@@ -738,38 +798,45 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int t_local = row / n_rep;
-        const bool valid = (t_local < a.tq) && (t0 + t_local < a.tokens);
-        const int pos_r = base + t0 + t_local;
         float* xch = reinterpret_cast<float*>(sm + PF_OFF_XCH);
         bool ok = true;
-        for (int i = 0; i < n_iter; ++i) {
-            const int k = i & 1, sb = i % kPfSBufs;
-            // s_full(i) also means PV(i - 3) -- issued before S(i) -- is done with the P in S[sb]
-            if (ok) ok = ptx::mbar_wait(&s_full[sb], (i / kPfSBufs) & 1, err);
-            ptx::tc_fence_after();
-            const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
-            float m;
-            // both halves reach the two barriers inside on every chunk, whatever `ok` says
-            softmax_half_tmem(tmem + lane_addr + PF_TM_S + sb * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter, m);
-            if (h == 0) {
-                // value rows past the last visible key of this tile are zeroed (they may hold
-                // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
-                // the chunk's V has landed
-                if (i * kAttnChunk + kAttnChunk - 1 > kv_last && ok)
-                    ok = ptx::mbar_wait(&v_full[k], (i >> 1) & 1, err);
-                if (i * kAttnChunk + row > kv_last) {
-                    uint8_t* vrow = sm + PF_OFF_V + k * 2 * kSub + row * 128;
+        int gi = 0;
+        for (int j = 0;; ++j) {
+            const int L = pf_tile_index(j, G);
+            if (L >= n_tiles) break;
+            const PfTile t = pf_tile(a, L, base);
+            const bool valid = (t_local < a.tq) && (t.t0 + t_local < a.tokens);
+            const int pos_r = base + t.t0 + t_local;
+            for (int i = 0; i < t.n_iter; ++i, ++gi) {
+                const int k = gi & 1, sb = gi % kPfSBufs;
+                // s_full(gi) also means PV(gi - 3) -- issued before S(gi) -- is done with the P in S[sb]
+                if (ok) ok = ptx::mbar_wait(&s_full[sb], (gi / kPfSBufs) & 1, err);
+                ptx::tc_fence_after();
+                const int jmax = valid ? min(kAttnChunk - 1, pos_r - i * kAttnChunk) : -1;
+                float m;
+                // both halves reach the two barriers inside on every chunk, whatever `ok` says
+                softmax_half_tmem(tmem + lane_addr + PF_TM_S + sb * 128, h, row, jmax, a.scale_log2, xch, 1 + quarter,
+                                  m);
+                if (h == 0) {
+                    // value rows past the last visible key of this tile are zeroed (they may hold
+                    // anything, including NaN; P is 0 there and 0 * NaN would poison O), once
+                    // the chunk's V has landed
+                    if (i * kAttnChunk + kAttnChunk - 1 > t.kv_last && ok)
+                        ok = ptx::mbar_wait(&v_full[k], (gi >> 1) & 1, err);
+                    if (i * kAttnChunk + row > t.kv_last) {
+                        uint8_t* vrow = sm + PF_OFF_V + k * 2 * kSub + row * 128;
 #pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(vrow + kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+                        for (int c16 = 0; c16 < 8; ++c16) {
+                            *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(vrow + kSub + c16 * 16) = make_uint4(0, 0, 0, 0);
+                        }
                     }
+                    ptx::fence_proxy_async_smem();
                 }
-                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&p_full[sb]);
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&p_full[sb]);
         }
     } else {
         // ------------------------------------------------------------------ fold + output
@@ -778,80 +845,88 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const int t_local = row / n_rep, h_local = row - t_local * n_rep;
-        const bool valid = (t_local < a.tq) && (t0 + t_local < a.tokens);
         float O[128];
-        float M = -INFINITY, L = 0.f;
-        bool started = false, ok = true;
+        bool ok = true;
+        int gi = 0;
+        for (int j = 0;; ++j) {
+            const int L = pf_tile_index(j, G);
+            if (L >= n_tiles) break;
+            const PfTile t = pf_tile(a, L, base);
+            const bool valid = (t_local < a.tq) && (t.t0 + t_local < a.tokens);
+            float M = -INFINITY, L_sum = 0.f;
+            bool started = false;
 #pragma unroll 1
-        for (int i = 0; i < n_iter; ++i) {
-            const int sb = i % kPfSBufs;
-            if (ok) ok = ptx::mbar_wait(&p_full[sb], (i / kPfSBufs) & 1, err);
-            ptx::tc_fence_after();
-            float ml[2];
-            ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + sb * 128 + PF_TM_ML, ml);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s_free[sb]);
-            const float m = ml[0], l = ml[1];
-            if (ok) ok = ptx::mbar_wait(oc_full, i & 1, err);
-            ptx::tc_fence_after();
-            // Per row: skip a chunk with no visible key, start from the first one, fold the
-            // rest (the combine kernel's formula).  The TMEM loads are issued by the whole
-            // warp whatever each row does (they are warp-collective).
-            const bool use = (m != -INFINITY);
-            const bool fold = use && started;
-            float alpha = 1.f, beta = 0.f;
-            if (fold) {
-                const float Mn = fmaxf(M, m);
-                alpha = exp2f(__fsub_rn(M, Mn));
-                beta = exp2f(__fsub_rn(m, Mn));
-                L = __fmaf_rn(L, alpha, __fmul_rn(l, beta));
-                M = Mn;
-            } else if (use) {
-                M = m;
-                L = l;
-            }
-            const uint32_t oc_addr = tmem + lane_addr + PF_TM_OC;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                float oc[32];
-                ptx::tmem_ld<32>(oc_addr + cb * 32, oc);
+            for (int i = 0; i < t.n_iter; ++i, ++gi) {
+                const int sb = gi % kPfSBufs;
+                if (ok) ok = ptx::mbar_wait(&p_full[sb], (gi / kPfSBufs) & 1, err);
+                ptx::tc_fence_after();
+                float ml[2];
+                ptx::tmem_ld<2>(tmem + lane_addr + PF_TM_S + sb * 128 + PF_TM_ML, ml);
                 ptx::tmem_wait_ld();
-                if (cb == 3) {   // O_c fully read: PV(i + 1) may overwrite it
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(oc_free);
-                }
-                if (fold) {   // o = fma(o, alpha, oc * beta), two columns per instruction
-                    const uint64_t a2 = pack2(alpha, alpha), b2 = pack2(beta, beta);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        float& o0 = O[cb * 32 + j];
-                        float& o1 = O[cb * 32 + j + 1];
-                        unpack2(fma2(pack2(o0, o1), a2, mul2(pack2(oc[j], oc[j + 1]), b2)), o0, o1);
-                    }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&s_free[sb]);
+                const float m = ml[0], l = ml[1];
+                if (ok) ok = ptx::mbar_wait(oc_full, gi & 1, err);
+                ptx::tc_fence_after();
+                // Per row: skip a chunk with no visible key, start from the first one, fold the
+                // rest (the combine kernel's formula).  The TMEM loads are issued by the whole
+                // warp whatever each row does (they are warp-collective).
+                const bool use = (m != -INFINITY);
+                const bool fold = use && started;
+                float alpha = 1.f, beta = 0.f;
+                if (fold) {
+                    const float Mn = fmaxf(M, m);
+                    alpha = exp2f(__fsub_rn(M, Mn));
+                    beta = exp2f(__fsub_rn(m, Mn));
+                    L_sum = __fmaf_rn(L_sum, alpha, __fmul_rn(l, beta));
+                    M = Mn;
                 } else if (use) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) O[cb * 32 + j] = oc[j];
+                    M = m;
+                    L_sum = l;
                 }
+                const uint32_t oc_addr = tmem + lane_addr + PF_TM_OC;
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    float oc[32];
+                    ptx::tmem_ld<32>(oc_addr + cb * 32, oc);
+                    ptx::tmem_wait_ld();
+                    if (cb == 3) {   // O_c fully read: PV(gi + 1) may overwrite it
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(oc_free);
+                    }
+                    if (fold) {   // o = fma(o, alpha, oc * beta), two columns per instruction
+                        const uint64_t a2 = pack2(alpha, alpha), b2 = pack2(beta, beta);
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 2) {
+                            float& o0 = O[cb * 32 + jj];
+                            float& o1 = O[cb * 32 + jj + 1];
+                            unpack2(fma2(pack2(o0, o1), a2, mul2(pack2(oc[jj], oc[jj + 1]), b2)), o0, o1);
+                        }
+                    } else if (use) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) O[cb * 32 + jj] = oc[jj];
+                    }
+                }
+                started = started || use;
             }
-            started = started || use;
-        }
-        // o = O * (1 / L), rounded to bf16
-        if (valid && ok && started) {
-            const float inv_l = __frcp_rn(L);
-            bf16* dst = a.o + ((size_t)b * a.tokens + t0 + t_local) * a.n_heads * 128 + (size_t)(g * n_rep + h_local) * 128;
+            // o = O * (1 / L), rounded to bf16, while the next tile's chunks run
+            if (valid && ok && started) {
+                const float inv_l = __frcp_rn(L_sum);
+                bf16* dst = a.o + ((size_t)t.b * a.tokens + t.t0 + t_local) * a.n_heads * 128 +
+                            (size_t)(t.g * n_rep + h_local) * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
-                uint32_t packed[4];
+                for (int c8 = 0; c8 < 16; ++c8) {
+                    uint32_t packed[4];
 #pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    const __nv_bfloat162 v2 =
-                        __floats2bfloat162_rn(__fmul_rn(O[c8 * 8 + j], inv_l), __fmul_rn(O[c8 * 8 + j + 1], inv_l));
-                    packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
+                    for (int jj = 0; jj < 8; jj += 2) {
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(__fmul_rn(O[c8 * 8 + jj], inv_l),
+                                                                        __fmul_rn(O[c8 * 8 + jj + 1], inv_l));
+                        packed[jj >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
+                    }
+                    *reinterpret_cast<uint4*>(dst + c8 * 8) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 }
-                *reinterpret_cast<uint4*>(dst + c8 * 8) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
         }
     }
@@ -1348,9 +1423,10 @@ cudaError_t launch_attention_tc_prefill(const AttnArgs& a, cudaStream_t s) {
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM_BYTES);
     });
     if (r != cudaSuccess) return r;
-    const int n_tiles = (a.tokens + k.tq - 1) / k.tq;
-    if (n_tiles > 65535) return cudaErrorInvalidValue;
-    dim3 grid(a.n_kv_heads * a.batch, n_tiles);
+    // persistent: one CTA per SM at most, each walking its tiles
+    const long n_tiles = (long)a.n_kv_heads * a.batch * ((a.tokens + k.tq - 1) / k.tq);
+    if (n_tiles > INT32_MAX) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)std::min(n_tiles, (long)device_sm_count()));
     return launch_pdl(k_attn_pf, grid, dim3(kPfThreads), PF_SMEM_BYTES, s, mq, mk, mv, k);
 }
 
