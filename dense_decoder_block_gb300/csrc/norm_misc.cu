@@ -161,8 +161,11 @@ __global__ void k_rope_append_f32(const float* __restrict__ qr, const float* __r
 }
 
 // RoPE in place on bf16 rows of 128 (q rows, then the cache rows of k): one
-// thread per 8 elements (4 pairs) -- a 16-byte load, rope_rotate_elem on the bf16
-// values (the inputs the fused epilogue rotates), a 16-byte store.
+// thread per 8 elements (4 pairs) of kRopeRows rows of the same token -- the
+// rotation of those pairs read once from the tables, the rows' 16-byte loads
+// issued together, rope_rotate_elem on the bf16 values (the inputs the fused
+// epilogue rotates), 16-byte stores.
+constexpr int kRopeRows = 4;
 __global__ void __launch_bounds__(256) k_rope_inplace(bf16* __restrict__ q, bf16* __restrict__ kc, int M, int T,
                                                       int n_heads, int n_kv_heads, int kv_seq, int start_pos,
                                                       const int* pos_dev, int max_pos,
@@ -173,34 +176,49 @@ __global__ void __launch_bounds__(256) k_rope_inplace(bf16* __restrict__ q, bf16
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     TRACE(const unsigned long long tr1 = trace_stamp();)
-    const int per_tok = (n_heads + n_kv_heads) * 16;   // 16 eight-element groups per 128-wide row
+    const int n_rows = n_heads + n_kv_heads;                     // 128-wide rows per token
+    const int n_grp = (n_rows + kRopeRows - 1) / kRopeRows;      // row groups per token
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (long long)M * per_tok) return;
-    const int n = (int)(idx / per_tok), r = (int)(idx - (long long)n * per_tok);
-    const int head = r >> 4, g8 = r & 15;
+    if (idx >= (long long)M * n_grp * 16) return;
+    const int g8 = (int)(idx & 15);                              // 8-element group of the row
+    const long long rest = idx >> 4;
+    const int n = (int)(rest / n_grp), grp = (int)(rest - (long long)n * n_grp);
     const int b = n / T, t = n - b * T;
     const int pos = (pos_dev ? *pos_dev : start_pos) + t;
     if (pos < 0 || pos >= max_pos) {
         record_error(err, LLAMA_ERR_POS_RANGE);
         return;
     }
-    bf16* row = head < n_heads ? q + (size_t)n * n_heads * 128 + (size_t)head * 128
-                               : kc + (((size_t)b * n_kv_heads + (head - n_heads)) * kv_seq + pos) * 128;
-    uint4* p = reinterpret_cast<uint4*>(row + g8 * 8);
-    uint4 u = *p;
     const float4 c = *reinterpret_cast<const float4*>(cos_tab + (size_t)pos * kRopeMaxPairs + g8 * 4);
     const float4 sn = *reinterpret_cast<const float4*>(sin_tab + (size_t)pos * kRopeMaxPairs + g8 * 4);
     const float cv[4] = {c.x, c.y, c.z, c.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
-    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+    uint4* p[kRopeRows];
+    uint4 u[kRopeRows];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-        const float a0 = __low2float(pr), a1 = __high2float(pr);
-        const __nv_bfloat162 o = __floats2bfloat162_rn(rope_rotate_elem(a0, a1, cv[k], sv[k], false),
-                                                       rope_rotate_elem(a1, a0, cv[k], sv[k], true));
-        w[k] = *reinterpret_cast<const uint32_t*>(&o);
+    for (int r = 0; r < kRopeRows; ++r) {
+        const int head = grp * kRopeRows + r;
+        p[r] = nullptr;
+        if (head < n_rows) {
+            bf16* row = head < n_heads ? q + (size_t)n * n_heads * 128 + (size_t)head * 128
+                                       : kc + (((size_t)b * n_kv_heads + (head - n_heads)) * kv_seq + pos) * 128;
+            p[r] = reinterpret_cast<uint4*>(row + g8 * 8);
+            u[r] = *p[r];
+        }
     }
-    *p = u;
+#pragma unroll
+    for (int r = 0; r < kRopeRows; ++r) {
+        if (p[r] == nullptr) continue;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&u[r]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+            const float a0 = __low2float(pr), a1 = __high2float(pr);
+            const __nv_bfloat162 o = __floats2bfloat162_rn(rope_rotate_elem(a0, a1, cv[k], sv[k], false),
+                                                           rope_rotate_elem(a1, a0, cv[k], sv[k], true));
+            w[k] = *reinterpret_cast<const uint32_t*>(&o);
+        }
+        *p[r] = u[r];
+    }
     TRACE(trace_cta(TR_ROPE, tr0, tr1);)
 }
 
@@ -351,7 +369,7 @@ cudaError_t launch_rope_inplace(void* q, void* kc, int M, int T, int n_heads, in
                                 int start_pos, const int* pos_dev, int max_pos, const float* cos_tab,
                                 const float* sin_tab, int* err, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    const long long threads = (long long)M * (n_heads + n_kv_heads) * 16;
+    const long long threads = (long long)M * ((n_heads + n_kv_heads + kRopeRows - 1) / kRopeRows) * 16;
     const dim3 grid((unsigned)((threads + 255) / 256));
     return launch_small(k_rope_inplace, grid, dim3(256), s, (bf16*)q, (bf16*)kc, M, T, n_heads, n_kv_heads,
                       kv_seq, start_pos, pos_dev, max_pos, cos_tab, sin_tab, err);
